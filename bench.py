@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""MoE-layer forward throughput on GB300: one JSON line.
+
+Workload: the Mixtral-8x7B-shaped MoE layer (d_model 4096, 8 experts, top-2,
+SwiGLU d_ff 14336, bf16 weights and activations, float32 accumulation) on a
+batch of T = 4096 seeded synthetic tokens.  One step = one pass of the whole
+layer (router, top-k, softmax, dispatch, expert FFN, combine) over the batch.
+The weights (2.8 GB) are larger than L2, so no flush is needed between steps.
+
+Contract: W untimed warm-up steps, then exactly K steps timed with CUDA
+events on the launching stream, bracketed by a barrier and a device
+synchronize on both sides; the max over ranks is reported.  Under torchrun
+each rank runs its own replica on its own GPU over its own tokens (token
+parallel, no collective on the data path): weak scaling.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the CPU oracle (float64 numpy) on the host cores on
+a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+STAGES = ["router", "dispatch", "gather", "expert_up", "expert_down", "combine", "rmsnorm"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the decode-size sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def algorithmic(shape, T, counts):
+    """Algorithmic bytes and FLOPs of one layer call (active experts only)."""
+    d, f, E, k = shape.d_model, shape.d_ff, shape.n_experts, shape.top_k
+    s = 2 if shape.dtype == "bf16" else 4
+    active = int((counts > 0).sum())
+    return {
+        "active_experts": active,
+        "bytes": active * 3 * d * f * s + d * E * s + 2 * T * d * s + T * k * 8,
+        "flops": 2 * T * d * E + 6 * T * k * d * f,
+        # per kernel
+        "up_flops": 4 * T * k * d * f, "down_flops": 2 * T * k * d * f,
+        "up_bytes": active * 2 * d * f * s + T * d * s + T * k * f * s,
+        "down_bytes": active * d * f * s + T * k * f * s + T * k * d * 4,
+    }
+
+
+def source_sha(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+KERNEL_SOURCES = {
+    "grouped_gemm_tc<kGateUp>": ("sparse_expert_ffn_gb300/csrc/gemm_tc.cu",),
+    "grouped_gemm_tc<kDown>": ("sparse_expert_ffn_gb300/csrc/gemm_tc.cu",),
+    "ffn_up_stream": ("sparse_expert_ffn_gb300/csrc/ffn_stream.cu", "sparse_expert_ffn_gb300/csrc/common.cuh"),
+    "ffn_down_stream": ("sparse_expert_ffn_gb300/csrc/ffn_stream.cu", "sparse_expert_ffn_gb300/csrc/common.cuh"),
+}
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source.
+
+    A summary line reads:  traffic-per-launch: <kernel> <workload> bytes=<B> source-sha=<sha>
+    """
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir) or kernel not in KERNEL_SOURCES:
+        return None
+    sha = source_sha(*KERNEL_SOURCES[kernel])
+    pat = re.compile(r"traffic-per-launch:\s+(\S+)\s+(\S+)\s+bytes=(\d+)\s+source-sha=(\w+)")
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, fn)) as fh:
+            for line in fh:
+                m = pat.search(line)
+                if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == sha:
+                    return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.marks = {}
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100", "-i", gpu_id],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.p = None
+
+    def _read(self):
+        for line in self.p.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self):
+        if self.p:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self, start="timed_start", end="timed_end"):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        t0, t1 = self.marks.get(start, 0), self.marks.get(end, time.time())
+        win = [s for t, s in self.samples if t0 - 0.15 <= t <= t1 + 0.15] or [s for _, s in self.samples]
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in win if num(s[1]) is not None]
+        mx = [num(s[2]) for s in win if num(s[2]) is not None]
+        pw = [num(s[3]) for s in win if num(s[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i in range(4)
+                          if len(s) > 5 + i and s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(layer, x, y, steps, warmup, world, stream, profile=False):
+    """W warm-up steps, then K steps between CUDA events; returns (ms, per-stage dict)."""
+    import ctypes
+
+    import torch
+    import sparse_expert_ffn_gb300 as sef
+    for _ in range(warmup):
+        layer.forward(x, y)
+    torch.cuda.synchronize()
+    lib = sef.library()
+    if profile:
+        lib.colibri_profile_enable(layer.handle, 1)
+    n0 = layer.launch_count
+    barrier(world)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        layer.forward(x, y, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = a.elapsed_time(b)
+    launches = layer.launch_count - n0
+    stages = None
+    if profile:
+        tot = (ctypes.c_double * 7)()
+        cnt = (ctypes.c_uint64 * 7)()
+        lib.colibri_profile_read(layer.handle, tot, cnt)
+        lib.colibri_profile_enable(layer.handle, 0)
+        stages = {STAGES[i]: {"ms_total": tot[i], "launches": int(cnt[i])}
+                  for i in range(7) if cnt[i]}
+    assert layer.check() == 0, "device-side failure during the timed region"
+    return ms, launches, stages
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import sparse_expert_ffn_gb300 as sef
+    import synth
+
+    world, rank, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape, T = synth.MIXTRAL, args.tokens
+    pk = peaks()
+    props = torch.cuda.get_device_properties(dev)
+    uid = str(getattr(props, "uuid", "") or "")
+    gpu_id = (uid if uid.startswith("GPU-") else "GPU-" + uid) if uid else str(local)
+    clocks = ClockSampler(gpu_id) if rank == 0 else None
+
+    # weights: layer seed per rank (replicas over independent synthetic layers)
+    seed = args.seed + rank
+    wr = synth.router_weight(shape, seed, 0, dev)
+    wg, wu, wd = synth.expert_weights(shape, seed, 0, dev)
+    max_t = max(T, 128)
+    layer = sef.MoELayer(wr, wg, wu, wd, shape.top_k, max_tokens=max_t)
+    del wg, wu, wd
+    torch.cuda.empty_cache()
+    x = synth.tokens(shape, T, seed, 0, dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    if clocks:
+        clocks.mark("warm_start")
+    layer.forward(x, y)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark("timed_start")
+    ms, launches, stages = time_steps(layer, x, y, args.steps, args.warmup, world, stream, profile=True)
+    if clocks:
+        clocks.mark("timed_end")
+    ms = max_over_ranks(ms, world)
+    r = layer.routing()
+    counts = r["counts"].cpu().numpy()
+    alg = algorithmic(shape, T, counts)
+    step_ms = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+
+    # roofline of the dominant kernel (largest share of the timed region)
+    dom = max(stages, key=lambda s: stages[s]["ms_total"])
+    per_launch_s = stages[dom]["ms_total"] / stages[dom]["launches"] / 1e3
+    grouped = "gather" in stages
+    kname = {("expert_up", True): "grouped_gemm_tc<kGateUp>", ("expert_down", True): "grouped_gemm_tc<kDown>",
+             ("expert_up", False): "ffn_up_stream", ("expert_down", False): "ffn_down_stream"}.get(
+        (dom, grouped), dom)
+    workload = f"mixtral_T{T}"
+    if grouped and dom in ("expert_up", "expert_down"):
+        fl = alg["up_flops"] if dom == "expert_up" else alg["down_flops"]
+        achieved = fl / per_launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
+                "peak_kind": f"bf16 dense burst, {pk['source']}"}
+    else:
+        by = {"expert_up": alg["up_bytes"], "expert_down": alg["down_bytes"]}.get(dom, alg["bytes"])
+        achieved = by / per_launch_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": f"HBM copy, {pk['source']}"}
+    roof["kernel"] = kname
+    roof["share_of_step"] = round(stages[dom]["ms_total"] / sum(v["ms_total"] for v in stages.values()), 4)
+    roof["traffic"] = measured_traffic(kname, workload)
+    roof["algorithmic_per_launch"] = (alg["up_flops"] if dom == "expert_up" else alg["down_flops"]) \
+        if roof["bound"] == "tensor" else None
+
+    whole = {"roofline_time_us": round(1e6 * max(alg["bytes"] / (pk["hbm_gbs"] * 1e9),
+                                                 alg["flops"] / (pk["bf16_tflops"] * 1e12)), 1),
+             "step_us": round(step_ms * 1e3, 1)}
+    whole["frac"] = round(whole["roofline_time_us"] / whole["step_us"], 4)
+
+    # end to end through the public C API on pinned host buffers
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        layer.forward_host(xh, yh)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        layer.forward_host(xh, yh)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": round(world * T * e2e_steps / e2e_s, 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
+           "d2h_bytes_per_step": int(yh.numel() * yh.element_size())}
+
+    # decode-size sweep (context; the headline is the T above)
+    sweep = {}
+    if not args.no_sweep:
+        for Ts in (1, 16, 128):
+            xs = synth.tokens(shape, Ts, seed, 0, dev)
+            ys = torch.empty_like(xs)
+            ms_s, _, st_s = time_steps(layer, xs, ys, args.steps, args.warmup, world, stream, profile=True)
+            ms_s = max_over_ranks(ms_s, world)
+            cs = layer.routing()["counts"].cpu().numpy()
+            a_s = algorithmic(shape, Ts, cs)
+            t_step = ms_s / args.steps / 1e3
+            sweep[f"T{Ts}"] = {"tokens_per_s": round(world * Ts / t_step, 1),
+                               "us_per_step": round(t_step * 1e6, 1),
+                               "hbm_frac_of_measured": round(a_s["bytes"] / t_step / 1e9 / pk["hbm_gbs"], 4),
+                               "active_experts": a_s["active_experts"],
+                               "stages_us": {k: round(v["ms_total"] * 1e3 / args.steps, 1)
+                                             for k, v in st_s.items()}}
+    if clocks:
+        clocks.stop()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(shape, x, seed=seed, target_s=args.cpu_seconds)
+
+    out = {
+        "metric": "MoE-layer tokens/s at 1 GB300; % of HBM (decode) / bf16 TC (prefill) roofline",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"Mixtral-8x7B-shaped MoE layer, T={T} tokens",
+                   "d_model": shape.d_model, "d_ff": shape.d_ff, "n_experts": shape.n_experts,
+                   "top_k": shape.top_k, "tokens_per_gpu": T, "parallelism": f"token-parallel x{world}",
+                   "l2": "inputs larger than L2 (2.8 GB of expert weights per step)"},
+        "roofline": roof,
+        "layer_roofline": whole,
+        "stages_us_per_step": {k: round(v["ms_total"] * 1e3 / args.steps, 1) for k, v in stages.items()},
+        "active_experts": alg["active_experts"],
+        "gpu_launches": int(launches),
+        "e2e": e2e,
+        "clocks": clocks.summary() if clocks else None,
+        "cpu_baseline": cpu,
+        "sweep": sweep,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    layer.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+
+
+def _host_inputs(shape, T, seed):
+    """Workload inputs on the host: generated on the GPU when one is present
+    (the counter-based generator gives the same values either way)."""
+    import torch
+
+    import synth
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wr = synth.router_weight(shape, seed, 0, dev).cpu()
+    wg, wu, wd = synth.expert_weights(shape, seed, 0, dev)
+    wg, wu, wd = wg.cpu(), wu.cpu(), wd.cpu()
+    x = synth.tokens(shape, T, seed, 0, dev).cpu()
+    return x, wr, wg, wu, wd
+
+
+def _oracle_weights(wr, wg, wu, wd):
+    import oracle
+    return (oracle.to_f64(wr), oracle.to_f64(wg), oracle.to_f64(wu), oracle.to_f64(wd))
+
+
+def cpu_baseline(shape, x, seed=0, target_s=15.0):
+    """The oracle, as it stands, on a bounded sample of the workload's tokens."""
+    import numpy as np
+
+    import oracle
+    xh, wr, wg, wu, wd = _host_inputs(shape, x.shape[0], seed)
+    W = _oracle_weights(wr, wg, wu, wd)
+    del wg, wu, wd
+    x64 = oracle.to_f64(xh)
+    # calibrate on 16 tokens, then size the sample to ~target_s seconds
+    t0 = time.perf_counter()
+    oracle.moe_layer(x64[:16], *W, shape.top_k)
+    per_tok = (time.perf_counter() - t0) / 16
+    n = int(min(x64.shape[0], max(16, target_s / max(per_tok, 1e-9))))
+    t0 = time.perf_counter()
+    oracle.moe_layer(x64[:n], *W, shape.top_k)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of the {x64.shape[0]} tokens, whole layer (float64 numpy, BLAS "
+                      f"threads = all {cores} cores), {dt:.1f} s"}
+
+
+def run_reference(args):
+    import numpy as np
+
+    import oracle
+    import synth
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    shape, T = synth.MIXTRAL, args.tokens
+    xh, wr, wg, wu, wd = _host_inputs(shape, T, args.seed)
+    W = _oracle_weights(wr, wg, wu, wd)
+    del wg, wu, wd
+    x64 = oracle.to_f64(xh)
+    t0 = time.perf_counter()
+    oracle.moe_layer(x64[:8], *W, shape.top_k)
+    per_tok = (time.perf_counter() - t0) / 8
+    # each step: a bounded sample sized so that W + K steps take ~2 minutes
+    n = int(max(4, min(T, 120.0 / max(per_tok, 1e-9) / max(1, args.steps + args.warmup))))
+    for i in range(args.warmup):
+        oracle.moe_layer(x64[:n], *W, shape.top_k)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        lo = (i * n) % max(1, T - n)
+        oracle.moe_layer(x64[lo:lo + n], *W, shape.top_k)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = f"{n} tokens per step out of the T={T} batch, whole layer, float64 numpy"
+    out = {"impl": "reference",
+           "metric": "MoE-layer tokens/s at 1 GB300; % of HBM (decode) / bf16 TC (prefill) roofline",
+           "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": f"Mixtral-8x7B-shaped MoE layer, T={T} tokens",
+                      "d_model": shape.d_model, "d_ff": shape.d_ff, "n_experts": shape.n_experts,
+                      "top_k": shape.top_k, "tokens_per_gpu": T, "parallelism": "none (host CPU)"},
+           "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

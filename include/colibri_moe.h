@@ -1,0 +1,201 @@
+/*
+ * colibri_moe.h - C ABI of a GB300 (sm_103a) Mixture-of-Experts layer forward.
+ *
+ * One MoE layer:  router logits -> per-token top-k -> softmax over the k
+ * selected logits -> dispatch (pairs grouped by expert) -> per-expert SwiGLU
+ * FFN -> gate-weighted combine back into token order.
+ *
+ * The call shape (init / forward / free, status codes, caller-owned buffers)
+ * follows the engine the source pages describe: pnsm.cn section 4.4
+ * (colibri_init / colibri_forward / colibri_free), zskr.cn
+ * "Colibri：面向MoE架构的C语言高效推理引擎解析" section 4.2 (caller-owned input
+ * and output buffers, COLIBRI_ERR_INVALID_ARG), and pnsm.cn section 5.1
+ * (init that fails returns no handle).
+ *
+ * Conventions for every entry point:
+ *  - All pointers are plain addresses; nothing here is a framework type.
+ *  - "device" pointers are CUDA device (or managed) memory on the handle's
+ *    device; "host" pointers are ordinary host memory (pinned is faster).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Device work is ordered on it; unless stated, a call returns
+ *    without waiting for the device.
+ *  - A handle is not thread-safe: use one handle per concurrently running
+ *    stream.  Two forwards on one handle must be stream-ordered.
+ *  - Every call returns a colibri_status_t; argument checks run on the host
+ *    before any CUDA call, so an INVALID_ARG call has no side effect.
+ */
+#ifndef COLIBRI_MOE_H
+#define COLIBRI_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    COLIBRI_OK = 0,
+    COLIBRI_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, misalignment, aliasing */
+    COLIBRI_ERR_OOM = 2,          /* a device or pinned-host allocation failed (init only) */
+    COLIBRI_ERR_CUDA = 3,         /* a CUDA runtime/launch error; the stream may hold garbage */
+    COLIBRI_ERR_UNSUPPORTED = 4,  /* not an sm_103 device, or a shape this build cannot run */
+    COLIBRI_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up (see colibri_check) */
+} colibri_status_t;
+
+typedef enum {
+    COLIBRI_DTYPE_FP32 = 0,       /* activations and weights float32, float32 arithmetic */
+    COLIBRI_DTYPE_BF16 = 1        /* activations and weights bfloat16, float32 accumulation */
+} colibri_dtype_t;
+
+typedef enum {
+    COLIBRI_EXEC_AUTO = 0,        /* choose from T and the shapes */
+    COLIBRI_EXEC_STREAM = 1,      /* weight-streaming expert FFN on CUDA cores (decode sizes, fp32) */
+    COLIBRI_EXEC_GROUPED = 2      /* tcgen05 grouped GEMM expert FFN (bf16 only) */
+} colibri_executor_t;
+
+/* Layer shape.  d_model % 64 == 0 and d_ff % 128 == 0 are required
+ * (UNSUPPORTED otherwise); 1 <= top_k <= n_experts <= 256; top_k <= 8. */
+typedef struct {
+    int32_t n_experts;   /* E */
+    int32_t top_k;       /* k */
+    int32_t d_model;     /* d */
+    int32_t d_ff;        /* f, expert hidden size */
+    int32_t max_tokens;  /* largest T any later call may pass; sizes the workspace */
+    int32_t dtype;       /* colibri_dtype_t */
+    int32_t device;      /* CUDA device ordinal */
+    int32_t executor;    /* colibri_executor_t (can be changed with colibri_set_executor) */
+} colibri_moe_config_t;
+
+typedef struct colibri_moe colibri_moe_t;  /* opaque */
+
+/*
+ * colibri_init - build a layer handle: validate, copy and repack the weights
+ * into the device layout, and allocate the whole workspace for max_tokens.
+ *
+ * Defines the layer of zskr.cn section 3.1/3.3 (router W_r, per-expert
+ * gate_proj / up_proj / down_proj) in the row-major layouts:
+ *   w_router     [d_model, E]           dtype
+ *   router_bias  [E] float32 or NULL    added to the logits before top-k and
+ *                                       softmax; -INFINITY masks an expert.
+ *                                       Not a learned bias: a per-expert
+ *                                       offset (e.g. a load skew or a mask).
+ *   w_gate/w_up  [E, d_model, d_ff]     dtype  (x . W_gate[e] -> [T, d_ff])
+ *   w_down       [E, d_ff, d_model]     dtype
+ * weights_on_device: 0 = the five pointers are host memory, 1 = device.
+ * The caller keeps ownership of its arrays and may free them once init
+ * returns (init synchronises the device before returning).
+ * On any failure *out is set to NULL and everything allocated is freed.
+ */
+colibri_status_t colibri_init(const colibri_moe_config_t* cfg,
+                              const void* w_router, const float* router_bias,
+                              const void* w_gate, const void* w_up, const void* w_down,
+                              int weights_on_device, colibri_moe_t** out);
+
+/*
+ * colibri_forward - y = MoE(x) for T tokens (zskr.cn section 3.3 stages 2-5).
+ *   x  [T, d_model] device, dtype, 16-byte aligned, read only
+ *   y  [T, d_model] device, dtype, 16-byte aligned, written; must not overlap x
+ *   0 <= T <= max_tokens; T == 0 is a no-op.
+ * Allocates nothing and does not synchronise the host.  Routing results of
+ * the last forward stay in the workspace until the next call (see
+ * colibri_get_routing).
+ */
+colibri_status_t colibri_forward(colibri_moe_t* h, const void* x, int32_t T, void* y,
+                                 void* stream);
+
+/*
+ * colibri_forward_host - the same layer on host buffers: copies x to the
+ * device, runs colibri_forward, copies y back and waits for the stream.
+ *   x_host, y_host [T, d_model] host memory (pinned recommended), dtype.
+ * Uses the workspace's own device copies of x and y (no allocation).
+ */
+colibri_status_t colibri_forward_host(colibri_moe_t* h, const void* x_host, int32_t T,
+                                      void* y_host, void* stream);
+
+/*
+ * colibri_rmsnorm_moe_residual - one layer of a pre-norm decode stack
+ * (pnsm.cn section 2.2: residual around the MoE block):
+ *   u = bf16(RMSNorm(hidden) * gamma),  hidden <- bf16(hidden + MoE(u))
+ * RMSNorm(h) = h / sqrt(mean(h^2) + eps), in float32; the residual sum is
+ * formed in float32 from the float32 combine result and rounded once.
+ *   hidden [T, d_model] device, dtype, updated in place
+ *   gamma  [d_model] device, dtype
+ * Requires dtype BF16 or FP32 matching the handle; allocates nothing.
+ */
+colibri_status_t colibri_rmsnorm_moe_residual(colibri_moe_t* h, void* hidden, int32_t T,
+                                              const void* gamma, float eps, void* stream);
+
+/*
+ * colibri_get_routing - copy the last forward's routing decisions out
+ * (zskr.cn section 3.3 stage 2 outputs, and the stage 3 grouping):
+ *   topk_idx [T, k] int32   expert ids, descending logit, ties -> lower id
+ *   topk_w   [T, k] float32 softmax over the k selected logits
+ *   counts   [E]    int32   pairs per expert
+ *   perm     [T*k]  int32   perm[p] = t*k + j of the p-th pair in expert order
+ * All device pointers; any may be NULL to skip it.  Stream-ordered after the
+ * forward on the same stream.  T is the last forward's T.
+ */
+colibri_status_t colibri_get_routing(colibri_moe_t* h, int32_t* topk_idx, float* topk_w,
+                                     int32_t* counts, int32_t* perm, void* stream);
+
+/* colibri_set_executor - choose the expert executor for later forwards.
+ * GROUPED needs dtype BF16 (UNSUPPORTED otherwise). */
+colibri_status_t colibri_set_executor(colibri_moe_t* h, int32_t executor);
+
+/*
+ * colibri_check - wait for `stream`, then report the first failure of any
+ * earlier call on this handle: COLIBRI_ERR_CUDA for a CUDA error,
+ * COLIBRI_ERR_TIMEOUT when a bounded device-side wait (an mbarrier wait in the
+ * grouped GEMM) gave up.  Clears the recorded device status.
+ */
+colibri_status_t colibri_check(colibri_moe_t* h, void* stream);
+
+/* colibri_launch_count - kernels this handle has launched since init
+ * (counted on the host, one per kernel launch). */
+colibri_status_t colibri_launch_count(const colibri_moe_t* h, uint64_t* n);
+
+/* colibri_workspace_bytes - device bytes held by the handle (weights + workspace). */
+colibri_status_t colibri_workspace_bytes(const colibri_moe_t* h, uint64_t* weights,
+                                         uint64_t* workspace);
+
+/* Stages of one forward, for colibri_profile_read. */
+typedef enum {
+    COLIBRI_STAGE_ROUTER = 0,     /* logits + top-k + softmax */
+    COLIBRI_STAGE_DISPATCH = 1,   /* histogram, scan, permutation, tile list */
+    COLIBRI_STAGE_GATHER = 2,     /* token rows into expert order (grouped executor) */
+    COLIBRI_STAGE_EXPERT_UP = 3,  /* gate/up projection + SiLU * up */
+    COLIBRI_STAGE_EXPERT_DOWN = 4,/* down projection */
+    COLIBRI_STAGE_COMBINE = 5,    /* gate-weighted sum (+ residual) */
+    COLIBRI_STAGE_RMSNORM = 6,    /* stack layers only */
+    COLIBRI_NUM_STAGES = 7
+} colibri_stage_t;
+
+/*
+ * colibri_profile_enable - when enable != 0, every later forward records a
+ * CUDA event pair around each stage's kernel on the caller's stream (events
+ * come from a host-side pool; no device memory is allocated).  0 turns it
+ * off and drops what was recorded.
+ */
+colibri_status_t colibri_profile_enable(colibri_moe_t* h, int enable);
+
+/*
+ * colibri_profile_read - wait for the recorded events, then add each stage's
+ * total device time (milliseconds) and number of kernel launches since the
+ * last read into total_ms[COLIBRI_NUM_STAGES] and launches[COLIBRI_NUM_STAGES]
+ * (host arrays, overwritten), and clear the record.
+ */
+colibri_status_t colibri_profile_read(colibri_moe_t* h, double* total_ms, uint64_t* launches);
+
+/* colibri_free - release everything the handle holds; NULL is allowed.
+ * Synchronises the handle's device first. */
+void colibri_free(colibri_moe_t* h);
+
+/* colibri_status_str - a static, never-NULL description of a status. */
+const char* colibri_status_str(colibri_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COLIBRI_MOE_H */

@@ -1,0 +1,97 @@
+// Shared device helpers for the MoE layer kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace colibri {
+
+// Element types the layer runs in.
+enum class DType : int { F32 = 0, BF16 = 1 };
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Load 8 consecutive elements starting at p (16-byte aligned for bf16,
+// 32-byte aligned for float) and widen them to float.
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __bfloat1622float2(b[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Streaming (read-once) variants for weights: bypass L1 allocation.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+// 8 elements of a weight row as raw registers (bf16: one 16-byte vector,
+// float: two).
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+    uint4 a;
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) { a = ld_stream16(p); }
+    __device__ __forceinline__ float dot(const float (&x)[8]) const {
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&a);
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(b[i]);
+            s = fmaf(x[2 * i], f.x, s);
+            s = fmaf(x[2 * i + 1], f.y, s);
+        }
+        return s;
+    }
+};
+template <> struct Raw8<float> {
+    uint4 a, b;
+    __device__ __forceinline__ void load(const float* p) {
+        a = ld_stream16(p);
+        b = ld_stream16(p + 4);
+    }
+    __device__ __forceinline__ float dot(const float (&x)[8]) const {
+        float s = 0.f;
+        s = fmaf(x[0], __uint_as_float(a.x), s);
+        s = fmaf(x[1], __uint_as_float(a.y), s);
+        s = fmaf(x[2], __uint_as_float(a.z), s);
+        s = fmaf(x[3], __uint_as_float(a.w), s);
+        s = fmaf(x[4], __uint_as_float(b.x), s);
+        s = fmaf(x[5], __uint_as_float(b.y), s);
+        s = fmaf(x[6], __uint_as_float(b.z), s);
+        s = fmaf(x[7], __uint_as_float(b.w), s);
+        return s;
+    }
+};
+
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(float v) { return v; }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Device status word values (written by kernels, read by colibri_check).
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
+
+}  // namespace colibri

@@ -1,0 +1,154 @@
+// Weight-streaming expert SwiGLU FFN on CUDA cores (decode-sized batches and
+// the float32 layer).
+//
+// zskr.cn "Colibri：面向MoE架构的C语言高效推理引擎解析" section 3.3 stage 4
+// (per expert: gate_proj, up_proj, SiLU, down_proj).  With few tokens per
+// expert the FFN is a weight stream: every activated expert's weights are read
+// from HBM exactly once, experts with no token are skipped entirely.
+//
+//   ffn_up_stream    one warp per hidden unit n: the gate row and the up row
+//                    of W^T (K contiguous) are streamed in 16-byte vectors and
+//                    dotted with up to kSlots token rows at a time;
+//                    H[p, n] = silu(g) * u, rounded to the layer dtype.
+//   ffn_down_stream  one warp per output feature c: the row c of W_down^T
+//                    (contiguous over d_ff) dotted with the H rows of the
+//                    expert's pairs; Y[p, c] in float32.
+// Pairs p are in expert order (the dispatch permutation), so the tokens of
+// one expert are consecutive rows of H and Y.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace colibri {
+
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kSlots = 8;
+
+// Row of the packed gate/up weight: [E][f/128][2][128][d], which = 0 gate, 1 up.
+__device__ __forceinline__ size_t gu_row(int e, int n, int which, int f) {
+    return ((size_t)(e * (f / 128) + n / 128) * 2 + which) * 128 + (n % 128);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+ffn_up_stream(const T* __restrict__ x, const T* __restrict__ wgu,
+              const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+              const int32_t* __restrict__ perm, int k, int d, int f, int E, T* __restrict__ H) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = blockIdx.x * kWarps + warp;
+    if (n >= f) return;
+    for (int e = 0; e < E; ++e) {
+        const int c = counts[e];
+        if (c == 0) continue;
+        const int off = offsets[e];
+        const T* g_row = wgu + gu_row(e, n, 0, f) * d;
+        const T* u_row = wgu + gu_row(e, n, 1, f) * d;
+        for (int s0 = 0; s0 < c; s0 += kSlots) {
+            const int ns = min(kSlots, c - s0);
+            const T* xr[kSlots];
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s)
+                xr[s] = x + (size_t)(perm[off + s0 + (s < ns ? s : 0)] / k) * d;
+            float ag[kSlots], au[kSlots];
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) ag[s] = au[s] = 0.f;
+#pragma unroll 2
+            for (int i = lane * 8; i < d; i += 256) {
+                Raw8<T> wg, wu;
+                wg.load(g_row + i);
+                wu.load(u_row + i);
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s) {
+                    if (s < ns) {
+                        float xv[8];
+                        load8(xr[s] + i, xv);
+                        ag[s] += wg.dot(xv);
+                        au[s] += wu.dot(xv);
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) {
+                if (s < ns) {
+                    const float g = warp_sum(ag[s]);
+                    const float u = warp_sum(au[s]);
+                    if (lane == 0) H[(size_t)(off + s0 + s) * f + n] = from_f32<T>(silu(g) * u);
+                }
+            }
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+ffn_down_stream(const T* __restrict__ H, const T* __restrict__ wdT,
+                const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets, int d,
+                int f, int E, float* __restrict__ Y) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col = blockIdx.x * kWarps + warp;
+    if (col >= d) return;
+    for (int e = 0; e < E; ++e) {
+        const int c = counts[e];
+        if (c == 0) continue;
+        const int off = offsets[e];
+        const T* w_row = wdT + ((size_t)e * d + col) * f;
+        for (int s0 = 0; s0 < c; s0 += kSlots) {
+            const int ns = min(kSlots, c - s0);
+            float acc[kSlots];
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) acc[s] = 0.f;
+#pragma unroll 2
+            for (int i = lane * 8; i < f; i += 256) {
+                Raw8<T> w;
+                w.load(w_row + i);
+#pragma unroll
+                for (int s = 0; s < kSlots; ++s) {
+                    if (s < ns) {
+                        float hv[8];
+                        load8(H + (size_t)(off + s0 + s) * f + i, hv);
+                        acc[s] += w.dot(hv);
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) {
+                if (s < ns) {
+                    const float v = warp_sum(acc[s]);
+                    if (lane == 0) Y[(size_t)(off + s0 + s) * d + col] = v;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* counts,
+                                 const int32_t* offsets, const int32_t* perm, int k, int d, int f,
+                                 int E, void* H, cudaStream_t s) {
+    const dim3 block(kWarps * 32), grid((f + kWarps - 1) / kWarps);
+    if (dt == DType::BF16)
+        ffn_up_stream<__nv_bfloat16><<<grid, block, 0, s>>>(
+            (const __nv_bfloat16*)x, (const __nv_bfloat16*)wgu, counts, offsets, perm, k, d, f,
+            E, (__nv_bfloat16*)H);
+    else
+        ffn_up_stream<float><<<grid, block, 0, s>>>((const float*)x, (const float*)wgu, counts,
+                                                    offsets, perm, k, d, f, E, (float*)H);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, const int32_t* counts,
+                                   const int32_t* offsets, int d, int f, int E, float* Y,
+                                   cudaStream_t s) {
+    const dim3 block(kWarps * 32), grid((d + kWarps - 1) / kWarps);
+    if (dt == DType::BF16)
+        ffn_down_stream<__nv_bfloat16><<<grid, block, 0, s>>>(
+            (const __nv_bfloat16*)H, (const __nv_bfloat16*)wdT, counts, offsets, d, f, E, Y);
+    else
+        ffn_down_stream<float><<<grid, block, 0, s>>>((const float*)H, (const float*)wdT, counts,
+                                                      offsets, d, f, E, Y);
+    return cudaGetLastError();
+}
+
+}  // namespace colibri

@@ -1,0 +1,476 @@
+// Grouped GEMM for the expert FFN on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA), bf16 operands, float32 accumulation.
+//
+// zskr.cn "Colibri：面向MoE架构的C语言高效推理引擎解析" section 3.3 stages 3-4
+// (the tokens of one expert batched into one GEMM; gate_proj, up_proj, SiLU and
+// down_proj per expert).  Two instantiations:
+//
+//   kGateUp  A = Xp (tokens of each expert, consecutive rows) [pairs, d]
+//            B = packed [W_gate^T | W_up^T] blocks of 128 rows each, K = d
+//            one tile = 128 rows x (128 gate + 128 up) columns; the epilogue
+//            reads both halves from TMEM and writes H = silu(G) * U (bf16).
+//   kDown    A = H [pairs, f], B = W_down^T [d, f] per expert, K = f
+//            one tile = 128 rows x 256 output features, written as float32.
+//
+// Work items are (m-tile, n-block) pairs.  An m-tile is up to 128 consecutive
+// pair rows of one expert (the dispatch kernel's tile list), so experts with
+// no token have no tile at all.  The kernel is persistent: CTA b takes work
+// b, b + grid, ...; work is walked in bands of kBand m-tiles, n-block-major
+// inside a band, so one weight block is reused from L2 by the band's m-tiles
+// of the same expert while the band's A rows stay resident.
+//
+// Roles (192 threads):
+//   warp 0      TMA producer: A and B tiles of 64 K-columns into a
+//               kStages-deep ring of 128B-swizzled shared-memory stages.
+//   warp 1      TMEM owner; lane 0 issues tcgen05.mma (M=128, N=256, K=16)
+//               into one of two 256-column accumulators, commits each stage
+//               back to the producer and each finished tile to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)..+31, i.e. tile rows), activation, stores.
+// Every mbarrier wait is bounded by a time limit: on expiry the CTA records
+// DEV_TIMEOUT in the status word, every role stops, outstanding TMA copies
+// and MMAs are waited for (again bounded) and TMEM is freed before exit.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "gemm_tc.h"
+#include "kernels.h"
+
+namespace colibri {
+
+namespace {
+
+constexpr int kBM = 128;          // tile rows (pairs)
+constexpr int kBN = 256;          // tile columns of B rows per MMA
+constexpr int kBK = 64;           // K per stage: one 128-byte swizzle atom of bf16
+constexpr int kStages = 4;
+constexpr int kBand = 8;          // m-tiles per raster band
+constexpr int kThreads = 192;
+constexpr int kAccCols = 256;     // TMEM columns per accumulator
+constexpr int kTmemCols = 512;    // two accumulators
+constexpr uint32_t kStageA = kBM * kBK * 2;   // 16 KB
+constexpr uint32_t kStageB = kBN * kBK * 2;   // 32 KB
+constexpr uint32_t kStageBytes = kStageA + kStageB;
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase with parity `parity` of `bar` has completed, or the
+// time limit passes, or another role has aborted.  Returns false on
+// timeout/abort (and records the timeout).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicExch(status, DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bounded wait used during teardown: ignores the abort flag.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > limit_ns) return;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, f32 accumulate).
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), start
+// address >> 4 in bits 0-13, descriptor version 1 in bits 46-47, layout
+// "128-byte swizzle" (2) in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+    d |= (uint64_t)1 << 46;             // version
+    d |= (uint64_t)2 << 61;             // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor for kind::f16: f32 accumulator (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- work decode
+
+struct Work {
+    int expert, row0, rows, nblk;
+};
+
+__device__ __forceinline__ Work decode_work(int w, int num_tiles, int n_blocks,
+                                            const int32_t* __restrict__ tile_expert,
+                                            const int32_t* __restrict__ tile_row,
+                                            const int32_t* __restrict__ tile_rows) {
+    const int per_band = kBand * n_blocks;
+    const int band = w / per_band;
+    const int rem = w - band * per_band;
+    const int m_lo = band * kBand;
+    const int cnt = min(kBand, num_tiles - m_lo);
+    const int nblk = rem / cnt;
+    const int m = m_lo + (rem - nblk * cnt);
+    Work r;
+    r.expert = tile_expert[m];
+    r.row0 = tile_row[m];
+    r.rows = tile_rows[m];
+    r.nblk = nblk;
+    return r;
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                TcGemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms.
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* stage_a = smem;
+    uint8_t* stage_b = smem + kStages * kStageA;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* full = bars;                 // [kStages]
+    uint64_t* empty = bars + kStages;      // [kStages]
+    uint64_t* acc_full = bars + 2 * kStages;     // [2]
+    uint64_t* acc_empty = bars + 2 * kStages + 2;  // [2]
+    uint64_t* mma_done = bars + 2 * kStages + 4;   // [1]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_tiles = *args.num_tiles;
+    const int total = num_tiles * args.n_blocks;
+    const uint64_t limit = args.wait_limit_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&acc_full[a]), 1);
+            mbar_init(smem_u32(&acc_empty[a]), 4 * 32);
+        }
+        mbar_init(smem_u32(&mma_done[0]), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool issued[kStages];
+            uint32_t issued_phase[kStages];
+            for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
+            for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+                const Work wk = decode_work(w, num_tiles, args.n_blocks, args.tile_expert,
+                                            args.tile_row, args.tile_rows);
+                const int b_row = wk.expert * args.b_rows_per_expert + wk.nblk * kBN;
+                bool ok = true;
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, args.status,
+                                   limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_expect_tx(fb, kStageBytes);
+                    tma_load_2d(smem_u32(stage_a + stage * kStageA), &tmA, kb * kBK, wk.row0, fb);
+                    tma_load_2d(smem_u32(stage_b + stage * kStageB), &tmB, kb * kBK, b_row, fb);
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == kStages) stage = 0, phase ^= 1;
+                }
+                if (!ok) break;
+            }
+            // Teardown: every copy this thread issued must have landed.
+            for (int s = 0; s < kStages; ++s)
+                if (issued[s]) mbar_wait_drain(smem_u32(&full[s]), issued_phase[s], limit);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+                if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1, abort_flag, args.status,
+                               limit))
+                    break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kAccCols;
+                bool ok = true;
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.status,
+                                   limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t da = smem_desc_sw128(smem_u32(stage_a + stage * kStageA));
+                    const uint64_t db = smem_desc_sw128(smem_u32(stage_b + stage * kStageB));
+#pragma unroll
+                    for (int ks = 0; ks < kBK / 16; ++ks)
+                        // +32 bytes of K per step inside the swizzle atom (encoded >> 4)
+                        mma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, idesc, (kb | ks) != 0);
+                    mma_commit(smem_u32(&empty[stage]));
+                    if (++stage == kStages) stage = 0, phase ^= 1;
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&acc_full[acc]));
+                if (++acc == 2) acc = 0, acc_phase ^= 1;
+            }
+            // Teardown: all MMAs issued by this thread complete before TMEM is freed.
+            mma_commit(smem_u32(&mma_done[0]));
+            mbar_wait_drain(smem_u32(&mma_done[0]), 0, limit);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;              // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;       // tile row of this thread
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+            const Work wk = decode_work(w, num_tiles, args.n_blocks, args.tile_expert,
+                                        args.tile_row, args.tile_rows);
+            const bool got =
+                mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, args.status, limit);
+            // tcgen05.ld is warp-collective: the whole warp stops if any lane gave up.
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
+            const bool live = row < wk.rows;
+            const size_t orow = (size_t)(wk.row0 + row);
+            if constexpr (kMode == kGateUp) {
+                __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
+#pragma unroll 1
+                for (int c = 0; c < 128 / 32; ++c) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(tbase + c * 32, g);
+                    tmem_ld32(tbase + 128 + c * 32, u);
+                    tmem_ld_wait();
+                    if (live) {
+                        uint4 pk[4];
+                        uint32_t* pw = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                            const float h1 =
+                                silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
+                            pw[i] = *reinterpret_cast<uint32_t*>(&b2);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(H + orow * args.out_ld +
+                                                              wk.nblk * 128 + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+                    }
+                }
+            } else {
+                float* Y = reinterpret_cast<float*>(args.out);
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    if (live) {
+                        float4* dst = reinterpret_cast<float4*>(Y + orow * args.out_ld +
+                                                                wk.nblk * kBN + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                 __uint_as_float(v[4 * i + 2]),
+                                                 __uint_as_float(v[4 * i + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&acc_empty[acc]));
+            if (++acc == 2) acc = 0, acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+size_t tc_gemm_smem_bytes() { return (size_t)kStages * kStageBytes + 1024 + 256; }
+int tc_gemm_block_m() { return kBM; }
+int tc_gemm_block_n(int mode) { return mode == kGateUp ? 128 : kBN; }
+
+// Tensor map of a row-major bf16 matrix [rows, cols] with a box of
+// 64 columns x box_rows rows, 128-byte swizzle, zero fill out of bounds.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_tc_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const TcGemmArgs& args, int grid, cudaStream_t s) {
+    const size_t smem = tc_gemm_smem_bytes();
+    if (grid <= 0) return cudaSuccess;
+    if (mode == kGateUp) {
+        auto k = grouped_gemm_tc<kGateUp>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kThreads, smem, s>>>(tmA, tmB, args);
+    } else {
+        auto k = grouped_gemm_tc<kDown>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kThreads, smem, s>>>(tmA, tmB, args);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace colibri

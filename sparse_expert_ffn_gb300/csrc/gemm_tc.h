@@ -1,0 +1,34 @@
+// Host interface of the tcgen05 grouped GEMM (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace colibri {
+
+enum : int { kGateUp = 0, kDown = 1 };
+
+struct TcGemmArgs {
+    const int32_t* tile_expert;  // [max_tiles] expert of each m-tile
+    const int32_t* tile_row;     // [max_tiles] first pair row of each m-tile
+    const int32_t* tile_rows;    // [max_tiles] valid rows (<= 128) of each m-tile
+    const int32_t* num_tiles;    // device scalar: number of m-tiles
+    int n_blocks;                // n-blocks per expert
+    int k_blocks;                // K / 64
+    int b_rows_per_expert;       // rows of the packed B operand per expert
+    void* out;                   // H (bf16, kGateUp) or Y (float32, kDown)
+    int out_ld;                  // row stride of `out` in elements
+    int* status;                 // device status word (DEV_TIMEOUT on a wait that gave up)
+    uint64_t wait_limit_ns;      // bound of every mbarrier wait
+};
+
+size_t tc_gemm_smem_bytes();
+int tc_gemm_block_m();
+int tc_gemm_block_n(int mode);
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
+cudaError_t launch_tc_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const TcGemmArgs& args, int grid, cudaStream_t s);
+
+}  // namespace colibri

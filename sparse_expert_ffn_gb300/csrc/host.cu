@@ -1,0 +1,622 @@
+// Host runtime of the C ABI (include/colibri_moe.h): argument checks, weight
+// repack, the workspace arena, executor choice and the launch sequence.
+//
+// Launch sequence of one forward, all on the caller's stream, no host sync,
+// no allocation (zskr.cn "Colibri：面向MoE架构的C语言高效推理引擎解析" section
+// 3.3 stages 2-5):
+//   router_topk  -> topk_idx, topk_w
+//   dispatch     -> counts, offsets, perm, inv, grouped-GEMM tile list
+//   STREAM:  ffn_up_stream -> H,  ffn_down_stream -> Y
+//   GROUPED: gather_rows -> Xp, tcgen05 gate/up GEMM -> H, tcgen05 down GEMM -> Y
+//   combine      -> y (optionally + residual)
+// The workspace is one device allocation carved into 256-byte aligned
+// sub-buffers at init for max_tokens (pnsm.cn section 3.2: an arena sized
+// once, no allocation on the hot path; zskr.cn section 3.2: the pool sized
+// from the model and the largest batch).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "colibri_moe.h"
+#include "common.cuh"
+#include "gemm_tc.h"
+#include "kernels.h"
+
+using namespace colibri;
+
+struct colibri_moe {
+    colibri_moe_config_t cfg;
+    DType dt;
+    int esz;
+    int num_sms;
+    int e_pad;
+    // packed weights
+    void* wr = nullptr;     // [e_pad, d]
+    float* bias = nullptr;  // [E] or null
+    void* wgu = nullptr;    // [E][f/128][2][128][d]
+    void* wdT = nullptr;    // [E][d][f]
+    uint64_t weight_bytes = 0;
+    // workspace
+    void* ws = nullptr;
+    uint64_t ws_bytes = 0;
+    int32_t* topk_idx = nullptr;
+    float* topk_w = nullptr;
+    int32_t* counts = nullptr;
+    int32_t* offsets = nullptr;
+    int32_t* perm = nullptr;
+    int32_t* inv = nullptr;
+    int32_t* tile_expert = nullptr;
+    int32_t* tile_row = nullptr;
+    int32_t* tile_rows = nullptr;
+    int32_t* num_tiles = nullptr;
+    int* status = nullptr;
+    void* xp = nullptr;     // [max_pairs, d]
+    void* H = nullptr;      // [max_pairs, f]
+    float* Y = nullptr;     // [max_pairs, d]
+    void* u = nullptr;      // [max_tokens, d]
+    void* x_stage = nullptr;
+    void* y_stage = nullptr;
+    int max_pairs = 0;
+    int max_tiles = 0;
+    bool grouped_ok = false;
+    CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT;
+    uint64_t wait_limit_ns = 2000000000ull;
+    int last_T = 0;
+    uint64_t launches = 0;
+    colibri_status_t sticky = COLIBRI_OK;
+    // opt-in per-stage event profiling
+    bool prof = false;
+    struct ProfRec {
+        int stage;
+        cudaEvent_t a, b;
+    };
+    std::vector<cudaEvent_t> ev_pool;
+    std::vector<ProfRec> recs;
+};
+
+namespace {
+
+// Allocation-failure injection for tests: COLIBRI_FAIL_ALLOC_AT=n makes the
+// n-th device allocation of an init fail (1-based).
+struct AllocCounter {
+    int n = 0;
+    int fail_at = 0;
+    AllocCounter() {
+        const char* e = std::getenv("COLIBRI_FAIL_ALLOC_AT");
+        fail_at = e ? std::atoi(e) : 0;
+    }
+    cudaError_t alloc(void** p, size_t bytes) {
+        ++n;
+        if (fail_at > 0 && n == fail_at) {
+            *p = nullptr;
+            return cudaErrorMemoryAllocation;
+        }
+        return cudaMalloc(p, bytes);
+    }
+};
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+colibri_status_t validate_config(const colibri_moe_config_t* c) {
+    if (!c) return COLIBRI_ERR_INVALID_ARG;
+    if (c->n_experts <= 0 || c->top_k <= 0 || c->d_model <= 0 || c->d_ff <= 0 ||
+        c->max_tokens <= 0 || c->device < 0)
+        return COLIBRI_ERR_INVALID_ARG;
+    if (c->top_k > c->n_experts) return COLIBRI_ERR_INVALID_ARG;
+    if (c->dtype != COLIBRI_DTYPE_FP32 && c->dtype != COLIBRI_DTYPE_BF16)
+        return COLIBRI_ERR_INVALID_ARG;
+    if (c->executor < COLIBRI_EXEC_AUTO || c->executor > COLIBRI_EXEC_GROUPED)
+        return COLIBRI_ERR_INVALID_ARG;
+    if ((int64_t)c->max_tokens * c->top_k > (int64_t)1 << 30) return COLIBRI_ERR_INVALID_ARG;
+    if (c->n_experts > 256 || c->top_k > 8) return COLIBRI_ERR_UNSUPPORTED;
+    if (c->d_model % 64 != 0 || c->d_ff % 128 != 0) return COLIBRI_ERR_UNSUPPORTED;
+    if (c->executor == COLIBRI_EXEC_GROUPED && c->dtype != COLIBRI_DTYPE_BF16)
+        return COLIBRI_ERR_UNSUPPORTED;
+    return COLIBRI_OK;
+}
+
+bool grouped_shape_ok(const colibri_moe_config_t& c) {
+    return c.dtype == COLIBRI_DTYPE_BF16 && c.d_model % 256 == 0 && c.d_ff % 128 == 0;
+}
+
+void release(colibri_moe_t* h) {
+    if (!h) return;
+    for (auto& r : h->recs) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    for (auto e : h->ev_pool) cudaEventDestroy(e);
+    cudaFree(h->wr);
+    cudaFree(h->bias);
+    cudaFree(h->wgu);
+    cudaFree(h->wdT);
+    cudaFree(h->ws);
+    delete h;
+}
+
+colibri_status_t from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return COLIBRI_OK;
+    if (e == cudaErrorMemoryAllocation) return COLIBRI_ERR_OOM;
+    return COLIBRI_ERR_CUDA;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+    return pa < pb + nb && pb < pa + na;
+}
+
+// Copy (host or device) matrices [batch][R][C] into the packed layout through
+// the remapping transpose; host inputs go through a device staging buffer one
+// batch entry at a time.
+colibri_status_t pack(colibri_moe_t* h, const void* src, bool src_on_device,
+                      void* dst, int batch, int R, int C, size_t out_batch, int blk, int period,
+                      int which, void* staging) {
+    const size_t mat = (size_t)R * C * h->esz;
+    if (src_on_device) {
+        return from_cuda(launch_transpose_remap(h->esz, src, dst, batch, R, C, (size_t)R * C,
+                                                out_batch, blk, period, which, 0));
+    }
+    for (int b = 0; b < batch; ++b) {
+        cudaError_t e = cudaMemcpy(staging, (const uint8_t*)src + (size_t)b * mat, mat,
+                                   cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = launch_transpose_remap(h->esz, staging, (uint8_t*)dst + (size_t)b * out_batch * h->esz,
+                                   1, R, C, (size_t)R * C, out_batch, blk, period, which, 0);
+        if (e != cudaSuccess) return from_cuda(e);
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    return COLIBRI_OK;
+}
+
+int choose_executor(const colibri_moe_t* h, int T) {
+    if (h->cfg.executor != COLIBRI_EXEC_AUTO) return h->cfg.executor;
+    if (!h->grouped_ok) return COLIBRI_EXEC_STREAM;
+    // Few pairs per expert: the FFN is a weight stream, CUDA cores keep up.
+    const int64_t pairs = (int64_t)T * h->cfg.top_k;
+    return pairs <= 4 * (int64_t)h->cfg.n_experts ? COLIBRI_EXEC_STREAM : COLIBRI_EXEC_GROUPED;
+}
+
+cudaEvent_t take_event(colibri_moe_t* h) {
+    if (!h->ev_pool.empty()) {
+        cudaEvent_t e = h->ev_pool.back();
+        h->ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Brackets one stage's kernel launch(es): records an event pair when
+// profiling is on, counts the launches, and maps launch errors.
+struct Stage {
+    colibri_moe_t* h;
+    int stage;
+    cudaStream_t s;
+    cudaEvent_t a = nullptr;
+    Stage(colibri_moe_t* h_, int stage_, cudaStream_t s_) : h(h_), stage(stage_), s(s_) {
+        if (h->prof && (a = take_event(h))) cudaEventRecord(a, s);
+    }
+    colibri_status_t done(cudaError_t e, int nlaunch) {
+        h->launches += nlaunch;
+        if (a) {
+            cudaEvent_t b = take_event(h);
+            if (b) {
+                cudaEventRecord(b, s);
+                h->recs.push_back({stage, a, b});
+            } else {
+                h->ev_pool.push_back(a);
+            }
+        }
+        return from_cuda(e);
+    }
+};
+
+// The layer on device buffers; `resid` (may equal y) adds a residual.
+colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, const void* resid,
+                           cudaStream_t s) {
+    const auto& c = h->cfg;
+    const int E = c.n_experts, k = c.top_k, d = c.d_model, f = c.d_ff;
+    const int npairs = T * k;
+    colibri_status_t st;
+    {
+        Stage g(h, COLIBRI_STAGE_ROUTER, s);
+        st = g.done(launch_router_simt(h->dt, x, h->wr, h->bias, T, d, E, k, h->topk_idx,
+                                       h->topk_w, s), 1);
+        if (st != COLIBRI_OK) return st;
+    }
+    {
+        Stage g(h, COLIBRI_STAGE_DISPATCH, s);
+        st = g.done(launch_dispatch(h->topk_idx, npairs, E, h->counts, h->offsets, h->perm,
+                                    h->inv, tc_gemm_block_m(), h->tile_expert, h->tile_row,
+                                    h->tile_rows, h->num_tiles, h->status, s), 1);
+        if (st != COLIBRI_OK) return st;
+    }
+    const int ex = choose_executor(h, T);
+    if (ex == COLIBRI_EXEC_STREAM) {
+        {
+            Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
+            st = g.done(launch_ffn_up_stream(h->dt, x, h->wgu, h->counts, h->offsets, h->perm, k,
+                                             d, f, E, h->H, s), 1);
+            if (st != COLIBRI_OK) return st;
+        }
+        {
+            Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
+            st = g.done(launch_ffn_down_stream(h->dt, h->H, h->wdT, h->counts, h->offsets, d, f,
+                                               E, h->Y, s), 1);
+            if (st != COLIBRI_OK) return st;
+        }
+    } else {
+        {
+            Stage g(h, COLIBRI_STAGE_GATHER, s);
+            st = g.done(launch_gather(h->esz, x, h->perm, k, d, npairs, h->xp, s), 1);
+            if (st != COLIBRI_OK) return st;
+        }
+        const int tiles_ub =
+            (npairs + tc_gemm_block_m() - 1) / tc_gemm_block_m() + std::min(E, npairs);
+        TcGemmArgs a{};
+        a.tile_expert = h->tile_expert;
+        a.tile_row = h->tile_row;
+        a.tile_rows = h->tile_rows;
+        a.num_tiles = h->num_tiles;
+        a.status = h->status;
+        a.wait_limit_ns = h->wait_limit_ns;
+        // gate/up: N = 2f in blocks of 256 rows (128 gate + 128 up), K = d
+        a.n_blocks = f / 128;
+        a.k_blocks = d / 64;
+        a.b_rows_per_expert = 2 * f;
+        a.out = h->H;
+        a.out_ld = f;
+        {
+            const int grid = (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks, h->num_sms);
+            Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
+            st = g.done(launch_tc_gemm(kGateUp, h->tm_xp, h->tm_wgu, a, grid, s), 1);
+            if (st != COLIBRI_OK) return st;
+        }
+        // down: N = d in blocks of 256, K = f
+        a.n_blocks = d / 256;
+        a.k_blocks = f / 64;
+        a.b_rows_per_expert = d;
+        a.out = h->Y;
+        a.out_ld = d;
+        {
+            const int grid = (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks, h->num_sms);
+            Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
+            st = g.done(launch_tc_gemm(kDown, h->tm_h, h->tm_wdT, a, grid, s), 1);
+            if (st != COLIBRI_OK) return st;
+        }
+    }
+    {
+        Stage g(h, COLIBRI_STAGE_COMBINE, s);
+        st = g.done(launch_combine(h->dt, h->Y, h->topk_w, h->inv, T, k, d, resid, y, s), 1);
+        if (st != COLIBRI_OK) return st;
+    }
+    h->last_T = T;
+    return COLIBRI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* colibri_status_str(colibri_status_t s) {
+    switch (s) {
+        case COLIBRI_OK: return "ok";
+        case COLIBRI_ERR_INVALID_ARG: return "invalid argument";
+        case COLIBRI_ERR_OOM: return "out of memory";
+        case COLIBRI_ERR_CUDA: return "CUDA error";
+        case COLIBRI_ERR_UNSUPPORTED: return "unsupported device or shape";
+        case COLIBRI_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_router,
+                              const float* router_bias, const void* w_gate, const void* w_up,
+                              const void* w_down, int weights_on_device, colibri_moe_t** out) {
+    if (!out) return COLIBRI_ERR_INVALID_ARG;
+    *out = nullptr;
+    colibri_status_t st = validate_config(cfg);
+    if (st != COLIBRI_OK) return st;
+    if (!w_router || !w_gate || !w_up || !w_down) return COLIBRI_ERR_INVALID_ARG;
+    if (weights_on_device != 0 && weights_on_device != 1) return COLIBRI_ERR_INVALID_ARG;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) return COLIBRI_ERR_CUDA;
+    if (cfg->device >= ndev) return COLIBRI_ERR_INVALID_ARG;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return COLIBRI_ERR_CUDA;
+    if (prop.major * 10 + prop.minor != 103) return COLIBRI_ERR_UNSUPPORTED;
+    DeviceGuard guard(cfg->device);
+    if (!guard.ok) return COLIBRI_ERR_CUDA;
+
+    colibri_moe_t* h = new (std::nothrow) colibri_moe;
+    if (!h) return COLIBRI_ERR_OOM;
+    h->cfg = *cfg;
+    h->dt = cfg->dtype == COLIBRI_DTYPE_BF16 ? DType::BF16 : DType::F32;
+    h->esz = cfg->dtype == COLIBRI_DTYPE_BF16 ? 2 : 4;
+    h->num_sms = prop.multiProcessorCount;
+    h->e_pad = (cfg->n_experts + 15) / 16 * 16;
+    if (const char* e = std::getenv("COLIBRI_WAIT_LIMIT_NS")) h->wait_limit_ns = std::strtoull(e, nullptr, 10);
+
+    const int E = cfg->n_experts, d = cfg->d_model, f = cfg->d_ff, k = cfg->top_k;
+    AllocCounter ac;
+    auto fail = [&](colibri_status_t s) {
+        cudaDeviceSynchronize();
+        release(h);
+        return s;
+    };
+
+    // ---- weights
+    const size_t wr_bytes = (size_t)h->e_pad * d * h->esz;
+    const size_t wgu_bytes = (size_t)E * 2 * f * d * h->esz;
+    const size_t wd_bytes = (size_t)E * d * f * h->esz;
+    if ((st = from_cuda(ac.alloc(&h->wr, wr_bytes))) != COLIBRI_OK) return fail(st);
+    if ((st = from_cuda(ac.alloc(&h->wgu, wgu_bytes))) != COLIBRI_OK) return fail(st);
+    if ((st = from_cuda(ac.alloc(&h->wdT, wd_bytes))) != COLIBRI_OK) return fail(st);
+    if (router_bias) {
+        if ((st = from_cuda(ac.alloc((void**)&h->bias, (size_t)E * 4))) != COLIBRI_OK)
+            return fail(st);
+        if ((st = from_cuda(cudaMemcpy(h->bias, router_bias, (size_t)E * 4, cudaMemcpyDefault))) !=
+            COLIBRI_OK)
+            return fail(st);
+    }
+    h->weight_bytes = wr_bytes + wgu_bytes + wd_bytes + (router_bias ? (size_t)E * 4 : 0);
+
+    void* staging = nullptr;
+    if (!weights_on_device) {
+        const size_t stage_bytes = (size_t)std::max(d * f, d * E) * h->esz;
+        if ((st = from_cuda(ac.alloc(&staging, stage_bytes))) != COLIBRI_OK) return fail(st);
+    }
+    auto fail_staged = [&](colibri_status_t s) {
+        cudaDeviceSynchronize();
+        cudaFree(staging);
+        return fail(s);
+    };
+    if ((st = from_cuda(cudaMemset(h->wr, 0, wr_bytes))) != COLIBRI_OK) return fail_staged(st);
+    // router [d, E] -> [E, d]
+    st = pack(h, w_router, weights_on_device, h->wr, 1, d, E, (size_t)h->e_pad * d, E, E, 0,
+              staging);
+    if (st != COLIBRI_OK) return fail_staged(st);
+    // gate/up [E][d][f] -> [E][f/128][2][128][d]
+    st = pack(h, w_gate, weights_on_device, h->wgu, E, d, f, (size_t)2 * f * d, 128, 256, 0,
+              staging);
+    if (st != COLIBRI_OK) return fail_staged(st);
+    st = pack(h, w_up, weights_on_device, h->wgu, E, d, f, (size_t)2 * f * d, 128, 256, 1,
+              staging);
+    if (st != COLIBRI_OK) return fail_staged(st);
+    // down [E][f][d] -> [E][d][f]
+    st = pack(h, w_down, weights_on_device, h->wdT, E, f, d, (size_t)d * f, d, d, 0, staging);
+    if (st != COLIBRI_OK) return fail_staged(st);
+    if ((st = from_cuda(cudaDeviceSynchronize())) != COLIBRI_OK) return fail_staged(st);
+    cudaFree(staging);
+    staging = nullptr;
+
+    // ---- workspace arena
+    const int M = cfg->max_tokens;
+    h->max_pairs = M * k;
+    h->max_tiles = (h->max_pairs + tc_gemm_block_m() - 1) / tc_gemm_block_m() + std::min(E, h->max_pairs);
+    h->grouped_ok = grouped_shape_ok(*cfg);
+    if (cfg->executor == COLIBRI_EXEC_GROUPED && !h->grouped_ok) return fail(COLIBRI_ERR_UNSUPPORTED);
+    const size_t P = (size_t)h->max_pairs;
+    size_t off = 0;
+    auto carve = [&](size_t bytes) {
+        const size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    const size_t o_idx = carve(P * 4), o_w = carve(P * 4), o_cnt = carve((size_t)E * 4),
+                 o_off = carve((size_t)(E + 1) * 4), o_perm = carve(P * 4), o_inv = carve(P * 4),
+                 o_te = carve((size_t)h->max_tiles * 4), o_tr = carve((size_t)h->max_tiles * 4),
+                 o_trs = carve((size_t)h->max_tiles * 4), o_nt = carve(4), o_st = carve(4),
+                 o_xp = h->grouped_ok ? carve(P * d * h->esz) : 0, o_h = carve(P * f * h->esz),
+                 o_y = carve(P * d * 4), o_u = carve((size_t)M * d * h->esz),
+                 o_xs = carve((size_t)M * d * h->esz), o_ys = carve((size_t)M * d * h->esz);
+    h->ws_bytes = off;
+    if ((st = from_cuda(ac.alloc(&h->ws, off))) != COLIBRI_OK) return fail(st);
+    uint8_t* b = (uint8_t*)h->ws;
+    h->topk_idx = (int32_t*)(b + o_idx);
+    h->topk_w = (float*)(b + o_w);
+    h->counts = (int32_t*)(b + o_cnt);
+    h->offsets = (int32_t*)(b + o_off);
+    h->perm = (int32_t*)(b + o_perm);
+    h->inv = (int32_t*)(b + o_inv);
+    h->tile_expert = (int32_t*)(b + o_te);
+    h->tile_row = (int32_t*)(b + o_tr);
+    h->tile_rows = (int32_t*)(b + o_trs);
+    h->num_tiles = (int32_t*)(b + o_nt);
+    h->status = (int*)(b + o_st);
+    h->xp = h->grouped_ok ? (void*)(b + o_xp) : nullptr;
+    h->H = b + o_h;
+    h->Y = (float*)(b + o_y);
+    h->u = b + o_u;
+    h->x_stage = b + o_xs;
+    h->y_stage = b + o_ys;
+    if ((st = from_cuda(cudaMemset(h->ws, 0, off))) != COLIBRI_OK) return fail(st);
+
+    if (h->grouped_ok) {
+        bool ok = make_tmap_bf16(&h->tm_xp, h->xp, P, d, 128) &&
+                  make_tmap_bf16(&h->tm_wgu, h->wgu, (uint64_t)E * 2 * f, d, 256) &&
+                  make_tmap_bf16(&h->tm_h, h->H, P, f, 128) &&
+                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 256);
+        if (!ok) {
+            if (cfg->executor == COLIBRI_EXEC_GROUPED) return fail(COLIBRI_ERR_CUDA);
+            h->grouped_ok = false;
+        }
+    }
+    if ((st = from_cuda(cudaDeviceSynchronize())) != COLIBRI_OK) return fail(st);
+    *out = h;
+    return COLIBRI_OK;
+}
+
+colibri_status_t colibri_forward(colibri_moe_t* h, const void* x, int32_t T, void* y,
+                                 void* stream) {
+    if (!h || !x || !y || T < 0 || T > h->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
+    if (((uintptr_t)x & 15) || ((uintptr_t)y & 15)) return COLIBRI_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)T * h->cfg.d_model * h->esz;
+    if (T > 0 && ranges_overlap(x, bytes, y, bytes)) return COLIBRI_ERR_INVALID_ARG;
+    if (T == 0) return COLIBRI_OK;
+    DeviceGuard g(h->cfg.device);
+    if (!g.ok) return COLIBRI_ERR_CUDA;
+    const colibri_status_t st = run_layer(h, x, T, y, nullptr, (cudaStream_t)stream);
+    if (st != COLIBRI_OK && h->sticky == COLIBRI_OK) h->sticky = st;
+    return st;
+}
+
+colibri_status_t colibri_forward_host(colibri_moe_t* h, const void* x_host, int32_t T,
+                                      void* y_host, void* stream) {
+    if (!h || !x_host || !y_host || T < 0 || T > h->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
+    if (T == 0) return COLIBRI_OK;
+    DeviceGuard g(h->cfg.device);
+    if (!g.ok) return COLIBRI_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t bytes = (size_t)T * h->cfg.d_model * h->esz;
+    cudaError_t e = cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    colibri_status_t st = run_layer(h, h->x_stage, T, h->y_stage, nullptr, s);
+    if (st != COLIBRI_OK) return st;
+    e = cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(cudaStreamSynchronize(s));
+}
+
+colibri_status_t colibri_rmsnorm_moe_residual(colibri_moe_t* h, void* hidden, int32_t T,
+                                              const void* gamma, float eps, void* stream) {
+    if (!h || !hidden || !gamma || T < 0 || T > h->cfg.max_tokens || !(eps >= 0.0f))
+        return COLIBRI_ERR_INVALID_ARG;
+    if ((uintptr_t)hidden & 15) return COLIBRI_ERR_INVALID_ARG;
+    if (T == 0) return COLIBRI_OK;
+    DeviceGuard g(h->cfg.device);
+    if (!g.ok) return COLIBRI_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    {
+        Stage g(h, COLIBRI_STAGE_RMSNORM, s);
+        const colibri_status_t st =
+            g.done(launch_rmsnorm(h->dt, hidden, gamma, T, h->cfg.d_model, eps, h->u, s), 1);
+        if (st != COLIBRI_OK) return st;
+    }
+    return run_layer(h, h->u, T, hidden, hidden, s);
+}
+
+colibri_status_t colibri_get_routing(colibri_moe_t* h, int32_t* topk_idx, float* topk_w,
+                                     int32_t* counts, int32_t* perm, void* stream) {
+    if (!h) return COLIBRI_ERR_INVALID_ARG;
+    DeviceGuard g(h->cfg.device);
+    if (!g.ok) return COLIBRI_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t P = (size_t)h->last_T * h->cfg.top_k;
+    cudaError_t e = cudaSuccess;
+    if (topk_idx && P && e == cudaSuccess)
+        e = cudaMemcpyAsync(topk_idx, h->topk_idx, P * 4, cudaMemcpyDeviceToDevice, s);
+    if (topk_w && P && e == cudaSuccess)
+        e = cudaMemcpyAsync(topk_w, h->topk_w, P * 4, cudaMemcpyDeviceToDevice, s);
+    if (counts && e == cudaSuccess)
+        e = cudaMemcpyAsync(counts, h->counts, (size_t)h->cfg.n_experts * 4,
+                            cudaMemcpyDeviceToDevice, s);
+    if (perm && P && e == cudaSuccess)
+        e = cudaMemcpyAsync(perm, h->perm, P * 4, cudaMemcpyDeviceToDevice, s);
+    return from_cuda(e);
+}
+
+colibri_status_t colibri_set_executor(colibri_moe_t* h, int32_t executor) {
+    if (!h || executor < COLIBRI_EXEC_AUTO || executor > COLIBRI_EXEC_GROUPED)
+        return COLIBRI_ERR_INVALID_ARG;
+    if (executor == COLIBRI_EXEC_GROUPED && !h->grouped_ok) return COLIBRI_ERR_UNSUPPORTED;
+    h->cfg.executor = executor;
+    return COLIBRI_OK;
+}
+
+colibri_status_t colibri_check(colibri_moe_t* h, void* stream) {
+    if (!h) return COLIBRI_ERR_INVALID_ARG;
+    DeviceGuard g(h->cfg.device);
+    if (!g.ok) return COLIBRI_ERR_CUDA;
+    colibri_status_t st = h->sticky;
+    h->sticky = COLIBRI_OK;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return COLIBRI_ERR_CUDA;
+    e = cudaGetLastError();
+    if (e != cudaSuccess && st == COLIBRI_OK) st = COLIBRI_ERR_CUDA;
+    int dev_status = 0;
+    e = cudaMemcpy(&dev_status, h->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return COLIBRI_ERR_CUDA;
+    if (dev_status != DEV_OK) {
+        cudaMemset(h->status, 0, sizeof(int));
+        if (st == COLIBRI_OK) st = dev_status == DEV_TIMEOUT ? COLIBRI_ERR_TIMEOUT : COLIBRI_ERR_CUDA;
+    }
+    return st;
+}
+
+colibri_status_t colibri_profile_enable(colibri_moe_t* h, int enable) {
+    if (!h) return COLIBRI_ERR_INVALID_ARG;
+    DeviceGuard g(h->cfg.device);
+    for (auto& r : h->recs) {
+        cudaEventSynchronize(r.b);
+        h->ev_pool.push_back(r.a);
+        h->ev_pool.push_back(r.b);
+    }
+    h->recs.clear();
+    h->prof = enable != 0;
+    return COLIBRI_OK;
+}
+
+colibri_status_t colibri_profile_read(colibri_moe_t* h, double* total_ms, uint64_t* launches) {
+    if (!h || !total_ms || !launches) return COLIBRI_ERR_INVALID_ARG;
+    DeviceGuard g(h->cfg.device);
+    for (int i = 0; i < COLIBRI_NUM_STAGES; ++i) total_ms[i] = 0.0, launches[i] = 0;
+    colibri_status_t st = COLIBRI_OK;
+    for (auto& r : h->recs) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+            st = COLIBRI_ERR_CUDA;
+        total_ms[r.stage] += ms;
+        launches[r.stage] += 1;
+        h->ev_pool.push_back(r.a);
+        h->ev_pool.push_back(r.b);
+    }
+    h->recs.clear();
+    return st;
+}
+
+colibri_status_t colibri_launch_count(const colibri_moe_t* h, uint64_t* n) {
+    if (!h || !n) return COLIBRI_ERR_INVALID_ARG;
+    *n = h->launches;
+    return COLIBRI_OK;
+}
+
+colibri_status_t colibri_workspace_bytes(const colibri_moe_t* h, uint64_t* weights,
+                                         uint64_t* workspace) {
+    if (!h) return COLIBRI_ERR_INVALID_ARG;
+    if (weights) *weights = h->weight_bytes;
+    if (workspace) *workspace = h->ws_bytes;
+    return COLIBRI_OK;
+}
+
+void colibri_free(colibri_moe_t* h) {
+    if (!h) return;
+    DeviceGuard g(h->cfg.device);
+    cudaDeviceSynchronize();
+    release(h);
+}
+
+}  // extern "C"

@@ -1,0 +1,41 @@
+// Launchers of the MoE layer kernels (host-side declarations, internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace colibri {
+
+enum class DType : int;
+
+size_t router_simt_smem(int d);
+cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const float* bias,
+                               int ntok, int d, int E, int k, int32_t* idx, float* w,
+                               cudaStream_t s);
+
+size_t dispatch_smem(int E);
+cudaError_t launch_dispatch(const int32_t* topk_idx, int n, int E, int32_t* counts,
+                            int32_t* offsets, int32_t* perm, int32_t* inv, int bm,
+                            int32_t* tile_expert, int32_t* tile_row, int32_t* tile_rows,
+                            int32_t* num_tiles, int* status, cudaStream_t s);
+
+cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* counts,
+                                 const int32_t* offsets, const int32_t* perm, int k, int d, int f,
+                                 int E, void* H, cudaStream_t s);
+cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, const int32_t* counts,
+                                   const int32_t* offsets, int d, int f, int E, float* Y,
+                                   cudaStream_t s);
+
+cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,
+                          int npairs, void* xp, cudaStream_t s);
+cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const int32_t* inv,
+                           int T, int k, int d, const void* resid, void* y, cudaStream_t s);
+cudaError_t launch_rmsnorm(DType dt, const void* h, const void* gamma, int T, int d, float eps,
+                           void* u, cudaStream_t s);
+cudaError_t launch_transpose_remap(int elem_bytes, const void* in, void* out, int batch, int R,
+                                   int C, size_t in_batch, size_t out_batch, int blk, int period,
+                                   int which, cudaStream_t s);
+
+}  // namespace colibri

@@ -1,0 +1,157 @@
+// Gather, combine, RMSNorm and the init-time weight repack.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace colibri {
+
+namespace {
+
+// Xp[p, :] = x[perm[p] / k, :] — the tokens of every expert as consecutive
+// rows (the A operand of the grouped GEMM).  One CTA per pair row, 16-byte
+// vectors.
+__global__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k,
+                            int row_vecs, uint4* __restrict__ xp) {
+    const int p = blockIdx.x;
+    const int t = perm[p] / k;
+    const uint4* src = x + (size_t)t * row_vecs;
+    uint4* dst = xp + (size_t)p * row_vecs;
+    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x) dst[i] = src[i];
+}
+
+// Combine: y[t, c] = sum_j w[t, j] * Y[inv[t*k + j], c], j in order, float32;
+// with `resid`, y[t, c] = resid[t, c] + that sum (one rounding at the end).
+// zskr.cn section 3.3 stage 5 (aggregation weighted by the expert scores).
+template <typename T>
+__global__ void combine_kernel(const float* __restrict__ Y, const float* __restrict__ topk_w,
+                               const int32_t* __restrict__ inv, int k, int d,
+                               const T* resid, T* y) {  // resid may alias y (in-place residual)
+    const int t = blockIdx.y;
+    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (c >= d) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+        const float w = topk_w[(size_t)t * k + j];
+        const float4 v = *reinterpret_cast<const float4*>(Y + (size_t)inv[(size_t)t * k + j] * d + c);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+    }
+    const size_t o = (size_t)t * d + c;
+    if (resid) {
+        acc.x += to_f32(resid[o]);
+        acc.y += to_f32(resid[o + 1]);
+        acc.z += to_f32(resid[o + 2]);
+        acc.w += to_f32(resid[o + 3]);
+    }
+    y[o] = from_f32<T>(acc.x);
+    y[o + 1] = from_f32<T>(acc.y);
+    y[o + 2] = from_f32<T>(acc.z);
+    y[o + 3] = from_f32<T>(acc.w);
+}
+
+// RMSNorm: u = h / sqrt(mean(h^2) + eps) * gamma, float32 arithmetic, one
+// CTA per token (Zhang & Sennrich, 2019).
+template <typename T>
+__global__ void rmsnorm_kernel(const T* __restrict__ h, const T* __restrict__ gamma, int d,
+                               float eps, T* __restrict__ u) {
+    __shared__ float red[32];
+    const int t = blockIdx.x;
+    const T* hr = h + (size_t)t * d;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        const float v = to_f32(hr[i]);
+        ss = fmaf(v, v, ss);
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+        v = warp_sum(v);
+        if (threadIdx.x == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float inv_rms = 1.0f / sqrtf(red[0] / (float)d + eps);
+    for (int i = threadIdx.x; i < d; i += blockDim.x)
+        u[(size_t)t * d + i] = from_f32<T>(to_f32(hr[i]) * inv_rms * to_f32(gamma[i]));
+}
+
+// Batched transpose with a row remap, for the init-time weight repack:
+// out[b][map(c)][r] = in[b][r][c] for an [R, C] matrix per batch entry b,
+// map(c) = (c / blk) * period + which * blk + c % blk.
+template <typename E>
+__global__ void transpose_remap(const E* __restrict__ in, E* __restrict__ out, int R, int C,
+                                size_t in_batch, size_t out_batch, int blk, int period,
+                                int which) {
+    __shared__ E tile[32][33];
+    const int b = blockIdx.z;
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const E* src = in + b * in_batch;
+    E* dst = out + b * out_batch;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int r = r0 + i, c = c0 + threadIdx.x;
+        if (r < R && c < C) tile[i][threadIdx.x] = src[(size_t)r * C + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i, r = r0 + threadIdx.x;
+        if (r < R && c < C) {
+            const size_t orow = (size_t)(c / blk) * period + (size_t)which * blk + c % blk;
+            dst[orow * R + r] = tile[threadIdx.x][i];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,
+                          int npairs, void* xp, cudaStream_t s) {
+    if (npairs <= 0) return cudaSuccess;
+    const int row_vecs = d * elem_bytes / 16;
+    gather_rows<<<npairs, 128, 0, s>>>((const uint4*)x, perm, k, row_vecs, (uint4*)xp);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const int32_t* inv,
+                           int T, int k, int d, const void* resid, void* y, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const dim3 block(128), grid((d / 4 + 127) / 128, T);
+    if (dt == DType::BF16)
+        combine_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
+            Y, topk_w, inv, k, d, (const __nv_bfloat16*)resid, (__nv_bfloat16*)y);
+    else
+        combine_kernel<float><<<grid, block, 0, s>>>(Y, topk_w, inv, k, d, (const float*)resid,
+                                                      (float*)y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(DType dt, const void* h, const void* gamma, int T, int d, float eps,
+                           void* u, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    if (dt == DType::BF16)
+        rmsnorm_kernel<__nv_bfloat16><<<T, 256, 0, s>>>((const __nv_bfloat16*)h,
+                                                        (const __nv_bfloat16*)gamma, d, eps,
+                                                        (__nv_bfloat16*)u);
+    else
+        rmsnorm_kernel<float><<<T, 256, 0, s>>>((const float*)h, (const float*)gamma, d, eps,
+                                                (float*)u);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_remap(int elem_bytes, const void* in, void* out, int batch, int R,
+                                   int C, size_t in_batch, size_t out_batch, int blk, int period,
+                                   int which, cudaStream_t s) {
+    const dim3 block(32, 8), grid((C + 31) / 32, (R + 31) / 32, batch);
+    if (elem_bytes == 2)
+        transpose_remap<uint16_t><<<grid, block, 0, s>>>((const uint16_t*)in, (uint16_t*)out, R,
+                                                         C, in_batch, out_batch, blk, period,
+                                                         which);
+    else
+        transpose_remap<uint32_t><<<grid, block, 0, s>>>((const uint32_t*)in, (uint32_t*)out, R,
+                                                         C, in_batch, out_batch, blk, period,
+                                                         which);
+    return cudaGetLastError();
+}
+
+}  // namespace colibri

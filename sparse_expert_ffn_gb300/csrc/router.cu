@@ -1,0 +1,127 @@
+// Router: logits x . W_r (+ offset), per-token top-k, softmax over the k.
+//
+// zskr.cn "Colibri：面向MoE架构的C语言高效推理引擎解析" section 3.3 stage 2 (a
+// routing kernel with one warp per sequence, warp-level partial top-k, outputs
+// expert_indices [batch, top_k] and expert_scores [batch, top_k]); lmnt.cn
+// section 2.2 (route_tokens: logits, top-k, softmax over the top-k logits).
+//
+// One warp per token.  The token's row is widened to float in shared memory;
+// every logit is a warp dot product over d against one packed router row
+// (W_r repacked to [E, d], K contiguous).  Top-k runs as k rounds of a warp
+// arg-max over a 64-bit key (ordered value, then ~expert so that the lower
+// index wins a tie); NaN ranks below -inf.  The softmax is over the k
+// selected logits, with the largest subtracted first.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace colibri {
+
+namespace {
+
+constexpr int kRouterWarps = 4;
+
+// Total order on float logits as an unsigned key: larger value -> larger key,
+// -0 == +0, NaN below -inf.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    if (v != v) return 0u;
+    if (v == 0.0f) v = 0.0f;
+    uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_topk_simt(const T* __restrict__ x, const T* __restrict__ wr, const float* __restrict__ bias,
+                 int ntok, int d, int E, int k, int32_t* __restrict__ topk_idx,
+                 float* __restrict__ topk_w) {
+    extern __shared__ float smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kRouterWarps + warp;
+    if (t >= ntok) return;
+    float* xs = smem + warp * (d + 256);
+    float* logit = xs + d;
+
+    const T* xr = x + (size_t)t * d;
+    for (int i = lane; i < d; i += 32) xs[i] = to_f32(xr[i]);
+    __syncwarp();
+
+    for (int e = 0; e < E; ++e) {
+        const T* w = wr + (size_t)e * d;
+        float s = 0.f;
+        for (int i = lane * 8; i < d; i += 256) {
+            float wv[8];
+            load8(w + i, wv);
+            const float4 xa = *reinterpret_cast<const float4*>(xs + i);
+            const float4 xb = *reinterpret_cast<const float4*>(xs + i + 4);
+            s = fmaf(xa.x, wv[0], s);
+            s = fmaf(xa.y, wv[1], s);
+            s = fmaf(xa.z, wv[2], s);
+            s = fmaf(xa.w, wv[3], s);
+            s = fmaf(xb.x, wv[4], s);
+            s = fmaf(xb.y, wv[5], s);
+            s = fmaf(xb.z, wv[6], s);
+            s = fmaf(xb.w, wv[7], s);
+        }
+        s = warp_sum(s);
+        if (lane == 0) logit[e] = bias ? s + bias[e] : s;
+    }
+    __syncwarp();
+
+    // k rounds of a warp arg-max; each lane owns experts lane, lane+32, ...
+    uint32_t taken = 0;
+    int sel_e[8];
+    float sel_l[8];
+    for (int j = 0; j < k; ++j) {
+        unsigned long long best = 0ull;
+        for (int s = 0, e = lane; e < E; ++s, e += 32) {
+            if (taken & (1u << s)) continue;
+            unsigned long long key =
+                ((unsigned long long)order_key(logit[e]) << 32) | (uint32_t)(~(uint32_t)e);
+            best = key > best ? key : best;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+            best = other > best ? other : best;
+        }
+        const int e = (int)(~(uint32_t)(best & 0xffffffffull));
+        if ((e & 31) == lane) taken |= 1u << (e >> 5);
+        sel_e[j] = e;
+        sel_l[j] = logit[e];
+    }
+    if (lane == 0) {
+        const float m = sel_l[0];
+        float sum = 0.f;
+        for (int j = 0; j < k; ++j) sum += expf(sel_l[j] - m);
+        for (int j = 0; j < k; ++j) {
+            topk_idx[(size_t)t * k + j] = sel_e[j];
+            topk_w[(size_t)t * k + j] = expf(sel_l[j] - m) / sum;
+        }
+    }
+}
+
+}  // namespace
+
+size_t router_simt_smem(int d) { return (size_t)kRouterWarps * (d + 256) * sizeof(float); }
+
+cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const float* bias,
+                               int ntok, int d, int E, int k, int32_t* idx, float* w,
+                               cudaStream_t s) {
+    if (ntok <= 0) return cudaSuccess;
+    const dim3 grid((ntok + kRouterWarps - 1) / kRouterWarps), block(kRouterWarps * 32);
+    const size_t smem = router_simt_smem(d);
+    if (dt == DType::BF16) {
+        auto kern = router_topk_simt<__nv_bfloat16>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<grid, block, smem, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)wr, bias,
+                                       ntok, d, E, k, idx, w);
+    } else {
+        auto kern = router_topk_simt<float>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<grid, block, smem, s>>>((const float*)x, (const float*)wr, bias, ntok, d, E, k,
+                                       idx, w);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace colibri
