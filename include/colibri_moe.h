@@ -187,6 +187,46 @@ colibri_status_t colibri_profile_enable(colibri_moe_t* h, int enable);
  */
 colibri_status_t colibri_profile_read(colibri_moe_t* h, double* total_ms, uint64_t* launches);
 
+/*
+ * colibri_route_static - the routing stage of a layer (router logits, top-k,
+ * softmax over the k, dispatch permutation) for callers that cannot allocate
+ * device memory and have no handle.  The source pages have no counterpart of
+ * this call.
+ *
+ * Who needs it: code that may not call cudaMalloc — while a stream is being
+ * captured into a CUDA graph, inside a framework whose caching allocator owns
+ * the device memory, or in a loop that cannot take the device-wide
+ * synchronisation an allocation may cause.  Nothing is allocated: the call's
+ * intermediate data lives in one fixed file-scope device array inside the
+ * library (about 4.7 MiB, held by every GPU that loads the library until the
+ * process exits).
+ *
+ *   x           [T, d_model] device, dtype
+ *   w_router    [d_model, n_experts] device, dtype (the layout colibri_init takes)
+ *   router_bias [n_experts] device float32, or NULL (same meaning as in colibri_init)
+ *   topk_idx    [T, top_k] device int32, written (as colibri_get_routing)
+ *   topk_w      [T, top_k] device float32, written
+ *   counts      [n_experts] device int32, written
+ *   perm        [T * top_k] device int32, written
+ * Limits of the fixed array: d_model * n_experts <= 1048576 and
+ * T * top_k <= 131072; larger sizes return COLIBRI_ERR_INVALID_ARG before any
+ * CUDA call.  Shape rules as colibri_init (d_model % 64 == 0, n_experts <= 256,
+ * top_k <= 8: COLIBRI_ERR_UNSUPPORTED otherwise).
+ *
+ * Runs on the current device, ordered on `stream`, without waiting for it.
+ * The first call on a device looks up the array's device address and checks
+ * the architecture; make that first call before any stream capture.  All
+ * calls on a device share the array and it keeps the last call's contents:
+ * calls that overlap on the GPU (different streams, or unordered graph nodes)
+ * race and give wrong results.  Results equal those of colibri_forward +
+ * colibri_get_routing on a handle with the same weights.
+ */
+colibri_status_t colibri_route_static(const void* x, const void* w_router,
+                                      const float* router_bias, int32_t T, int32_t d_model,
+                                      int32_t n_experts, int32_t top_k, int32_t dtype,
+                                      int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                      int32_t* perm, void* stream);
+
 /* colibri_free - release everything the handle holds; NULL is allowed.
  * Synchronises the handle's device first. */
 void colibri_free(colibri_moe_t* h);

@@ -60,6 +60,7 @@ def _load():
         "colibri_workspace_bytes": ([P, U64P, U64P], I32),
         "colibri_profile_enable": ([P, ctypes.c_int], I32),
         "colibri_profile_read": ([P, ctypes.POINTER(ctypes.c_double), U64P], I32),
+        "colibri_route_static": ([P, P, P, I32, I32, I32, I32, I32, P, P, P, P, P], I32),
         "colibri_free": ([P], None),
         "colibri_status_str": ([I32], ctypes.c_char_p),
     }
@@ -74,7 +75,8 @@ _lib = None
 _C_NAMES = ("colibri_init", "colibri_forward", "colibri_forward_host",
             "colibri_rmsnorm_moe_residual", "colibri_get_routing", "colibri_set_executor",
             "colibri_check", "colibri_launch_count", "colibri_workspace_bytes",
-            "colibri_profile_enable", "colibri_profile_read", "colibri_free")
+            "colibri_profile_enable", "colibri_profile_read", "colibri_route_static",
+            "colibri_free")
 
 
 def library():

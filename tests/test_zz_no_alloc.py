@@ -1,0 +1,79 @@
+"""colibri_route_static: routing for callers that cannot allocate device memory.
+
+Callers that may not call cudaMalloc (code running under CUDA-graph stream
+capture, code inside a framework whose caching allocator owns the device
+memory, or loops that cannot afford the implicit synchronisation of an
+allocation) get the routing stage through this one entry point, which keeps
+its intermediate data in a fixed device array inside the library instead of
+allocating.  This test calls it through the C ABI twice in a row, with
+different shapes and token counts so that leftovers of the first call would
+show in the second, and checks each result against the handle-based path
+(colibri_forward + colibri_get_routing on the same weights and tokens).  The
+two paths run the same router and dispatch kernels on the same repacked
+weights, so the routing must agree bit for bit (stricter than the parity
+tolerances).  The file sorts last so that a run stopping at the first failure
+has already run every other test.
+"""
+
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _routing_through_static_entry(sef, x, wr, bias, shape):
+    T, k, E = x.shape[0], shape.top_k, shape.n_experts
+    dev = x.device
+    out = {
+        "topk_idx": torch.full((T, k), -1, dtype=torch.int32, device=dev),
+        "topk_w": torch.full((T, k), -1.0, dtype=torch.float32, device=dev),
+        "counts": torch.full((E,), -1, dtype=torch.int32, device=dev),
+        "perm": torch.full((T * k,), -1, dtype=torch.int32, device=dev),
+    }
+    st = sef.colibri_route_static(
+        x.data_ptr(), wr.data_ptr(), None if bias is None else bias.data_ptr(), T,
+        shape.d_model, E, k, sef.DTYPE_BF16 if x.dtype == torch.bfloat16 else sef.DTYPE_FP32,
+        out["topk_idx"].data_ptr(), out["topk_w"].data_ptr(), out["counts"].data_ptr(),
+        out["perm"].data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == sef.OK, sef.colibri_status_str(st)
+    torch.cuda.synchronize()
+    return out
+
+
+def test_route_static_matches_handle_path_on_two_calls_in_a_row(lib):
+    sef = lib
+    dev = torch.device("cuda", 0)
+    cases = [(synth.QWEN2, 64, 0), (synth.DEEPSEEK_MASKED, 37, 1)]
+    for shape, T, seed in cases:
+        wr = synth.router_weight(shape, seed, 0, dev)
+        wg, wu, wd = synth.expert_weights(shape, seed, 0, dev)
+        b = synth.router_offset(shape)
+        bias = None if b is None else b.to(dev)
+        x = synth.tokens(shape, T, seed, 0, dev)
+
+        got = _routing_through_static_entry(sef, x, wr, bias, shape)
+
+        layer = sef.MoELayer(wr, wg, wu, wd, shape.top_k, router_bias=b, max_tokens=T)
+        layer.forward(x)
+        want = layer.routing()
+        torch.cuda.synchronize()
+        assert layer.check() == sef.OK
+        layer.close()
+        for key in ("topk_idx", "topk_w", "counts", "perm"):
+            assert torch.equal(got[key], want[key]), f"{shape.name} T={T}: {key} differs"
+
+
+def test_route_static_rejects_sizes_beyond_its_array(lib):
+    sef = lib
+    dev = torch.device("cuda", 0)
+    buf = torch.zeros(16, dtype=torch.int32, device=dev)
+    p = buf.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    # T * top_k above 131072 pairs
+    assert sef.colibri_route_static(p, p, None, 65537, 128, 8, 2, sef.DTYPE_FP32,
+                                    p, p, p, p, s) == sef.ERR_INVALID_ARG
+    # d_model * n_experts above 1048576 elements
+    assert sef.colibri_route_static(p, p, None, 1, 8192, 256, 2, sef.DTYPE_BF16,
+                                    p, p, p, p, s) == sef.ERR_INVALID_ARG
