@@ -338,15 +338,19 @@ def run_ours(args):
     # decode-size sweep (context; the headline is the T above)
     sweep = {}
     if not args.no_sweep:
-        for Ts in (1, 16, 128):
+        for Ts, ex in ((1, "auto"), (1, "grouped"), (16, "auto"), (16, "stream"), (128, "auto")):
+            layer.set_executor(ex)
             xs = synth.tokens(shape, Ts, seed, 0, dev)
             ys = torch.empty_like(xs)
             ms_s, _, st_s = time_steps(layer, xs, ys, args.steps, args.warmup, world, stream, profile=True)
+            layer.set_executor("auto")
             ms_s = max_over_ranks(ms_s, world)
             cs = layer.routing()["counts"].cpu().numpy()
             a_s = algorithmic(shape, Ts, cs)
             t_step = ms_s / args.steps / 1e3
-            sweep[f"T{Ts}"] = {"tokens_per_s": round(world * Ts / t_step, 1),
+            sweep[f"T{Ts}" + ("" if ex == "auto" else "_" + ex)] = {
+                               "executor": "grouped" if "gather" in st_s else "stream",
+                               "tokens_per_s": round(world * Ts / t_step, 1),
                                "us_per_step": round(t_step * 1e6, 1),
                                "hbm_frac_of_measured": round(a_s["bytes"] / t_step / 1e9 / pk["hbm_gbs"], 4),
                                "active_experts": a_s["active_experts"],

@@ -15,7 +15,12 @@
 //   pass 2  the same walk again: position = warp base + running count + rank
 //           of the lane inside its match group.
 // The same kernel also writes the grouped GEMM's tile list: one entry per
-// block of `bm` consecutive pairs of one expert.
+// block of `bm` consecutive pairs of one expert.  Tiles are grouped into
+// raster bands that never cross an expert boundary (at most kMaxBand tiles of
+// one expert per band), so that the GEMM walks all of a band's m-tiles against
+// one weight block at a time and every weight block is streamed from HBM once.
+// tile_info[t] packs: bits 0-7 valid rows (1..bm), bits 8-15 the tile's
+// position inside its band, bits 16-23 the band's length in tiles.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,12 +29,13 @@ namespace colibri {
 namespace {
 
 constexpr int kDispatchWarps = 32;
+constexpr int kMaxBand = 32;
 
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_kernel(const int32_t* __restrict__ topk_idx, int n, int E, int32_t* __restrict__ counts,
                 int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                 int32_t* __restrict__ inv, int bm, int32_t* __restrict__ tile_expert,
-                int32_t* __restrict__ tile_row, int32_t* __restrict__ tile_rows,
+                int32_t* __restrict__ tile_row, int32_t* __restrict__ tile_info,
                 int32_t* __restrict__ num_tiles, int* __restrict__ status) {
     extern __shared__ int32_t sh[];
     int32_t* wcnt = sh;                           // [kDispatchWarps][E]
@@ -91,10 +97,12 @@ dispatch_kernel(const int32_t* __restrict__ topk_idx, int n, int E, int32_t* __r
         counts[e] = ecount[e];
         offsets[e] = eoff[e];
         const int32_t c = ecount[e];
-        for (int i = 0, tb = tbase[e]; i * bm < c; ++i, ++tb) {
+        const int nt = (c + bm - 1) / bm;
+        for (int i = 0, tb = tbase[e]; i < nt; ++i, ++tb) {
+            const int band_len = min(kMaxBand, nt - (i / kMaxBand) * kMaxBand);
             tile_expert[tb] = e;
             tile_row[tb] = eoff[e] + i * bm;
-            tile_rows[tb] = min(bm, c - i * bm);
+            tile_info[tb] = min(bm, c - i * bm) | ((i % kMaxBand) << 8) | (band_len << 16);
         }
     }
     if (threadIdx.x == 0) offsets[E] = eoff[E];
@@ -124,13 +132,13 @@ size_t dispatch_smem(int E) { return (size_t)(kDispatchWarps * E + 3 * E + 2) * 
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int n, int E, int32_t* counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int bm,
-                            int32_t* tile_expert, int32_t* tile_row, int32_t* tile_rows,
+                            int32_t* tile_expert, int32_t* tile_row, int32_t* tile_info,
                             int32_t* num_tiles, int* status, cudaStream_t s) {
     const size_t smem = dispatch_smem(E);
     cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dispatch_kernel<<<1, kDispatchWarps * 32, smem, s>>>(topk_idx, n, E, counts, offsets, perm,
                                                          inv, bm, tile_expert, tile_row,
-                                                         tile_rows, num_tiles, status);
+                                                         tile_info, num_tiles, status);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,10 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kSlots = 8;
+// 16-byte weight chunks per lane issued before their first use: enough bytes
+// in flight per warp to cover HBM latency without a shared-memory ring.
+constexpr int kAhead = 4;      // x2 rows (gate, up)
+constexpr int kAheadDown = 8;
 
 // Row of the packed gate/up weight: [E][f/128][2][128][d], which = 0 gate, 1 up.
 __device__ __forceinline__ size_t gu_row(int e, int n, int which, int f) {
@@ -53,18 +57,29 @@ ffn_up_stream(const T* __restrict__ x, const T* __restrict__ wgu,
             float ag[kSlots], au[kSlots];
 #pragma unroll
             for (int s = 0; s < kSlots; ++s) ag[s] = au[s] = 0.f;
-#pragma unroll 2
-            for (int i = lane * 8; i < d; i += 256) {
-                Raw8<T> wg, wu;
-                wg.load(g_row + i);
-                wu.load(u_row + i);
+            for (int i0 = lane * 8; i0 < d; i0 += 256 * kAhead) {
+                // issue every weight load of this stretch before the first use
+                Raw8<T> wg[kAhead], wu[kAhead];
 #pragma unroll
-                for (int s = 0; s < kSlots; ++s) {
-                    if (s < ns) {
-                        float xv[8];
-                        load8(xr[s] + i, xv);
-                        ag[s] += wg.dot(xv);
-                        au[s] += wu.dot(xv);
+                for (int a = 0; a < kAhead; ++a) {
+                    if (i0 + a * 256 < d) {
+                        wg[a].load(g_row + i0 + a * 256);
+                        wu[a].load(u_row + i0 + a * 256);
+                    }
+                }
+#pragma unroll
+                for (int a = 0; a < kAhead; ++a) {
+                    const int i = i0 + a * 256;
+                    if (i < d) {
+#pragma unroll
+                        for (int s = 0; s < kSlots; ++s) {
+                            if (s < ns) {
+                                float xv[8];
+                                load8(xr[s] + i, xv);
+                                ag[s] += wg[a].dot(xv);
+                                au[s] += wu[a].dot(xv);
+                            }
+                        }
                     }
                 }
             }
@@ -98,16 +113,23 @@ ffn_down_stream(const T* __restrict__ H, const T* __restrict__ wdT,
             float acc[kSlots];
 #pragma unroll
             for (int s = 0; s < kSlots; ++s) acc[s] = 0.f;
-#pragma unroll 2
-            for (int i = lane * 8; i < f; i += 256) {
-                Raw8<T> w;
-                w.load(w_row + i);
+            for (int i0 = lane * 8; i0 < f; i0 += 256 * kAheadDown) {
+                Raw8<T> w[kAheadDown];
 #pragma unroll
-                for (int s = 0; s < kSlots; ++s) {
-                    if (s < ns) {
-                        float hv[8];
-                        load8(H + (size_t)(off + s0 + s) * f + i, hv);
-                        acc[s] += w.dot(hv);
+                for (int a = 0; a < kAheadDown; ++a)
+                    if (i0 + a * 256 < f) w[a].load(w_row + i0 + a * 256);
+#pragma unroll
+                for (int a = 0; a < kAheadDown; ++a) {
+                    const int i = i0 + a * 256;
+                    if (i < f) {
+#pragma unroll
+                        for (int s = 0; s < kSlots; ++s) {
+                            if (s < ns) {
+                                float hv[8];
+                                load8(H + (size_t)(off + s0 + s) * f + i, hv);
+                                acc[s] += w[a].dot(hv);
+                            }
+                        }
                     }
                 }
             }

@@ -15,9 +15,10 @@
 // Work items are (m-tile, n-block) pairs.  An m-tile is up to 128 consecutive
 // pair rows of one expert (the dispatch kernel's tile list), so experts with
 // no token have no tile at all.  The kernel is persistent: CTA b takes work
-// b, b + grid, ...; work is walked in bands of kBand m-tiles, n-block-major
-// inside a band, so one weight block is reused from L2 by the band's m-tiles
-// of the same expert while the band's A rows stay resident.
+// b, b + grid, ...; work is walked band by band (a band = up to 32 m-tiles of
+// one expert), n-block-major inside a band, so one weight block is read from
+// HBM once and reused from L2 by all of the band's m-tiles, while the band's A
+// rows stay resident in L2 across the n-blocks.
 //
 // Roles (192 threads):
 //   warp 0      TMA producer: A and B tiles of 64 K-columns into a
@@ -44,13 +45,16 @@ constexpr int kBM = 128;          // tile rows (pairs)
 constexpr int kBN = 256;          // tile columns of B rows per MMA
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle atom of bf16
 constexpr int kStages = 4;
-constexpr int kBand = 8;          // m-tiles per raster band
 constexpr int kThreads = 192;
 constexpr int kAccCols = 256;     // TMEM columns per accumulator
 constexpr int kTmemCols = 512;    // two accumulators
 constexpr uint32_t kStageA = kBM * kBK * 2;   // 16 KB
 constexpr uint32_t kStageB = kBN * kBK * 2;   // 32 KB
 constexpr uint32_t kStageBytes = kStageA + kStageB;
+// Teardown waits (copies and MMAs already issued) use their own bound,
+// independent of the configurable wait limit, so that a CTA never exits with
+// a TMA copy or an MMA of its own still in flight.
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
 // ---------------------------------------------------------------- PTX wrappers
 
@@ -207,21 +211,25 @@ struct Work {
     int expert, row0, rows, nblk;
 };
 
-__device__ __forceinline__ Work decode_work(int w, int num_tiles, int n_blocks,
+// Work w -> (m-tile, n-block).  Bands of m-tiles (one expert each, from the
+// dispatch kernel) are laid out back to back; inside a band the m-tile index
+// runs fastest, so consecutive work items share one weight block.  The band
+// holding work w contains the tile w / n_blocks.
+__device__ __forceinline__ Work decode_work(int w, int n_blocks,
                                             const int32_t* __restrict__ tile_expert,
                                             const int32_t* __restrict__ tile_row,
-                                            const int32_t* __restrict__ tile_rows) {
-    const int per_band = kBand * n_blocks;
-    const int band = w / per_band;
-    const int rem = w - band * per_band;
-    const int m_lo = band * kBand;
-    const int cnt = min(kBand, num_tiles - m_lo);
-    const int nblk = rem / cnt;
-    const int m = m_lo + (rem - nblk * cnt);
+                                            const int32_t* __restrict__ tile_info) {
+    const int t = w / n_blocks;
+    const int info = tile_info[t];
+    const int first = t - ((info >> 8) & 0xFF);
+    const int len = (info >> 16) & 0xFF;
+    const int rem = w - first * n_blocks;
+    const int nblk = rem / len;
+    const int m = first + (rem - nblk * len);
     Work r;
     r.expert = tile_expert[m];
     r.row0 = tile_row[m];
-    r.rows = tile_rows[m];
+    r.rows = tile_info[m] & 0xFF;
     r.nblk = nblk;
     return r;
 }
@@ -280,8 +288,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t issued_phase[kStages];
             for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
             for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
-                const Work wk = decode_work(w, num_tiles, args.n_blocks, args.tile_expert,
-                                            args.tile_row, args.tile_rows);
+                const Work wk =
+                    decode_work(w, args.n_blocks, args.tile_expert, args.tile_row, args.tile_info);
                 const int b_row = wk.expert * args.b_rows_per_expert + wk.nblk * kBN;
                 bool ok = true;
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
@@ -302,7 +310,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             // Teardown: every copy this thread issued must have landed.
             for (int s = 0; s < kStages; ++s)
-                if (issued[s]) mbar_wait_drain(smem_u32(&full[s]), issued_phase[s], limit);
+                if (issued[s]) mbar_wait_drain(smem_u32(&full[s]), issued_phase[s], kDrainLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -342,7 +350,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             // Teardown: all MMAs issued by this thread complete before TMEM is freed.
             mma_commit(smem_u32(&mma_done[0]));
-            mbar_wait_drain(smem_u32(&mma_done[0]), 0, limit);
+            mbar_wait_drain(smem_u32(&mma_done[0]), 0, kDrainLimitNs);
         }
         __syncwarp();
     } else {
@@ -352,8 +360,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            const Work wk = decode_work(w, num_tiles, args.n_blocks, args.tile_expert,
-                                        args.tile_row, args.tile_rows);
+            const Work wk =
+                decode_work(w, args.n_blocks, args.tile_expert, args.tile_row, args.tile_info);
             const bool got =
                 mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, args.status, limit);
             // tcgen05.ld is warp-collective: the whole warp stops if any lane gave up.

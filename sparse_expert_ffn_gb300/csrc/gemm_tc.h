@@ -12,7 +12,7 @@ enum : int { kGateUp = 0, kDown = 1 };
 struct TcGemmArgs {
     const int32_t* tile_expert;  // [max_tiles] expert of each m-tile
     const int32_t* tile_row;     // [max_tiles] first pair row of each m-tile
-    const int32_t* tile_rows;    // [max_tiles] valid rows (<= 128) of each m-tile
+    const int32_t* tile_info;    // [max_tiles] rows | band position << 8 | band length << 16
     const int32_t* num_tiles;    // device scalar: number of m-tiles
     int n_blocks;                // n-blocks per expert
     int k_blocks;                // K / 64

@@ -53,7 +53,7 @@ struct colibri_moe {
     int32_t* inv = nullptr;
     int32_t* tile_expert = nullptr;
     int32_t* tile_row = nullptr;
-    int32_t* tile_rows = nullptr;
+    int32_t* tile_info = nullptr;
     int32_t* num_tiles = nullptr;
     int* status = nullptr;
     void* xp = nullptr;     // [max_pairs, d]
@@ -191,9 +191,11 @@ colibri_status_t pack(colibri_moe_t* h, const void* src, bool src_on_device,
 int choose_executor(const colibri_moe_t* h, int T) {
     if (h->cfg.executor != COLIBRI_EXEC_AUTO) return h->cfg.executor;
     if (!h->grouped_ok) return COLIBRI_EXEC_STREAM;
-    // Few pairs per expert: the FFN is a weight stream, CUDA cores keep up.
+    // Under one pair per expert on average the FFN is a pure weight stream
+    // over a few experts: CUDA cores keep up and the grouped GEMM would have
+    // too few work items to fill the GPU.  Above that the tensor cores win.
     const int64_t pairs = (int64_t)T * h->cfg.top_k;
-    return pairs <= 4 * (int64_t)h->cfg.n_experts ? COLIBRI_EXEC_STREAM : COLIBRI_EXEC_GROUPED;
+    return pairs <= (int64_t)h->cfg.n_experts ? COLIBRI_EXEC_STREAM : COLIBRI_EXEC_GROUPED;
 }
 
 cudaEvent_t take_event(colibri_moe_t* h) {
@@ -249,7 +251,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         Stage g(h, COLIBRI_STAGE_DISPATCH, s);
         st = g.done(launch_dispatch(h->topk_idx, npairs, E, h->counts, h->offsets, h->perm,
                                     h->inv, tc_gemm_block_m(), h->tile_expert, h->tile_row,
-                                    h->tile_rows, h->num_tiles, h->status, s), 1);
+                                    h->tile_info, h->num_tiles, h->status, s), 1);
         if (st != COLIBRI_OK) return st;
     }
     const int ex = choose_executor(h, T);
@@ -277,7 +279,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         TcGemmArgs a{};
         a.tile_expert = h->tile_expert;
         a.tile_row = h->tile_row;
-        a.tile_rows = h->tile_rows;
+        a.tile_info = h->tile_info;
         a.num_tiles = h->num_tiles;
         a.status = h->status;
         a.wait_limit_ns = h->wait_limit_ns;
@@ -428,7 +430,7 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     const size_t o_idx = carve(P * 4), o_w = carve(P * 4), o_cnt = carve((size_t)E * 4),
                  o_off = carve((size_t)(E + 1) * 4), o_perm = carve(P * 4), o_inv = carve(P * 4),
                  o_te = carve((size_t)h->max_tiles * 4), o_tr = carve((size_t)h->max_tiles * 4),
-                 o_trs = carve((size_t)h->max_tiles * 4), o_nt = carve(4), o_st = carve(4),
+                 o_tinfo = carve((size_t)h->max_tiles * 4), o_nt = carve(4), o_st = carve(4),
                  o_xp = h->grouped_ok ? carve(P * d * h->esz) : 0, o_h = carve(P * f * h->esz),
                  o_y = carve(P * d * 4), o_u = carve((size_t)M * d * h->esz),
                  o_xs = carve((size_t)M * d * h->esz), o_ys = carve((size_t)M * d * h->esz);
@@ -443,7 +445,7 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     h->inv = (int32_t*)(b + o_inv);
     h->tile_expert = (int32_t*)(b + o_te);
     h->tile_row = (int32_t*)(b + o_tr);
-    h->tile_rows = (int32_t*)(b + o_trs);
+    h->tile_info = (int32_t*)(b + o_tinfo);
     h->num_tiles = (int32_t*)(b + o_nt);
     h->status = (int*)(b + o_st);
     h->xp = h->grouped_ok ? (void*)(b + o_xp) : nullptr;

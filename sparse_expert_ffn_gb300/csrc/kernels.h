@@ -10,7 +10,6 @@ namespace colibri {
 
 enum class DType : int;
 
-size_t router_simt_smem(int d);
 cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const float* bias,
                                int ntok, int d, int E, int k, int32_t* idx, float* w,
                                cudaStream_t s);
@@ -18,7 +17,7 @@ cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const fl
 size_t dispatch_smem(int E);
 cudaError_t launch_dispatch(const int32_t* topk_idx, int n, int E, int32_t* counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int bm,
-                            int32_t* tile_expert, int32_t* tile_row, int32_t* tile_rows,
+                            int32_t* tile_expert, int32_t* tile_row, int32_t* tile_info,
                             int32_t* num_tiles, int* status, cudaStream_t s);
 
 cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* counts,

@@ -42,8 +42,8 @@ constexpr size_t kOffOffsets = kOffRouter + round256((size_t)kStaticMaxRouterEle
 constexpr size_t kOffInv = kOffOffsets + round256(257 * 4);
 constexpr size_t kOffTileExpert = kOffInv + round256((size_t)kStaticMaxPairs * 4);
 constexpr size_t kOffTileRow = kOffTileExpert + round256((size_t)kStaticMaxTiles * 4);
-constexpr size_t kOffTileRows = kOffTileRow + round256((size_t)kStaticMaxTiles * 4);
-constexpr size_t kOffNumTiles = kOffTileRows + round256((size_t)kStaticMaxTiles * 4);
+constexpr size_t kOffTileInfo = kOffTileRow + round256((size_t)kStaticMaxTiles * 4);
+constexpr size_t kOffNumTiles = kOffTileInfo + round256((size_t)kStaticMaxTiles * 4);
 constexpr size_t kOffStatus = kOffNumTiles + 256;
 constexpr size_t kStaticScratchBytes = kOffStatus + 256;
 
@@ -110,7 +110,7 @@ extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_ro
     int32_t* inv = reinterpret_cast<int32_t*>(s + kOffInv);
     int32_t* tile_expert = reinterpret_cast<int32_t*>(s + kOffTileExpert);
     int32_t* tile_row = reinterpret_cast<int32_t*>(s + kOffTileRow);
-    int32_t* tile_rows = reinterpret_cast<int32_t*>(s + kOffTileRows);
+    int32_t* tile_info = reinterpret_cast<int32_t*>(s + kOffTileInfo);
     int32_t* num_tiles = reinterpret_cast<int32_t*>(s + kOffNumTiles);
     int* status = reinterpret_cast<int*>(s + kOffStatus);
 
@@ -126,6 +126,6 @@ extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_ro
         e = launch_router_simt(dt, x, wr_packed, router_bias, T, d, E, k, topk_idx, topk_w, cs);
     if (e == cudaSuccess)
         e = launch_dispatch(topk_idx, T * k, E, counts, offsets, perm, inv, kStaticTileRows,
-                            tile_expert, tile_row, tile_rows, num_tiles, status, cs);
+                            tile_expert, tile_row, tile_info, num_tiles, status, cs);
     return e == cudaSuccess ? COLIBRI_OK : COLIBRI_ERR_CUDA;
 }

@@ -5,9 +5,9 @@
 // expert_indices [batch, top_k] and expert_scores [batch, top_k]); lmnt.cn
 // section 2.2 (route_tokens: logits, top-k, softmax over the top-k logits).
 //
-// One warp per token.  The token's row is widened to float in shared memory;
-// every logit is a warp dot product over d against one packed router row
-// (W_r repacked to [E, d], K contiguous).  Top-k runs as k rounds of a warp
+// The token's row is widened to float in shared memory; every logit is a warp
+// dot product over d against one packed router row (W_r repacked to [E, d],
+// K contiguous).  Top-k runs as k rounds of a warp
 // arg-max over a 64-bit key (ordered value, then ~expert so that the lower
 // index wins a tie); NaN ranks below -inf.  The softmax is over the k
 // selected logits, with the largest subtracted first.
@@ -18,7 +18,7 @@ namespace colibri {
 
 namespace {
 
-constexpr int kRouterWarps = 4;
+constexpr int kRouterWarps = 8;
 
 // Total order on float logits as an unsigned key: larger value -> larger key,
 // -0 == +0, NaN below -inf.
@@ -29,43 +29,54 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-template <typename T>
+// One CTA of kRouterWarps warps routes kRouterWarps / kWarpsPerToken tokens;
+// the kWarpsPerToken warps of a token split its experts (e = sub, sub + W, ...).
+// Large batches use one warp per token; small ones spread a token over all
+// warps of the CTA so that the E dot products run in parallel.
+template <typename T, int kWarpsPerToken>
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_topk_simt(const T* __restrict__ x, const T* __restrict__ wr, const float* __restrict__ bias,
                  int ntok, int d, int E, int k, int32_t* __restrict__ topk_idx,
                  float* __restrict__ topk_w) {
     extern __shared__ float smem[];
+    constexpr int kTokens = kRouterWarps / kWarpsPerToken;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kRouterWarps + warp;
-    if (t >= ntok) return;
-    float* xs = smem + warp * (d + 256);
+    const int slot = warp / kWarpsPerToken, sub = warp % kWarpsPerToken;
+    const int t = blockIdx.x * kTokens + slot;
+    const bool live = t < ntok;
+    float* xs = smem + slot * (d + 256);
     float* logit = xs + d;
 
-    const T* xr = x + (size_t)t * d;
-    for (int i = lane; i < d; i += 32) xs[i] = to_f32(xr[i]);
-    __syncwarp();
-
-    for (int e = 0; e < E; ++e) {
-        const T* w = wr + (size_t)e * d;
-        float s = 0.f;
-        for (int i = lane * 8; i < d; i += 256) {
-            float wv[8];
-            load8(w + i, wv);
-            const float4 xa = *reinterpret_cast<const float4*>(xs + i);
-            const float4 xb = *reinterpret_cast<const float4*>(xs + i + 4);
-            s = fmaf(xa.x, wv[0], s);
-            s = fmaf(xa.y, wv[1], s);
-            s = fmaf(xa.z, wv[2], s);
-            s = fmaf(xa.w, wv[3], s);
-            s = fmaf(xb.x, wv[4], s);
-            s = fmaf(xb.y, wv[5], s);
-            s = fmaf(xb.z, wv[6], s);
-            s = fmaf(xb.w, wv[7], s);
-        }
-        s = warp_sum(s);
-        if (lane == 0) logit[e] = bias ? s + bias[e] : s;
+    if (live) {
+        const T* xr = x + (size_t)t * d;
+        for (int i = sub * 32 + lane; i < d; i += 32 * kWarpsPerToken) xs[i] = to_f32(xr[i]);
     }
-    __syncwarp();
+    __syncthreads();
+
+    if (live) {
+        for (int e = sub; e < E; e += kWarpsPerToken) {
+            const T* w = wr + (size_t)e * d;
+            float s = 0.f;
+            for (int i = lane * 8; i < d; i += 256) {
+                float wv[8];
+                load8(w + i, wv);
+                const float4 xa = *reinterpret_cast<const float4*>(xs + i);
+                const float4 xb = *reinterpret_cast<const float4*>(xs + i + 4);
+                s = fmaf(xa.x, wv[0], s);
+                s = fmaf(xa.y, wv[1], s);
+                s = fmaf(xa.z, wv[2], s);
+                s = fmaf(xa.w, wv[3], s);
+                s = fmaf(xb.x, wv[4], s);
+                s = fmaf(xb.y, wv[5], s);
+                s = fmaf(xb.z, wv[6], s);
+                s = fmaf(xb.w, wv[7], s);
+            }
+            s = warp_sum(s);
+            if (lane == 0) logit[e] = bias ? s + bias[e] : s;
+        }
+    }
+    __syncthreads();
+    if (!live || sub != 0) return;
 
     // k rounds of a warp arg-max; each lane owns experts lane, lane+32, ...
     uint32_t taken = 0;
@@ -100,28 +111,32 @@ router_topk_simt(const T* __restrict__ x, const T* __restrict__ wr, const float*
     }
 }
 
-}  // namespace
+template <typename T, int kWarpsPerToken>
+cudaError_t launch_router_t(const void* x, const void* wr, const float* bias, int ntok, int d,
+                            int E, int k, int32_t* idx, float* w, cudaStream_t s) {
+    constexpr int kTokens = kRouterWarps / kWarpsPerToken;
+    const dim3 grid((ntok + kTokens - 1) / kTokens), block(kRouterWarps * 32);
+    const size_t smem = (size_t)kTokens * (d + 256) * sizeof(float);
+    auto kern = router_topk_simt<T, kWarpsPerToken>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<grid, block, smem, s>>>((const T*)x, (const T*)wr, bias, ntok, d, E, k, idx, w);
+    return cudaGetLastError();
+}
 
-size_t router_simt_smem(int d) { return (size_t)kRouterWarps * (d + 256) * sizeof(float); }
+}  // namespace
 
 cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const float* bias,
                                int ntok, int d, int E, int k, int32_t* idx, float* w,
                                cudaStream_t s) {
     if (ntok <= 0) return cudaSuccess;
-    const dim3 grid((ntok + kRouterWarps - 1) / kRouterWarps), block(kRouterWarps * 32);
-    const size_t smem = router_simt_smem(d);
-    if (dt == DType::BF16) {
-        auto kern = router_topk_simt<__nv_bfloat16>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<grid, block, smem, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)wr, bias,
-                                       ntok, d, E, k, idx, w);
-    } else {
-        auto kern = router_topk_simt<float>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<grid, block, smem, s>>>((const float*)x, (const float*)wr, bias, ntok, d, E, k,
-                                       idx, w);
-    }
-    return cudaGetLastError();
+    // Few tokens: spread every token over a whole CTA; many: two warps per
+    // token, four tokens per CTA (70 KB of shared memory at d = 4096).
+    const bool small = ntok <= 256;
+    if (dt == DType::BF16)
+        return small ? launch_router_t<__nv_bfloat16, kRouterWarps>(x, wr, bias, ntok, d, E, k, idx, w, s)
+                     : launch_router_t<__nv_bfloat16, 2>(x, wr, bias, ntok, d, E, k, idx, w, s);
+    return small ? launch_router_t<float, kRouterWarps>(x, wr, bias, ntok, d, E, k, idx, w, s)
+                 : launch_router_t<float, 2>(x, wr, bias, ntok, d, E, k, idx, w, s);
 }
 
 }  // namespace colibri

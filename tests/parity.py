@@ -118,3 +118,22 @@ def check_output(case: Case, x64, y, r, l, tokens=None):
     tol = Y_RTOL[case.shape.dtype]
     assert err <= tol, f"max|err|/max|ref| = {err:.3e} > {tol}"
     return err
+
+
+def stack_case_layers(n_layers: int, seed: int, max_tokens: int):
+    """The decode stack's layers (Mixtral-shaped) as library handles, one per layer.
+
+    Returns (layers, gamma) with gamma = ones [d] bf16 on the device.  Layer l
+    draws its weights with layer index l of the seeded generator."""
+    import sparse_expert_ffn_gb300 as sef
+    shape = synth.MIXTRAL
+    dev = torch.device("cuda", 0)
+    layers = []
+    for l in range(n_layers):
+        wr = synth.router_weight(shape, seed, l, dev)
+        wg, wu, wd = synth.expert_weights(shape, seed, l, dev)
+        layers.append(sef.MoELayer(wr, wg, wu, wd, shape.top_k, max_tokens=max_tokens))
+        del wr, wg, wu, wd
+    torch.cuda.empty_cache()
+    gamma = torch.ones(shape.d_model, dtype=torch.bfloat16, device=dev)
+    return layers, gamma

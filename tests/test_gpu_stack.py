@@ -1,0 +1,70 @@
+"""GPU parity of the decode stack: 32 Mixtral-shaped layers, each
+RMSNorm -> MoE -> residual, batches of 1, 8 and 64 single-token sequences.
+
+Routing decisions compound across layers, so parity is checked per layer on
+identical inputs (teacher-forced): the GPU's input to layer l is handed to the
+oracle's stack layer and both outputs are compared.  The end-to-end drift of
+the last hidden state against an oracle run of all 32 layers is not gated."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import Y_RTOL, stack_case_layers
+
+pytestmark = pytest.mark.gpu
+
+N_LAYERS = synth.STACK_LAYERS
+CHECK_LAYERS = (0, N_LAYERS - 1)
+
+
+@pytest.fixture(scope="module")
+def stack(lib):
+    layers, gamma = stack_case_layers(N_LAYERS, seed=0, max_tokens=64)
+    yield layers, gamma
+    for l in layers:
+        l.close()
+    torch.cuda.empty_cache()
+
+
+def _layer_weights64(l, seed=0):
+    shape = synth.MIXTRAL
+    wr = synth.router_weight(shape, seed, l, "cuda")
+    wg, wu, wd = synth.expert_weights(shape, seed, l, "cuda")
+    out = tuple(oracle.to_f64(t.cpu()) for t in (wr, wg, wu, wd))
+    del wr, wg, wu, wd
+    torch.cuda.empty_cache()
+    return out
+
+
+def test_stack_teacher_forced_layers(stack):
+    layers, gamma = stack
+    shape = synth.MIXTRAL
+    weights = {l: _layer_weights64(l) for l in CHECK_LAYERS}
+    g64 = np.ones(shape.d_model)
+    for B in synth.STACK_BATCHES:
+        h = synth.tokens(shape, B, seed=7, device="cuda")           # bf16 N(0,1) hidden state
+        for l, layer in enumerate(layers):
+            h_in = h.clone()
+            layer.rmsnorm_moe_residual(h, gamma, synth.STACK_EPS)
+            if l in CHECK_LAYERS:
+                torch.cuda.synchronize()
+                assert layer.check() == 0
+                r = {k: v.cpu().numpy() for k, v in layer.routing().items()}
+                h64 = oracle.to_f64(h_in.cpu())
+                ref = oracle.stack_layer(h64, g64, synth.STACK_EPS, *weights[l], shape.top_k)
+                # routing on the oracle's normalised input; near-ties allowed
+                near = oracle.near_tie_tokens(ref["u"], weights[l][0], ref["logits"], shape.top_k)
+                bad = (r["topk_idx"] != ref["topk_idx"]).any(axis=1) & ~near
+                assert not bad.any(), f"B={B} layer {l}: routing differs on {int(bad.sum())} tokens"
+                if not near.any():
+                    assert np.array_equal(r["counts"], ref["counts"])
+                    got = oracle.to_f64(h.cpu())
+                    err = np.abs(got - ref["h_out"]).max() / np.abs(ref["h_out"]).max()
+                    assert err <= Y_RTOL["bf16"], f"B={B} layer {l}: {err:.3e}"
+                    # the MoE increment itself, against the oracle's y
+                    dy = np.abs((got - h64) - ref["y"]).max() / np.abs(ref["y"]).max()
+                    assert dy <= 5e-2, f"B={B} layer {l}: increment error {dy:.3e}"
+        assert torch.isfinite(h.float()).all()
