@@ -181,15 +181,19 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- our arm
 
 
-def dist_setup(args):
+def dist_setup(args, backend="nccl"):
+    """Rank layout from the torchrun environment; one rank per GPU."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     return world, rank, local
 
 
@@ -199,14 +203,25 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """The largest value of v over all ranks (the slowest rank's time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(base_seed, rank):
+    """Each rank runs its own replica layer on its own synthetic tokens."""
+    return base_seed + rank
+
+
+def job_throughput(world, tokens_per_rank, steps, max_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
 
 
 def time_steps(layer, x, y, steps, warmup, world, stream, profile=False):
@@ -263,7 +278,7 @@ def run_ours(args):
     clocks = ClockSampler(gpu_id) if rank == 0 else None
 
     # weights: layer seed per rank (replicas over independent synthetic layers)
-    seed = args.seed + rank
+    seed = rank_seed(args.seed, rank)
     wr = synth.router_weight(shape, seed, 0, dev)
     wg, wu, wd = synth.expert_weights(shape, seed, 0, dev)
     max_t = max(T, 128)
@@ -288,7 +303,7 @@ def run_ours(args):
     counts = r["counts"].cpu().numpy()
     alg = algorithmic(shape, T, counts)
     step_ms = ms / args.steps
-    value = world * T * args.steps / (ms / 1e3)
+    value = job_throughput(world, T, args.steps, ms)
 
     # roofline of the dominant kernel (largest share of the timed region)
     dom = max(stages, key=lambda s: stages[s]["ms_total"])
@@ -338,7 +353,7 @@ def run_ours(args):
     # decode-size sweep (context; the headline is the T above)
     sweep = {}
     if not args.no_sweep:
-        for Ts, ex in ((1, "auto"), (1, "grouped"), (16, "auto"), (16, "stream"), (128, "auto")):
+        for Ts, ex in ((1, "auto"), (1, "stream"), (16, "auto"), (128, "auto"), (512, "auto")):
             layer.set_executor(ex)
             xs = synth.tokens(shape, Ts, seed, 0, dev)
             ys = torch.empty_like(xs)

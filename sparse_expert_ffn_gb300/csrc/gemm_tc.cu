@@ -3,14 +3,18 @@
 //
 // zskr.cn "Colibri：面向MoE架构的C语言高效推理引擎解析" section 3.3 stages 3-4
 // (the tokens of one expert batched into one GEMM; gate_proj, up_proj, SiLU and
-// down_proj per expert).  Two instantiations:
+// down_proj per expert).  Three instantiations:
 //
 //   kGateUp  A = Xp (tokens of each expert, consecutive rows) [pairs, d]
 //            B = packed [W_gate^T | W_up^T] blocks of 128 rows each, K = d
 //            one tile = 128 rows x (128 gate + 128 up) columns; the epilogue
 //            reads both halves from TMEM and writes H = silu(G) * U (bf16).
 //   kDown    A = H [pairs, f], B = W_down^T [d, f] per expert, K = f
-//            one tile = 128 rows x 256 output features, written as float32.
+//            one tile = 128 rows x 256 output features, written as float32
+//            (optionally one K slice of it: split-K for small batches).
+//   kRouter  A = x [T, d] (the caller's tokens), B = packed router [E_pad, d]:
+//            the router logits of 128 tokens per tile (N = E rounded up to 16),
+//            top-k and softmax in the epilogue (p1 section 3.3 stage 2).
 //
 // Work items are (m-tile, n-block) pairs.  An m-tile is up to 128 consecutive
 // pair rows of one expert (the dispatch kernel's tile list), so experts with
@@ -208,17 +212,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 // ---------------------------------------------------------------- work decode
 
 struct Work {
-    int expert, row0, rows, nblk;
+    int expert, row0, rows, nblk, split;
 };
 
 // Work w -> (m-tile, n-block).  Bands of m-tiles (one expert each, from the
 // dispatch kernel) are laid out back to back; inside a band the m-tile index
 // runs fastest, so consecutive work items share one weight block.  The band
 // holding work w contains the tile w / n_blocks.
-__device__ __forceinline__ Work decode_work(int w, int n_blocks,
+__device__ __forceinline__ Work decode_work(int w, int n_blocks, int k_splits,
                                             const int32_t* __restrict__ tile_expert,
                                             const int32_t* __restrict__ tile_row,
                                             const int32_t* __restrict__ tile_info) {
+    // (n-block, K slice) pairs act as one combined n index, slices fastest
+    n_blocks *= k_splits;
     const int t = w / n_blocks;
     const int info = tile_info[t];
     const int first = t - ((info >> 8) & 0xFF);
@@ -230,8 +236,35 @@ __device__ __forceinline__ Work decode_work(int w, int n_blocks,
     r.expert = tile_expert[m];
     r.row0 = tile_row[m];
     r.rows = tile_info[m] & 0xFF;
-    r.nblk = nblk;
+    r.nblk = nblk / k_splits;
+    r.split = nblk - r.nblk * k_splits;
     return r;
+}
+
+// Router mode: dense m-tiles of 128 consecutive tokens, one n-block.
+__device__ __forceinline__ Work dense_work(int w, int rows_total) {
+    Work r;
+    r.expert = 0;
+    r.row0 = w * kBM;
+    r.rows = min(kBM, rows_total - r.row0);
+    r.nblk = 0;
+    r.split = 0;
+    return r;
+}
+
+template <int kMode>
+__device__ __forceinline__ Work get_work(int w, const TcGemmArgs& a) {
+    if constexpr (kMode == kRouter) return dense_work(w, a.dense_rows);
+    else return decode_work(w, a.n_blocks, a.k_splits, a.tile_expert, a.tile_row, a.tile_info);
+}
+
+// Total order on float logits as an unsigned key (as the CUDA-core router):
+// larger value -> larger key, -0 == +0, NaN below -inf.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    if (v != v) return 0u;
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -256,8 +289,13 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_tiles = *args.num_tiles;
-    const int total = num_tiles * args.n_blocks;
+    const int num_tiles =
+        kMode == kRouter ? (args.dense_rows + kBM - 1) / kBM : *args.num_tiles;
+    const int total = num_tiles * args.n_blocks * args.k_splits;
+    // B tile rows = MMA N: 256, or the padded expert count for the router
+    const int bn = kMode == kRouter ? args.bn_rows : kBN;
+    const uint32_t stage_tx = kStageA + (uint32_t)bn * kBK * 2;
+    const int kb_per_split = (args.k_blocks + args.k_splits - 1) / args.k_splits;
     const uint64_t limit = args.wait_limit_ns;
 
     if (threadIdx.x == 0) {
@@ -287,19 +325,21 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             bool issued[kStages];
             uint32_t issued_phase[kStages];
             for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
-            for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
-                const Work wk =
-                    decode_work(w, args.n_blocks, args.tile_expert, args.tile_row, args.tile_info);
+            for (int w = blockIdx.x; w < total && !*abort_flag && !args.stall_producer;
+                 w += gridDim.x) {
+                const Work wk = get_work<kMode>(w, args);
                 const int b_row = wk.expert * args.b_rows_per_expert + wk.nblk * kBN;
+                const int kb0 = wk.split * kb_per_split;
+                const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
                 bool ok = true;
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, args.status,
                                    limit)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_u32(&full[stage]);
-                    mbar_expect_tx(fb, kStageBytes);
+                    mbar_expect_tx(fb, stage_tx);
                     tma_load_2d(smem_u32(stage_a + stage * kStageA), &tmA, kb * kBK, wk.row0, fb);
                     tma_load_2d(smem_u32(stage_b + stage * kStageB), &tmB, kb * kBK, b_row, fb);
                     issued[stage] = true;
@@ -316,19 +356,22 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+            const uint32_t idesc = idesc_bf16(kBM, bn);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+                const Work wk = get_work<kMode>(w, args);
+                const int kb0 = wk.split * kb_per_split;
+                const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
                 if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1, abort_flag, args.status,
                                limit))
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
                 bool ok = true;
-                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.status,
                                    limit)) {
                         ok = false;
@@ -340,7 +383,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                     for (int ks = 0; ks < kBK / 16; ++ks)
                         // +32 bytes of K per step inside the swizzle atom (encoded >> 4)
-                        mma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, idesc, (kb | ks) != 0);
+                        mma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, idesc, (kb > kb0) || ks != 0);
                     mma_commit(smem_u32(&empty[stage]));
                     if (++stage == kStages) stage = 0, phase ^= 1;
                 }
@@ -360,8 +403,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            const Work wk =
-                decode_work(w, args.n_blocks, args.tile_expert, args.tile_row, args.tile_info);
+            const Work wk = get_work<kMode>(w, args);
             const bool got =
                 mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, args.status, limit);
             // tcgen05.ld is warp-collective: the whole warp stops if any lane gave up.
@@ -370,7 +412,58 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
             const bool live = row < wk.rows;
             const size_t orow = (size_t)(wk.row0 + row);
-            if constexpr (kMode == kGateUp) {
+            if constexpr (kMode == kRouter) {
+                // Logits of this thread's token: the E accumulator columns
+                // (+ offset).  Top-k by insertion over a key that puts the
+                // larger logit first and the lower expert id first on ties,
+                // then the softmax over the k (as the CUDA-core router).
+                unsigned long long key[8];
+                float val[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) key[j] = 0ull, val[j] = 0.f;
+                const int E = args.n_experts;
+#pragma unroll 1
+                for (int c = 0; c < bn; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = c + i;
+                        if (e < E) {
+                            float l = __uint_as_float(v[i]);
+                            if (args.bias) l += args.bias[e];
+                            unsigned long long kk =
+                                ((unsigned long long)order_key(l) << 32) | (uint32_t)(~(uint32_t)e);
+                            float vv = l;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                if (kk > key[j]) {
+                                    const unsigned long long tk = key[j];
+                                    const float tv = val[j];
+                                    key[j] = kk, val[j] = vv;
+                                    kk = tk, vv = tv;
+                                }
+                            }
+                        }
+                    }
+                }
+                if (live) {
+                    const int k = args.top_k;
+                    const size_t t = (size_t)(wk.row0 + row);
+                    float sum = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j < k) sum += expf(val[j] - val[0]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (j < k) {
+                            args.topk_idx[t * k + j] = (int)(~(uint32_t)(key[j] & 0xffffffffull));
+                            args.topk_w[t * k + j] = expf(val[j] - val[0]) / sum;
+                        }
+                    }
+                }
+            } else if constexpr (kMode == kGateUp) {
                 __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
 #pragma unroll 1
                 for (int c = 0; c < 128 / 32; ++c) {
@@ -396,7 +489,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                 }
             } else {
-                float* Y = reinterpret_cast<float*>(args.out);
+                float* Y = reinterpret_cast<float*>(args.out) + wk.split * args.out_split_stride;
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t v[32];
@@ -471,6 +564,10 @@ cudaError_t launch_tc_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& 
     if (grid <= 0) return cudaSuccess;
     if (mode == kGateUp) {
         auto k = grouped_gemm_tc<kGateUp>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kThreads, smem, s>>>(tmA, tmB, args);
+    } else if (mode == kRouter) {
+        auto k = grouped_gemm_tc<kRouter>;
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         k<<<grid, kThreads, smem, s>>>(tmA, tmB, args);
     } else {

@@ -7,7 +7,7 @@
 
 namespace colibri {
 
-enum : int { kGateUp = 0, kDown = 1 };
+enum : int { kGateUp = 0, kDown = 1, kRouter = 2 };
 
 struct TcGemmArgs {
     const int32_t* tile_expert;  // [max_tiles] expert of each m-tile
@@ -16,11 +16,23 @@ struct TcGemmArgs {
     const int32_t* num_tiles;    // device scalar: number of m-tiles
     int n_blocks;                // n-blocks per expert
     int k_blocks;                // K / 64
+    int k_splits;                // K split into this many slices (1 = none); every slice
+                                 // non-empty; slice s writes out + s * out_split_stride
     int b_rows_per_expert;       // rows of the packed B operand per expert
     void* out;                   // H (bf16, kGateUp) or Y (float32, kDown)
     int out_ld;                  // row stride of `out` in elements
+    size_t out_split_stride;     // elements between the outputs of two K slices
     int* status;                 // device status word (DEV_TIMEOUT on a wait that gave up)
     uint64_t wait_limit_ns;      // bound of every mbarrier wait
+    // router mode (kRouter): dense tiles over dense_rows tokens, MMA N = bn_rows
+    int dense_rows;
+    int bn_rows;
+    int n_experts, top_k;
+    const float* bias;           // [E] or null
+    int32_t* topk_idx;           // [T, k]
+    float* topk_w;               // [T, k]
+    int stall_producer;          // failure-detection tests only: issue no TMA copy, so
+                                 // the first wait on a full stage runs out its bound
 };
 
 size_t tc_gemm_smem_bytes();

@@ -65,8 +65,9 @@ struct colibri_moe {
     int max_pairs = 0;
     int max_tiles = 0;
     bool grouped_ok = false;
-    CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT;
+    CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT, tm_wr;
     uint64_t wait_limit_ns = 2000000000ull;
+    bool stall_tma = false;  // failure-detection tests (COLIBRI_TEST_STALL_TMA=1)
     int last_T = 0;
     uint64_t launches = 0;
     colibri_status_t sticky = COLIBRI_OK;
@@ -102,6 +103,13 @@ struct AllocCounter {
 };
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Split-K of the down projection: only for batches of at most kSplitMaxPairs
+// (token, slot) pairs, into at most kMaxKSplit slices; Y holds room for them.
+constexpr int kSplitMaxPairs = 2048;
+// Batches from this many tokens route on the tensor cores.
+constexpr int kTcRouterMinTokens = 512;
+constexpr int kMaxKSplit = 8;
 
 struct DeviceGuard {
     int prev = -1;
@@ -190,12 +198,12 @@ colibri_status_t pack(colibri_moe_t* h, const void* src, bool src_on_device,
 
 int choose_executor(const colibri_moe_t* h, int T) {
     if (h->cfg.executor != COLIBRI_EXEC_AUTO) return h->cfg.executor;
-    if (!h->grouped_ok) return COLIBRI_EXEC_STREAM;
-    // Under one pair per expert on average the FFN is a pure weight stream
-    // over a few experts: CUDA cores keep up and the grouped GEMM would have
-    // too few work items to fill the GPU.  Above that the tensor cores win.
-    const int64_t pairs = (int64_t)T * h->cfg.top_k;
-    return pairs <= (int64_t)h->cfg.n_experts ? COLIBRI_EXEC_STREAM : COLIBRI_EXEC_GROUPED;
+    // bf16: the TMA-fed grouped GEMM streams the active experts' weights
+    // faster than the CUDA-core kernels at every batch size measured (one
+    // token included, with split-K on the down projection); CUDA cores run
+    // the float32 layer and shapes the tensor-core path does not take.
+    (void)T;
+    return h->grouped_ok ? COLIBRI_EXEC_GROUPED : COLIBRI_EXEC_STREAM;
 }
 
 cudaEvent_t take_event(colibri_moe_t* h) {
@@ -241,7 +249,30 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     const int E = c.n_experts, k = c.top_k, d = c.d_model, f = c.d_ff;
     const int npairs = T * k;
     colibri_status_t st;
-    {
+    if (h->grouped_ok && T >= kTcRouterMinTokens) {
+        // Large batch: the router logits are a [T, d] x [d, E] GEMM on the
+        // tensor cores, top-k and softmax in its epilogue.
+        CUtensorMap tm_x;
+        if (!make_tmap_bf16(&tm_x, x, (uint64_t)T, (uint64_t)d, 128)) return COLIBRI_ERR_CUDA;
+        TcGemmArgs a{};
+        a.dense_rows = T;
+        a.bn_rows = h->e_pad;
+        a.n_experts = E;
+        a.top_k = k;
+        a.bias = h->bias;
+        a.topk_idx = h->topk_idx;
+        a.topk_w = h->topk_w;
+        a.n_blocks = 1;
+        a.k_blocks = d / 64;
+        a.k_splits = 1;
+        a.status = h->status;
+        a.wait_limit_ns = h->wait_limit_ns;
+        a.stall_producer = h->stall_tma ? 1 : 0;
+        const int grid = std::min((T + tc_gemm_block_m() - 1) / tc_gemm_block_m(), h->num_sms);
+        Stage g(h, COLIBRI_STAGE_ROUTER, s);
+        st = g.done(launch_tc_gemm(kRouter, tm_x, h->tm_wr, a, grid, s), 1);
+        if (st != COLIBRI_OK) return st;
+    } else {
         Stage g(h, COLIBRI_STAGE_ROUTER, s);
         st = g.done(launch_router_simt(h->dt, x, h->wr, h->bias, T, d, E, k, h->topk_idx,
                                        h->topk_w, s), 1);
@@ -255,6 +286,8 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         if (st != COLIBRI_OK) return st;
     }
     const int ex = choose_executor(h, T);
+    int nsplit = 1;
+    size_t split_stride = 0;
     if (ex == COLIBRI_EXEC_STREAM) {
         {
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
@@ -283,9 +316,12 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.num_tiles = h->num_tiles;
         a.status = h->status;
         a.wait_limit_ns = h->wait_limit_ns;
+        a.stall_producer = h->stall_tma ? 1 : 0;
         // gate/up: N = 2f in blocks of 256 rows (128 gate + 128 up), K = d
         a.n_blocks = f / 128;
         a.k_blocks = d / 64;
+        a.k_splits = 1;
+        a.out_split_stride = 0;
         a.b_rows_per_expert = 2 * f;
         a.out = h->H;
         a.out_ld = f;
@@ -295,22 +331,37 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             st = g.done(launch_tc_gemm(kGateUp, h->tm_xp, h->tm_wgu, a, grid, s), 1);
             if (st != COLIBRI_OK) return st;
         }
-        // down: N = d in blocks of 256, K = f
+        // down: N = d in blocks of 256, K = f.  Few pairs leave too few
+        // (m-tile, n-block) items to fill the GPU: split K into slices whose
+        // float32 partials the combine adds in slice order.
         a.n_blocks = d / 256;
         a.k_blocks = f / 64;
         a.b_rows_per_expert = d;
         a.out = h->Y;
         a.out_ld = d;
+        a.k_splits = 1;
+        if (npairs <= kSplitMaxPairs) {
+            const int64_t items = (int64_t)tiles_ub * a.n_blocks;
+            int ks = (int)std::min<int64_t>(kMaxKSplit, (2 * h->num_sms + items - 1) / items);
+            ks = std::max(1, std::min(ks, a.k_blocks));
+            const int per = (a.k_blocks + ks - 1) / ks;
+            a.k_splits = (a.k_blocks + per - 1) / per;  // every slice non-empty
+        }
+        a.out_split_stride = (size_t)npairs * d;
         {
-            const int grid = (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks, h->num_sms);
+            const int grid = (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks * a.k_splits,
+                                                    h->num_sms);
             Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
             st = g.done(launch_tc_gemm(kDown, h->tm_h, h->tm_wdT, a, grid, s), 1);
             if (st != COLIBRI_OK) return st;
         }
+        nsplit = a.k_splits;
+        split_stride = a.out_split_stride;
     }
     {
         Stage g(h, COLIBRI_STAGE_COMBINE, s);
-        st = g.done(launch_combine(h->dt, h->Y, h->topk_w, h->inv, T, k, d, resid, y, s), 1);
+        st = g.done(launch_combine(h->dt, h->Y, h->topk_w, h->inv, T, k, d, nsplit, split_stride,
+                                   resid, y, s), 1);
         if (st != COLIBRI_OK) return st;
     }
     h->last_T = T;
@@ -359,7 +410,10 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     h->esz = cfg->dtype == COLIBRI_DTYPE_BF16 ? 2 : 4;
     h->num_sms = prop.multiProcessorCount;
     h->e_pad = (cfg->n_experts + 15) / 16 * 16;
+    // Failure-detection tests: a shorter bound for the device-side waits, and
+    // a producer that never issues its copies (a flag that nothing sets).
     if (const char* e = std::getenv("COLIBRI_WAIT_LIMIT_NS")) h->wait_limit_ns = std::strtoull(e, nullptr, 10);
+    if (const char* e = std::getenv("COLIBRI_TEST_STALL_TMA")) h->stall_tma = std::atoi(e) != 0;
 
     const int E = cfg->n_experts, d = cfg->d_model, f = cfg->d_ff, k = cfg->top_k;
     AllocCounter ac;
@@ -432,7 +486,9 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
                  o_te = carve((size_t)h->max_tiles * 4), o_tr = carve((size_t)h->max_tiles * 4),
                  o_tinfo = carve((size_t)h->max_tiles * 4), o_nt = carve(4), o_st = carve(4),
                  o_xp = h->grouped_ok ? carve(P * d * h->esz) : 0, o_h = carve(P * f * h->esz),
-                 o_y = carve(P * d * 4), o_u = carve((size_t)M * d * h->esz),
+                 o_y = carve(std::max(P, (size_t)kMaxKSplit * std::min<size_t>(P, kSplitMaxPairs)) *
+                             d * 4),
+                 o_u = carve((size_t)M * d * h->esz),
                  o_xs = carve((size_t)M * d * h->esz), o_ys = carve((size_t)M * d * h->esz);
     h->ws_bytes = off;
     if ((st = from_cuda(ac.alloc(&h->ws, off))) != COLIBRI_OK) return fail(st);
@@ -460,7 +516,8 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
         bool ok = make_tmap_bf16(&h->tm_xp, h->xp, P, d, 128) &&
                   make_tmap_bf16(&h->tm_wgu, h->wgu, (uint64_t)E * 2 * f, d, 256) &&
                   make_tmap_bf16(&h->tm_h, h->H, P, f, 128) &&
-                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 256);
+                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 256) &&
+                  make_tmap_bf16(&h->tm_wr, h->wr, (uint64_t)h->e_pad, d, (uint32_t)h->e_pad);
         if (!ok) {
             if (cfg->executor == COLIBRI_EXEC_GROUPED) return fail(COLIBRI_ERR_CUDA);
             h->grouped_ok = false;

@@ -30,7 +30,8 @@ cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, con
 cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,
                           int npairs, void* xp, cudaStream_t s);
 cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const int32_t* inv,
-                           int T, int k, int d, const void* resid, void* y, cudaStream_t s);
+                           int T, int k, int d, int nsplit, size_t split_stride,
+                           const void* resid, void* y, cudaStream_t s);
 cudaError_t launch_rmsnorm(DType dt, const void* h, const void* gamma, int T, int d, float eps,
                            void* u, cudaStream_t s);
 cudaError_t launch_transpose_remap(int elem_bytes, const void* in, void* out, int batch, int R,

@@ -21,9 +21,12 @@ __global__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restri
 // Combine: y[t, c] = sum_j w[t, j] * Y[inv[t*k + j], c], j in order, float32;
 // with `resid`, y[t, c] = resid[t, c] + that sum (one rounding at the end).
 // zskr.cn section 3.3 stage 5 (aggregation weighted by the expert scores).
+// When the down projection was split over K, Y holds `nsplit` partial slices
+// `split_stride` floats apart; they are added first, in slice order.
 template <typename T>
 __global__ void combine_kernel(const float* __restrict__ Y, const float* __restrict__ topk_w,
-                               const int32_t* __restrict__ inv, int k, int d,
+                               const int32_t* __restrict__ inv, int k, int d, int nsplit,
+                               size_t split_stride,
                                const T* resid, T* y) {  // resid may alias y (in-place residual)
     const int t = blockIdx.y;
     const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
@@ -31,7 +34,15 @@ __global__ void combine_kernel(const float* __restrict__ Y, const float* __restr
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
         const float w = topk_w[(size_t)t * k + j];
-        const float4 v = *reinterpret_cast<const float4*>(Y + (size_t)inv[(size_t)t * k + j] * d + c);
+        const float* row = Y + (size_t)inv[(size_t)t * k + j] * d + c;
+        float4 v = *reinterpret_cast<const float4*>(row);
+        for (int sp = 1; sp < nsplit; ++sp) {
+            const float4 p = *reinterpret_cast<const float4*>(row + sp * split_stride);
+            v.x += p.x;
+            v.y += p.y;
+            v.z += p.z;
+            v.w += p.w;
+        }
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
@@ -114,15 +125,17 @@ cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, in
 }
 
 cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const int32_t* inv,
-                           int T, int k, int d, const void* resid, void* y, cudaStream_t s) {
+                           int T, int k, int d, int nsplit, size_t split_stride,
+                           const void* resid, void* y, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const dim3 block(128), grid((d / 4 + 127) / 128, T);
     if (dt == DType::BF16)
         combine_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
-            Y, topk_w, inv, k, d, (const __nv_bfloat16*)resid, (__nv_bfloat16*)y);
+            Y, topk_w, inv, k, d, nsplit, split_stride, (const __nv_bfloat16*)resid,
+            (__nv_bfloat16*)y);
     else
-        combine_kernel<float><<<grid, block, 0, s>>>(Y, topk_w, inv, k, d, (const float*)resid,
-                                                      (float*)y);
+        combine_kernel<float><<<grid, block, 0, s>>>(Y, topk_w, inv, k, d, nsplit, split_stride,
+                                                      (const float*)resid, (float*)y);
     return cudaGetLastError();
 }
 

@@ -8,8 +8,11 @@ Parity rules (all float tolerances are written here once):
 * counts and perm must equal the oracle's dispatch of the GPU's own topk_idx
   (an integer function: always exact), and the oracle's own dispatch when no
   token is a near-tie.
-* topk_w within GATE_ATOL of softmax over the oracle's float64 logits at the
-  GPU's selected experts.
+* topk_w within GATE_ATOL + 1/2 max_j tau[t, j] of the softmax over the
+  oracle's float64 logits at the GPU's selected experts.  tau is the logit
+  error radius of the near-tie rule (the accuracy the routing contract grants
+  float32 accumulation in any order); the softmax Jacobian bounds the induced
+  gate error: |dg_i| <= 2 g_i (1 - g_i) max_j |dl_j| <= max_j |dl_j| / 2.
 * y: max|y - y_ref| / max|y_ref| <= Y_RTOL[dtype], y_ref the oracle's
   sum_j g_j FFN_{e_j}(x) at the GPU's selected experts (identical to the plain
   oracle wherever routing agrees).
@@ -24,6 +27,7 @@ import oracle
 import synth
 
 GATE_ATOL = 1e-6
+NEAR_TIE_REL = 2.0 ** -20   # oracle.near_tie_tokens' default radius
 Y_RTOL = {"fp32": 1e-4, "bf16": 2e-2}
 
 
@@ -94,8 +98,11 @@ def check_routing(case: Case, x64, r, allow_near_ties: bool = True):
     assert bad.size == 0, f"topk_idx differs on {bad.size} non-near-tie tokens, e.g. t={bad[:5]}"
     # gates against the float64 softmax at the GPU's experts
     g_ref = oracle.softmax_selected(l, gidx)
-    gerr = np.abs(r["topk_w"] - g_ref).max()
-    assert gerr <= GATE_ATOL, f"gate error {gerr}"
+    tau = NEAR_TIE_REL * (np.abs(x64) @ np.abs(case.wr64))
+    tau_sel = np.take_along_axis(tau, gidx.astype(np.int64), axis=1).max(axis=1, keepdims=True)
+    gerr = np.abs(r["topk_w"] - g_ref)
+    bad = gerr > GATE_ATOL + 0.5 * tau_sel
+    assert not bad.any(), f"gate error {gerr.max():.3e} (bound {GATE_ATOL} + tau/2)"
     # dispatch: exact function of the GPU's own topk_idx
     counts, offsets, perm, inv = oracle.dispatch(gidx, E)
     assert np.array_equal(r["counts"], counts), "counts differ"

@@ -1,0 +1,81 @@
+"""Failure detection on the GPU without faulting it.
+
+* An allocation failure injected on the host (COLIBRI_FAIL_ALLOC_AT=n fails
+  init's n-th device allocation) must return COLIBRI_ERR_OOM, leave no handle
+  and free everything init had allocated.
+* The grouped GEMM's mbarrier waits are bounded.  A handle built with
+  COLIBRI_TEST_STALL_TMA=1 has a TMA producer that never issues its copies (a
+  flag that nothing sets), and COLIBRI_WAIT_LIMIT_NS=20000000 bounds every
+  wait at 20 ms: the MMA warp's first wait on a full stage runs out, the kernel
+  records a timeout in the handle's status word, every role stops, tensor
+  memory is freed and the kernel returns.  colibri_check must report
+  COLIBRI_ERR_TIMEOUT, and the context must stay usable: a normal handle used
+  before and after computes the same result.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = synth.LayerShape("failure_probe", 512, 1024, 8, 2, "bf16")
+
+
+def _weights(dev):
+    wr = synth.router_weight(SHAPE, 3, 0, dev)
+    wg, wu, wd = synth.expert_weights(SHAPE, 3, 0, dev)
+    return wr, wg, wu, wd
+
+
+def test_injected_allocation_failure_rolls_back(lib, monkeypatch):
+    sef = lib
+    dev = torch.device("cuda", 0)
+    ws = _weights(dev)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    # weights on the device: four device allocations (router, gate/up, down, workspace)
+    for n in range(1, 5):
+        monkeypatch.setenv("COLIBRI_FAIL_ALLOC_AT", str(n))
+        with pytest.raises(sef.ColibriError) as ei:
+            sef.MoELayer(*ws, SHAPE.top_k, max_tokens=256)
+        assert ei.value.status == sef.ERR_OOM
+    monkeypatch.delenv("COLIBRI_FAIL_ALLOC_AT")
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert abs(free1 - free0) < 64 << 20, "failed inits leaked device memory"
+    layer = sef.MoELayer(*ws, SHAPE.top_k, max_tokens=256)
+    layer.close()
+
+
+def test_bounded_wait_times_out_and_context_survives(lib, monkeypatch):
+    sef = lib
+    dev = torch.device("cuda", 0)
+    ws = _weights(dev)
+    x = synth.tokens(SHAPE, 256, 3, 0, dev)
+
+    ref_layer = sef.MoELayer(*ws, SHAPE.top_k, max_tokens=256, executor="grouped")
+    y_ref = ref_layer.forward(x)
+    assert ref_layer.check() == sef.OK
+
+    monkeypatch.setenv("COLIBRI_WAIT_LIMIT_NS", "20000000")
+    monkeypatch.setenv("COLIBRI_TEST_STALL_TMA", "1")
+    short = sef.MoELayer(*ws, SHAPE.top_k, max_tokens=256, executor="grouped")
+    monkeypatch.delenv("COLIBRI_WAIT_LIMIT_NS")
+    monkeypatch.delenv("COLIBRI_TEST_STALL_TMA")
+    short.forward(x)
+    assert short.check() == sef.ERR_TIMEOUT
+    # the status word is cleared by the check
+    assert short.check() == sef.OK
+    short.close()
+
+    # the context is intact: the default-bound handle still gives its result
+    y2 = ref_layer.forward(x)
+    assert ref_layer.check() == sef.OK
+    assert torch.equal(y_ref, y2)
+    ref_layer.close()

@@ -44,6 +44,7 @@ def test_stack_teacher_forced_layers(stack):
     shape = synth.MIXTRAL
     weights = {l: _layer_weights64(l) for l in CHECK_LAYERS}
     g64 = np.ones(shape.d_model)
+    compared = 0
     for B in synth.STACK_BATCHES:
         h = synth.tokens(shape, B, seed=7, device="cuda")           # bf16 N(0,1) hidden state
         for l, layer in enumerate(layers):
@@ -67,4 +68,7 @@ def test_stack_teacher_forced_layers(stack):
                     # the MoE increment itself, against the oracle's y
                     dy = np.abs((got - h64) - ref["y"]).max() / np.abs(ref["y"]).max()
                     assert dy <= 5e-2, f"B={B} layer {l}: increment error {dy:.3e}"
+                    compared += 1
         assert torch.isfinite(h.float()).all()
+    # near-ties can skip a layer's output check, but not most of them
+    assert compared >= len(synth.STACK_BATCHES) * len(CHECK_LAYERS) - 1
