@@ -38,6 +38,16 @@ sys.path.insert(0, ROOT)
 
 STAGES = ["router", "dispatch", "gather", "expert_up", "expert_down", "combine", "rmsnorm"]
 
+# name -> (synth shape name, default tokens, label, decode-size sweep)
+WORKLOADS = {
+    "mixtral": ("MIXTRAL", 4096, "Mixtral-8x7B-shaped MoE layer", (1, 16, 128, 512)),
+    "qwen2_moe": ("QWEN2", 8192, "Qwen2-MoE-shaped MoE layer (Zipf(1.1) router offset)", (1, 64, 2048)),
+    "deepseek_moe": ("DEEPSEEK", 16384, "DeepSeek-MoE-16B-shaped MoE layer", ()),
+    "deepseek_moe_masked": ("DEEPSEEK_MASKED", 16384,
+                            "DeepSeek-MoE-16B-shaped MoE layer, experts e%4==3 masked", ()),
+    "stack": ("MIXTRAL", 64, "32-layer Mixtral-shaped decode stack (RMSNorm, MoE, residual)", ()),
+}
+
 
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -45,7 +55,10 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--tokens", type=int, default=4096)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral",
+                    help="layer workload (default: the Mixtral-shaped layer the metric is quoted on)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="tokens per step (default per workload; batch per step for the stack)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true", help="skip the decode-size sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -270,7 +283,9 @@ def run_ours(args):
     world, rank, local = dist_setup(args)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    shape, T = synth.MIXTRAL, args.tokens
+    shape_name, T_default, label, sweep_T = WORKLOADS[args.workload]
+    shape = getattr(synth, shape_name)
+    T = args.tokens or T_default
     pk = peaks()
     props = torch.cuda.get_device_properties(dev)
     uid = str(getattr(props, "uuid", "") or "")
@@ -282,7 +297,9 @@ def run_ours(args):
     wr = synth.router_weight(shape, seed, 0, dev)
     wg, wu, wd = synth.expert_weights(shape, seed, 0, dev)
     max_t = max(T, 128)
-    layer = sef.MoELayer(wr, wg, wu, wd, shape.top_k, max_tokens=max_t)
+    layer = sef.MoELayer(wr, wg, wu, wd, shape.top_k, router_bias=synth.router_offset(shape),
+                         max_tokens=max_t)
+    weight_gb = (wg.numel() + wu.numel() + wd.numel()) * wg.element_size() / 1e9
     del wg, wu, wd
     torch.cuda.empty_cache()
     x = synth.tokens(shape, T, seed, 0, dev)
@@ -312,7 +329,7 @@ def run_ours(args):
     kname = {("expert_up", True): "grouped_gemm_tc<kGateUp>", ("expert_down", True): "grouped_gemm_tc<kDown>",
              ("expert_up", False): "ffn_up_stream", ("expert_down", False): "ffn_down_stream"}.get(
         (dom, grouped), dom)
-    workload = f"mixtral_T{T}"
+    workload = f"{args.workload}_T{T}"
     if grouped and dom in ("expert_up", "expert_down"):
         fl = alg["up_flops"] if dom == "expert_up" else alg["down_flops"]
         achieved = fl / per_launch_s / 1e12
@@ -353,7 +370,7 @@ def run_ours(args):
     # decode-size sweep (context; the headline is the T above)
     sweep = {}
     if not args.no_sweep:
-        for Ts, ex in ((1, "auto"), (1, "stream"), (16, "auto"), (128, "auto"), (512, "auto")):
+        for Ts, ex in [(t, "auto") for t in sweep_T if t <= max_t]:
             layer.set_executor(ex)
             xs = synth.tokens(shape, Ts, seed, 0, dev)
             ys = torch.empty_like(xs)
@@ -383,10 +400,10 @@ def run_ours(args):
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"Mixtral-8x7B-shaped MoE layer, T={T} tokens",
+        "config": {"workload": f"{label}, T={T} tokens",
                    "d_model": shape.d_model, "d_ff": shape.d_ff, "n_experts": shape.n_experts,
                    "top_k": shape.top_k, "tokens_per_gpu": T, "parallelism": f"token-parallel x{world}",
-                   "l2": "inputs larger than L2 (2.8 GB of expert weights per step)"},
+                   "l2": f"inputs larger than L2 ({weight_gb:.2f} GB of expert weights per step)"},
         "roofline": roof,
         "layer_roofline": whole,
         "stages_us_per_step": {k: round(v["ms_total"] * 1e3 / args.steps, 1) for k, v in stages.items()},
@@ -403,6 +420,96 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_stack(args):
+    """One step = 32 Mixtral-shaped layers, each RMSNorm -> MoE -> residual,
+    over a batch of B single-token sequences; weight-streaming bound."""
+    import ctypes
+
+    import torch
+
+    import sparse_expert_ffn_gb300 as sef
+    import synth
+
+    world, rank, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape, B = synth.MIXTRAL, args.tokens or 64
+    pk = peaks()
+    seed = rank_seed(args.seed, rank)
+    layers = []
+    for l in range(synth.STACK_LAYERS):
+        wr = synth.router_weight(shape, seed, l, dev)
+        wg, wu, wd = synth.expert_weights(shape, seed, l, dev)
+        layers.append(sef.MoELayer(wr, wg, wu, wd, shape.top_k, max_tokens=max(B, 1)))
+        del wr, wg, wu, wd
+    torch.cuda.empty_cache()
+    gamma = torch.ones(shape.d_model, dtype=torch.bfloat16, device=dev)
+    h0 = synth.tokens(shape, B, seed, 0, dev)
+    h = h0.clone()
+    lib = sef.library()
+
+    def step():
+        for layer in layers:
+            layer.rmsnorm_moe_residual(h, gamma, synth.STACK_EPS)
+
+    for _ in range(args.warmup):
+        h.copy_(h0)
+        step()
+    torch.cuda.synchronize()
+    for layer in layers:
+        lib.colibri_profile_enable(layer.handle, 1)
+    n0 = sum(l.launch_count for l in layers)
+    stream = torch.cuda.current_stream()
+    barrier(world)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b), world)
+    launches = sum(l.launch_count for l in layers) - n0
+    stages = {}
+    active = 0
+    for layer in layers:
+        tot = (ctypes.c_double * 7)()
+        cnt = (ctypes.c_uint64 * 7)()
+        lib.colibri_profile_read(layer.handle, tot, cnt)
+        for i in range(7):
+            if cnt[i]:
+                st = stages.setdefault(STAGES[i], {"ms_total": 0.0, "launches": 0})
+                st["ms_total"] += tot[i]
+                st["launches"] += int(cnt[i])
+        active += int((layer.routing()["counts"] > 0).sum().item())
+        assert layer.check() == 0
+    step_s = ms / args.steps / 1e3
+    d, f, E = shape.d_model, shape.d_ff, shape.n_experts
+    step_bytes = active * 3 * d * f * 2 + synth.STACK_LAYERS * (d * E * 2 + 4 * B * d * 2 + d * 2)
+    out = {
+        "metric": "MoE-layer tokens/s at 1 GB300; % of HBM (decode) / bf16 TC (prefill) roofline",
+        "value": round(job_throughput(world, B, args.steps, ms), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOADS['stack'][2]}, batch {B}", "layers": synth.STACK_LAYERS,
+                   "batch": B, "parallelism": f"token-parallel x{world}",
+                   "l2": "inputs larger than L2 (90 GB of weights)"},
+        "stack_roofline": {"bound": "hbm", "bytes_per_step": step_bytes,
+                           "achieved_gbs": round(step_bytes / step_s / 1e9, 1),
+                           "peak": pk["hbm_gbs"],
+                           "frac": round(step_bytes / step_s / 1e9 / pk["hbm_gbs"], 4),
+                           "active_experts_per_step": active},
+        "stages_us_per_step": {k: round(v["ms_total"] * 1e3 / args.steps, 1) for k, v in stages.items()},
+        "gpu_launches": int(launches),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    for layer in layers:
+        layer.close()
 
 
 # ----------------------------------------------------------------------------- oracle (CPU)
@@ -432,17 +539,20 @@ def cpu_baseline(shape, x, seed=0, target_s=15.0):
     import numpy as np
 
     import oracle
+    import synth
     xh, wr, wg, wu, wd = _host_inputs(shape, x.shape[0], seed)
     W = _oracle_weights(wr, wg, wu, wd)
     del wg, wu, wd
     x64 = oracle.to_f64(xh)
     # calibrate on 16 tokens, then size the sample to ~target_s seconds
+    off = synth.router_offset(shape)
+    off = None if off is None else off.double().numpy()
     t0 = time.perf_counter()
-    oracle.moe_layer(x64[:16], *W, shape.top_k)
-    per_tok = (time.perf_counter() - t0) / 16
+    oracle.moe_layer(x64[:64], *W, shape.top_k, off)
+    per_tok = (time.perf_counter() - t0) / 64
     n = int(min(x64.shape[0], max(16, target_s / max(per_tok, 1e-9))))
     t0 = time.perf_counter()
-    oracle.moe_layer(x64[:n], *W, shape.top_k)
+    oracle.moe_layer(x64[:n], *W, shape.top_k, off)
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -459,22 +569,27 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    shape, T = synth.MIXTRAL, args.tokens
+    wl = "mixtral" if args.workload == "stack" else args.workload
+    shape_name, T_default, label, _ = WORKLOADS[wl]
+    shape = getattr(synth, shape_name)
+    T = args.tokens or T_default
     xh, wr, wg, wu, wd = _host_inputs(shape, T, args.seed)
+    off = synth.router_offset(shape)
+    off = None if off is None else off.double().numpy()
     W = _oracle_weights(wr, wg, wu, wd)
     del wg, wu, wd
     x64 = oracle.to_f64(xh)
     t0 = time.perf_counter()
-    oracle.moe_layer(x64[:8], *W, shape.top_k)
+    oracle.moe_layer(x64[:8], *W, shape.top_k, off)
     per_tok = (time.perf_counter() - t0) / 8
     # each step: a bounded sample sized so that W + K steps take ~2 minutes
     n = int(max(4, min(T, 120.0 / max(per_tok, 1e-9) / max(1, args.steps + args.warmup))))
     for i in range(args.warmup):
-        oracle.moe_layer(x64[:n], *W, shape.top_k)
+        oracle.moe_layer(x64[:n], *W, shape.top_k, off)
     t0 = time.perf_counter()
     for i in range(args.steps):
         lo = (i * n) % max(1, T - n)
-        oracle.moe_layer(x64[lo:lo + n], *W, shape.top_k)
+        oracle.moe_layer(x64[lo:lo + n], *W, shape.top_k, off)
     dt = time.perf_counter() - t0
     value = n * args.steps / dt
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
@@ -485,7 +600,7 @@ def run_reference(args):
            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
-           "config": {"workload": f"Mixtral-8x7B-shaped MoE layer, T={T} tokens",
+           "config": {"workload": f"{label}, T={T} tokens",
                       "d_model": shape.d_model, "d_ff": shape.d_ff, "n_experts": shape.n_experts,
                       "top_k": shape.top_k, "tokens_per_gpu": T, "parallelism": "none (host CPU)"},
            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
@@ -499,6 +614,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "stack":
+        run_stack(args)
     else:
         run_ours(args)
 

@@ -19,8 +19,8 @@
 // raster bands that never cross an expert boundary (at most kMaxBand tiles of
 // one expert per band), so that the GEMM walks all of a band's m-tiles against
 // one weight block at a time and every weight block is streamed from HBM once.
-// tile_info[t] packs: bits 0-7 valid rows (1..bm), bits 8-15 the tile's
-// position inside its band, bits 16-23 the band's length in tiles.
+// tile_info[t] packs: bits 0-9 valid rows (1..bm, bm <= 512), bits 10-17 the
+// tile's position inside its band, bits 18-25 the band's length in tiles.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -29,7 +29,7 @@ namespace colibri {
 namespace {
 
 constexpr int kDispatchWarps = 32;
-constexpr int kMaxBand = 32;
+constexpr int kMaxBand = 16;   // tiles of up to 256 rows
 
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_kernel(const int32_t* __restrict__ topk_idx, int n, int E, int32_t* __restrict__ counts,
@@ -102,7 +102,7 @@ dispatch_kernel(const int32_t* __restrict__ topk_idx, int n, int E, int32_t* __r
             const int band_len = min(kMaxBand, nt - (i / kMaxBand) * kMaxBand);
             tile_expert[tb] = e;
             tile_row[tb] = eoff[e] + i * bm;
-            tile_info[tb] = min(bm, c - i * bm) | ((i % kMaxBand) << 8) | (band_len << 16);
+            tile_info[tb] = min(bm, c - i * bm) | ((i % kMaxBand) << 10) | (band_len << 18);
         }
     }
     if (threadIdx.x == 0) offsets[E] = eoff[E];

@@ -25,8 +25,9 @@
 // rows stay resident in L2 across the n-blocks.
 //
 // Roles (192 threads):
-//   warp 0      TMA producer: A and B tiles of 64 K-columns into a
-//               kStages-deep ring of 128B-swizzled shared-memory stages.
+//   warp 0      TMA producer: A and B tiles of 64 K-columns into a ring of
+//               128B-swizzled shared-memory stages (4 deep for a single CTA,
+//               6 deep for a CTA of a pair).
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma (M=128, N=256, K=16)
 //               into one of two 256-column accumulators, commits each stage
 //               back to the producer and each finished tile to the epilogue.
@@ -48,13 +49,18 @@ namespace {
 constexpr int kBM = 128;          // tile rows (pairs)
 constexpr int kBN = 256;          // tile columns of B rows per MMA
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle atom of bf16
-constexpr int kStages = 4;
+// Shared-memory ring: a single CTA holds 4 stages of A (16 KB) + B (up to
+// 256 rows, 32 KB); a CTA of a pair loads only half of B (16 KB), so it
+// holds 6 stages.  Both keep ~192 KB of copies in flight per SM.
+template <bool kPair> struct Ring {
+    static constexpr int kStages = kPair ? 6 : 4;
+    static constexpr uint32_t kStageB = (kPair ? 128 : 256) * 64 * 2;
+};
 constexpr int kThreads = 192;
 constexpr int kAccCols = 256;     // TMEM columns per accumulator
 constexpr int kTmemCols = 512;    // two accumulators
 constexpr uint32_t kStageA = kBM * kBK * 2;   // 16 KB
-constexpr uint32_t kStageB = kBN * kBK * 2;   // 32 KB
-constexpr uint32_t kStageBytes = kStageA + kStageB;
+
 // Teardown waits (copies and MMAs already issued) use their own bound,
 // independent of the configurable wait limit, so that a CTA never exits with
 // a TMA copy or an MMA of its own still in flight.
@@ -132,16 +138,67 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+// The same copy for a CTA pair: the mbarrier may be the peer CTA's (a
+// shared::cluster address), so both halves of a pair's stage complete on the
+// leader's barrier.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0,
+                                                 int c1, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
 }
 
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                  : "memory");
+}
+
+// Tensor-memory allocation: for a CTA pair one warp of each CTA allocates
+// the same columns collectively (cta_group::2).
+template <bool kPair>
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    if constexpr (kPair) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+}
+
+template <bool kPair>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    if constexpr (kPair)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -152,21 +209,57 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, f32 accumulate).
+// For a CTA pair (cta_group::2, issued by the leader) A is the 2 x 128 rows
+// held by the two CTAs, B the 2 x N/2 rows, and each CTA's TMEM receives its
+// own 128 rows of D over all N columns.
+template <bool kPair>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (kPair)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
-// Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has
+// completed; for a pair, on the barrier at that offset in both CTAs.
+template <bool kPair>
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
+    if constexpr (kPair) {
+        const uint16_t both = 0x3;
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;" ::"r"(bar),
+            "h"(both)
+            : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    }
+}
+
+// Commit onto the issuing CTA's own barrier only.
+template <bool kPair>
+__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+    if constexpr (kPair)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
 }
 
 // 32 consecutive 32-bit TMEM columns of this thread's lane.
@@ -227,15 +320,15 @@ __device__ __forceinline__ Work decode_work(int w, int n_blocks, int k_splits,
     n_blocks *= k_splits;
     const int t = w / n_blocks;
     const int info = tile_info[t];
-    const int first = t - ((info >> 8) & 0xFF);
-    const int len = (info >> 16) & 0xFF;
+    const int first = t - ((info >> 10) & 0xFF);
+    const int len = (info >> 18) & 0xFF;
     const int rem = w - first * n_blocks;
     const int nblk = rem / len;
     const int m = first + (rem - nblk * len);
     Work r;
     r.expert = tile_expert[m];
     r.row0 = tile_row[m];
-    r.rows = tile_info[m] & 0xFF;
+    r.rows = tile_info[m] & 0x3FF;
     r.nblk = nblk / k_splits;
     r.split = nblk - r.nblk * k_splits;
     return r;
@@ -269,7 +362,7 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 
 // ---------------------------------------------------------------- the kernel
 
-template <int kMode>
+template <int kMode, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 TcGemmArgs args) {
@@ -277,9 +370,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // 1024-byte alignment for the 128-byte swizzle atoms.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    constexpr int kStages = Ring<kPair>::kStages;
+    constexpr uint32_t kStageB = Ring<kPair>::kStageB;
     uint8_t* stage_a = smem;
     uint8_t* stage_b = smem + kStages * kStageA;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * (kStageA + kStageB));
     uint64_t* full = bars;                 // [kStages]
     uint64_t* empty = bars + kStages;      // [kStages]
     uint64_t* acc_full = bars + 2 * kStages;     // [2]
@@ -289,12 +384,22 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // CTA pair: rank 0 (leader) owns the full / acc_empty barriers and issues
+    // the MMAs; both CTAs load their halves of A and B and run an epilogue on
+    // their own 128 rows of the 256-row tile.
+    const uint32_t rank = kPair ? cluster_rank() : 0;
+    const bool leader = rank == 0;
+    const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int n_units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+
     const int num_tiles =
         kMode == kRouter ? (args.dense_rows + kBM - 1) / kBM : *args.num_tiles;
     const int total = num_tiles * args.n_blocks * args.k_splits;
-    // B tile rows = MMA N: 256, or the padded expert count for the router
+    // Rows of B this CTA loads per stage (= MMA N, or half of it for a pair).
     const int bn = kMode == kRouter ? args.bn_rows : kBN;
-    const uint32_t stage_tx = kStageA + (uint32_t)bn * kBK * 2;
+    const int b_rows_cta = kPair ? bn / 2 : bn;
+    const uint32_t cta_tx = kStageA + (uint32_t)b_rows_cta * kBK * 2;
+    const uint32_t stage_tx = kPair ? 2 * cta_tx : cta_tx;   // bytes landing on `full`
     const int kb_per_split = (args.k_blocks + args.k_splits - 1) / args.k_splits;
     const uint64_t limit = args.wait_limit_ns;
 
@@ -305,15 +410,17 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&acc_full[a]), 1);
-            mbar_init(smem_u32(&acc_empty[a]), 4 * 32);
+            // one elected lane per epilogue warp, in each CTA of the pair
+            mbar_init(smem_u32(&acc_empty[a]), kPair ? 8 : 4);
         }
         mbar_init(smem_u32(&mma_done[0]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    if (warp == 1) tmem_alloc<kPair>(smem_u32(tmem_slot), kTmemCols);
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync();   // the peer's barriers exist before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -325,10 +432,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             bool issued[kStages];
             uint32_t issued_phase[kStages];
             for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
-            for (int w = blockIdx.x; w < total && !*abort_flag && !args.stall_producer;
-                 w += gridDim.x) {
+            for (int w = unit; w < total && !*abort_flag && !args.stall_producer; w += n_units) {
                 const Work wk = get_work<kMode>(w, args);
-                const int b_row = wk.expert * args.b_rows_per_expert + wk.nblk * kBN;
+                const int a_row = wk.row0 + (int)rank * kBM;
+                const int b_row = wk.expert * args.b_rows_per_expert + wk.nblk * kBN +
+                                  (int)rank * b_rows_cta;
                 const int kb0 = wk.split * kb_per_split;
                 const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
                 bool ok = true;
@@ -338,30 +446,41 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&full[stage]);
-                    mbar_expect_tx(fb, stage_tx);
-                    tma_load_2d(smem_u32(stage_a + stage * kStageA), &tmA, kb * kBK, wk.row0, fb);
-                    tma_load_2d(smem_u32(stage_b + stage * kStageB), &tmB, kb * kBK, b_row, fb);
+                    const uint32_t fb_local = smem_u32(&full[stage]);
+                    if (leader) mbar_expect_tx(fb_local, stage_tx);
+                    const uint32_t sa = smem_u32(stage_a + stage * kStageA);
+                    const uint32_t sb = smem_u32(stage_b + stage * kStageB);
+                    if constexpr (kPair) {
+                        // both halves complete on the leader's barrier
+                        const uint32_t fb = map_to_rank(fb_local, 0);
+                        tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
+                        tma_load_2d_pair(sb, &tmB, kb * kBK, b_row, fb);
+                    } else {
+                        tma_load_2d(sa, &tmA, kb * kBK, a_row, fb_local);
+                        tma_load_2d(sb, &tmB, kb * kBK, b_row, fb_local);
+                    }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
                     if (++stage == kStages) stage = 0, phase ^= 1;
                 }
                 if (!ok) break;
             }
-            // Teardown: every copy this thread issued must have landed.
-            for (int s = 0; s < kStages; ++s)
-                if (issued[s]) mbar_wait_drain(smem_u32(&full[s]), issued_phase[s], kDrainLimitNs);
+            // Teardown: every copy issued must have landed.  The leader's
+            // `full` barriers count the copies of both CTAs of a pair.
+            if (leader)
+                for (int s = 0; s < kStages; ++s)
+                    if (issued[s]) mbar_wait_drain(smem_u32(&full[s]), issued_phase[s], kDrainLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(kBM, bn);
+        // ------------------------------------------------ MMA issuer (leader)
+        if (lane == 0 && leader) {
+            const uint32_t idesc = idesc_bf16(kPair ? 2 * kBM : kBM, bn);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int w = blockIdx.x; w < total && !*abort_flag; w += gridDim.x) {
+            for (int w = unit; w < total && !*abort_flag; w += n_units) {
                 const Work wk = get_work<kMode>(w, args);
                 const int kb0 = wk.split * kb_per_split;
                 const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
@@ -383,26 +502,29 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                     for (int ks = 0; ks < kBK / 16; ++ks)
                         // +32 bytes of K per step inside the swizzle atom (encoded >> 4)
-                        mma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, idesc, (kb > kb0) || ks != 0);
-                    mma_commit(smem_u32(&empty[stage]));
+                        mma_bf16<kPair>(d_tmem, da + 2 * ks, db + 2 * ks, idesc,
+                                        (kb > kb0) || ks != 0);
+                    mma_commit<kPair>(smem_u32(&empty[stage]));
                     if (++stage == kStages) stage = 0, phase ^= 1;
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&acc_full[acc]));
+                mma_commit<kPair>(smem_u32(&acc_full[acc]));
                 if (++acc == 2) acc = 0, acc_phase ^= 1;
             }
             // Teardown: all MMAs issued by this thread complete before TMEM is freed.
-            mma_commit(smem_u32(&mma_done[0]));
+            mma_commit_local<kPair>(smem_u32(&mma_done[0]));
             mbar_wait_drain(smem_u32(&mma_done[0]), 0, kDrainLimitNs);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;              // TMEM lane quarter this warp may access
-        const int row = q * 32 + lane;       // tile row of this thread
+        const int row = q * 32 + lane;       // row of this CTA's 128-row half
+        const uint32_t acc_empty_leader0 =
+            kPair ? map_to_rank(smem_u32(&acc_empty[0]), 0) : smem_u32(&acc_empty[0]);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+        for (int w = unit; w < total; w += n_units) {
             const Work wk = get_work<kMode>(w, args);
             const bool got =
                 mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, args.status, limit);
@@ -410,8 +532,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-            const bool live = row < wk.rows;
-            const size_t orow = (size_t)(wk.row0 + row);
+            const int my_row = (int)rank * kBM + row;          // row inside the tile
+            const bool live = my_row < wk.rows;
+            const size_t orow = (size_t)(wk.row0 + my_row);
             if constexpr (kMode == kRouter) {
                 // Logits of this thread's token: the E accumulator columns
                 // (+ offset).  Top-k by insertion over a key that puts the
@@ -450,7 +573,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
                 if (live) {
                     const int k = args.top_k;
-                    const size_t t = (size_t)(wk.row0 + row);
+                    const size_t t = orow;
                     float sum = 0.f;
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
@@ -507,15 +630,23 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(&acc_empty[acc]));
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t ae = acc_empty_leader0 + acc * 8;   // &acc_empty[acc] in the leader
+                if constexpr (kPair) mbar_arrive_cluster(ae);
+                else mbar_arrive(ae);
+            }
             if (++acc == 2) acc = 0, acc_phase ^= 1;
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    // A pair ends together: the leader's MMAs read the peer's shared memory
+    // and the peer's copies complete on the leader's barriers.
+    if constexpr (kPair) cluster_sync();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+    if (warp == 1) tmem_dealloc<kPair>(tmem_base, kTmemCols);
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -538,9 +669,13 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-size_t tc_gemm_smem_bytes() { return (size_t)kStages * kStageBytes + 1024 + 256; }
+size_t tc_gemm_smem_bytes() {
+    const size_t single = (size_t)Ring<false>::kStages * (kStageA + Ring<false>::kStageB);
+    const size_t pair = (size_t)Ring<true>::kStages * (kStageA + Ring<true>::kStageB);
+    return (single > pair ? single : pair) + 1024 + 256;
+}
 int tc_gemm_block_m() { return kBM; }
-int tc_gemm_block_n(int mode) { return mode == kGateUp ? 128 : kBN; }
+int tc_gemm_pair_rows() { return 2 * kBM; }
 
 // Tensor map of a row-major bf16 matrix [rows, cols] with a box of
 // 64 columns x box_rows rows, 128-byte swizzle, zero fill out of bounds.
@@ -558,24 +693,64 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int kMode, bool kPair>
+cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcGemmArgs& args,
+                       int grid, cudaStream_t s) {
+    const size_t smem = tc_gemm_smem_bytes();
+    auto k = grouped_gemm_tc<kMode, kPair>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPair ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, tmA, tmB, args);
+}
+
 cudaError_t launch_tc_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s) {
-    const size_t smem = tc_gemm_smem_bytes();
     if (grid <= 0) return cudaSuccess;
-    if (mode == kGateUp) {
-        auto k = grouped_gemm_tc<kGateUp>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, kThreads, smem, s>>>(tmA, tmB, args);
-    } else if (mode == kRouter) {
-        auto k = grouped_gemm_tc<kRouter>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, kThreads, smem, s>>>(tmA, tmB, args);
-    } else {
-        auto k = grouped_gemm_tc<kDown>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, kThreads, smem, s>>>(tmA, tmB, args);
-    }
+    cudaError_t e;
+    if (mode == kGateUp)
+        e = launch_one<kGateUp, true>(tmA, tmB, args, grid & ~1, s);
+    else if (mode == kDown)
+        e = launch_one<kDown, true>(tmA, tmB, args, grid & ~1, s);
+    else
+        e = launch_one<kRouter, false>(tmA, tmB, args, grid, s);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+int tc_gemm_max_pairs() {
+    // CTA pairs of the expert GEMMs that can be resident at once.
+    static int pairs = -1;
+    if (pairs < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = tc_gemm_smem_bytes();
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        auto k = grouped_gemm_tc<kGateUp, true>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc_gemm_smem_bytes());
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) n = 0;
+        pairs = n;
+    }
+    return pairs;
 }
 
 }  // namespace colibri

@@ -12,7 +12,7 @@ enum : int { kGateUp = 0, kDown = 1, kRouter = 2 };
 struct TcGemmArgs {
     const int32_t* tile_expert;  // [max_tiles] expert of each m-tile
     const int32_t* tile_row;     // [max_tiles] first pair row of each m-tile
-    const int32_t* tile_info;    // [max_tiles] rows | band position << 8 | band length << 16
+    const int32_t* tile_info;    // [max_tiles] rows | band position << 10 | band length << 18
     const int32_t* num_tiles;    // device scalar: number of m-tiles
     int n_blocks;                // n-blocks per expert
     int k_blocks;                // K / 64
@@ -37,7 +37,8 @@ struct TcGemmArgs {
 
 size_t tc_gemm_smem_bytes();
 int tc_gemm_block_m();
-int tc_gemm_block_n(int mode);
+int tc_gemm_pair_rows();     // rows of one expert tile of a CTA pair (256)
+int tc_gemm_max_pairs();     // CTA pairs resident at once (0 if unknown)
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
 cudaError_t launch_tc_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB,

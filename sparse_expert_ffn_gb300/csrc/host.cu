@@ -64,6 +64,7 @@ struct colibri_moe {
     void* y_stage = nullptr;
     int max_pairs = 0;
     int max_tiles = 0;
+    int max_resident_pairs = 0;  // CTA pairs of the expert GEMMs resident at once
     bool grouped_ok = false;
     CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT, tm_wr;
     uint64_t wait_limit_ns = 2000000000ull;
@@ -281,7 +282,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     {
         Stage g(h, COLIBRI_STAGE_DISPATCH, s);
         st = g.done(launch_dispatch(h->topk_idx, npairs, E, h->counts, h->offsets, h->perm,
-                                    h->inv, tc_gemm_block_m(), h->tile_expert, h->tile_row,
+                                    h->inv, tc_gemm_pair_rows(), h->tile_expert, h->tile_row,
                                     h->tile_info, h->num_tiles, h->status, s), 1);
         if (st != COLIBRI_OK) return st;
     }
@@ -307,8 +308,10 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             st = g.done(launch_gather(h->esz, x, h->perm, k, d, npairs, h->xp, s), 1);
             if (st != COLIBRI_OK) return st;
         }
+        // Expert tiles of 256 rows, one per CTA pair (each CTA 128 rows).
         const int tiles_ub =
-            (npairs + tc_gemm_block_m() - 1) / tc_gemm_block_m() + std::min(E, npairs);
+            (npairs + tc_gemm_pair_rows() - 1) / tc_gemm_pair_rows() + std::min(E, npairs);
+        const int max_pairs = h->max_resident_pairs > 0 ? h->max_resident_pairs : h->num_sms / 2;
         TcGemmArgs a{};
         a.tile_expert = h->tile_expert;
         a.tile_row = h->tile_row;
@@ -326,7 +329,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.out = h->H;
         a.out_ld = f;
         {
-            const int grid = (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks, h->num_sms);
+            const int grid = 2 * (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks, max_pairs);
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
             st = g.done(launch_tc_gemm(kGateUp, h->tm_xp, h->tm_wgu, a, grid, s), 1);
             if (st != COLIBRI_OK) return st;
@@ -342,15 +345,15 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.k_splits = 1;
         if (npairs <= kSplitMaxPairs) {
             const int64_t items = (int64_t)tiles_ub * a.n_blocks;
-            int ks = (int)std::min<int64_t>(kMaxKSplit, (2 * h->num_sms + items - 1) / items);
+            int ks = (int)std::min<int64_t>(kMaxKSplit, (2 * max_pairs + items - 1) / items);
             ks = std::max(1, std::min(ks, a.k_blocks));
             const int per = (a.k_blocks + ks - 1) / ks;
             a.k_splits = (a.k_blocks + per - 1) / per;  // every slice non-empty
         }
         a.out_split_stride = (size_t)npairs * d;
         {
-            const int grid = (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks * a.k_splits,
-                                                    h->num_sms);
+            const int grid =
+                2 * (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks * a.k_splits, max_pairs);
             Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
             st = g.done(launch_tc_gemm(kDown, h->tm_h, h->tm_wdT, a, grid, s), 1);
             if (st != COLIBRI_OK) return st;
@@ -514,14 +517,15 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
 
     if (h->grouped_ok) {
         bool ok = make_tmap_bf16(&h->tm_xp, h->xp, P, d, 128) &&
-                  make_tmap_bf16(&h->tm_wgu, h->wgu, (uint64_t)E * 2 * f, d, 256) &&
+                  make_tmap_bf16(&h->tm_wgu, h->wgu, (uint64_t)E * 2 * f, d, 128) &&
                   make_tmap_bf16(&h->tm_h, h->H, P, f, 128) &&
-                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 256) &&
+                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 128) &&
                   make_tmap_bf16(&h->tm_wr, h->wr, (uint64_t)h->e_pad, d, (uint32_t)h->e_pad);
         if (!ok) {
             if (cfg->executor == COLIBRI_EXEC_GROUPED) return fail(COLIBRI_ERR_CUDA);
             h->grouped_ok = false;
         }
+        h->max_resident_pairs = tc_gemm_max_pairs();
     }
     if ((st = from_cuda(cudaDeviceSynchronize())) != COLIBRI_OK) return fail(st);
     *out = h;
