@@ -381,7 +381,6 @@ def run_ours(args):
             a_s = algorithmic(shape, Ts, cs)
             t_step = ms_s / args.steps / 1e3
             sweep[f"T{Ts}" + ("" if ex == "auto" else "_" + ex)] = {
-                               "executor": "grouped" if "gather" in st_s else "stream",
                                "tokens_per_s": round(world * Ts / t_step, 1),
                                "us_per_step": round(t_step * 1e6, 1),
                                "hbm_frac_of_measured": round(a_s["bytes"] / t_step / 1e9 / pk["hbm_gbs"], 4),

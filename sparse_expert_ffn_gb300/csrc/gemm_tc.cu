@@ -41,6 +41,7 @@
 #include "common.cuh"
 #include "gemm_tc.h"
 #include "kernels.h"
+#include "routing.cuh"
 
 namespace colibri {
 
@@ -351,15 +352,6 @@ __device__ __forceinline__ Work get_work(int w, const TcGemmArgs& a) {
     else return decode_work(w, a.n_blocks, a.k_splits, a.tile_expert, a.tile_row, a.tile_info);
 }
 
-// Total order on float logits as an unsigned key (as the CUDA-core router):
-// larger value -> larger key, -0 == +0, NaN below -inf.
-__device__ __forceinline__ uint32_t order_key(float v) {
-    if (v != v) return 0u;
-    if (v == 0.0f) v = 0.0f;
-    const uint32_t b = __float_as_uint(v);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
 // ---------------------------------------------------------------- the kernel
 
 template <int kMode, bool kPair>
@@ -557,7 +549,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             float l = __uint_as_float(v[i]);
                             if (args.bias) l += args.bias[e];
                             unsigned long long kk =
-                                ((unsigned long long)order_key(l) << 32) | (uint32_t)(~(uint32_t)e);
+                                ((unsigned long long)logit_order_key(l) << 32) | (uint32_t)(~(uint32_t)e);
                             float vv = l;
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
@@ -698,7 +690,7 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcG
                        int grid, cudaStream_t s) {
     const size_t smem = tc_gemm_smem_bytes();
     auto k = grouped_gemm_tc<kMode, kPair>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    smem_attr((const void*)k, (int)smem);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
@@ -714,14 +706,16 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcG
     return cudaLaunchKernelEx(&cfg, k, tmA, tmB, args);
 }
 
-cudaError_t launch_tc_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
+cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;
     cudaError_t e;
     if (mode == kGateUp)
-        e = launch_one<kGateUp, true>(tmA, tmB, args, grid & ~1, s);
+        e = pair ? launch_one<kGateUp, true>(tmA, tmB, args, grid & ~1, s)
+                 : launch_one<kGateUp, false>(tmA, tmB, args, grid, s);
     else if (mode == kDown)
-        e = launch_one<kDown, true>(tmA, tmB, args, grid & ~1, s);
+        e = pair ? launch_one<kDown, true>(tmA, tmB, args, grid & ~1, s)
+                 : launch_one<kDown, false>(tmA, tmB, args, grid, s);
     else
         e = launch_one<kRouter, false>(tmA, tmB, args, grid, s);
     if (e != cudaSuccess) return e;
@@ -744,8 +738,7 @@ int tc_gemm_max_pairs() {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         auto k = grouped_gemm_tc<kGateUp, true>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)tc_gemm_smem_bytes());
+        smem_attr((const void*)k, (int)tc_gemm_smem_bytes());
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) n = 0;
         pairs = n;

@@ -41,7 +41,9 @@ int tc_gemm_pair_rows();     // rows of one expert tile of a CTA pair (256)
 int tc_gemm_max_pairs();     // CTA pairs resident at once (0 if unknown)
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
-cudaError_t launch_tc_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB,
+// pair: run the expert GEMMs on CTA pairs (256-row tiles, B tensor map with
+// 128-row boxes) instead of single CTAs (128-row tiles, 256-row B boxes).
+cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s);
 
 }  // namespace colibri

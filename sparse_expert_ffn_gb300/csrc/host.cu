@@ -55,9 +55,10 @@ struct colibri_moe {
     int32_t* tile_row = nullptr;
     int32_t* tile_info = nullptr;
     int32_t* num_tiles = nullptr;
+    int32_t* block_counts = nullptr;  // multi-CTA dispatch: per-CTA counts, then bases
     int* status = nullptr;
-    void* xp = nullptr;     // [max_pairs, d]
     void* H = nullptr;      // [max_pairs, f]
+    void* xp = nullptr;     // [max_pairs, d] token rows in expert order
     float* Y = nullptr;     // [max_pairs, d]
     void* u = nullptr;      // [max_tokens, d]
     void* x_stage = nullptr;
@@ -66,7 +67,8 @@ struct colibri_moe {
     int max_tiles = 0;
     int max_resident_pairs = 0;  // CTA pairs of the expert GEMMs resident at once
     bool grouped_ok = false;
-    CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT, tm_wr;
+    // B operands: 128-row boxes for CTA pairs, 256-row boxes for single CTAs
+    CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT, tm_wr, tm_wgu1, tm_wdT1;
     uint64_t wait_limit_ns = 2000000000ull;
     bool stall_tma = false;  // failure-detection tests (COLIBRI_TEST_STALL_TMA=1)
     int last_T = 0;
@@ -108,6 +110,8 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 // Split-K of the down projection: only for batches of at most kSplitMaxPairs
 // (token, slot) pairs, into at most kMaxKSplit slices; Y holds room for them.
 constexpr int kSplitMaxPairs = 2048;
+// Above this many (token, slot) pairs the dispatch runs over many CTAs.
+constexpr int kMultiDispatchPairs = 12288;
 // Batches from this many tokens route on the tensor cores.
 constexpr int kTcRouterMinTokens = 512;
 constexpr int kMaxKSplit = 8;
@@ -250,7 +254,23 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     const int E = c.n_experts, k = c.top_k, d = c.d_model, f = c.d_ff;
     const int npairs = T * k;
     colibri_status_t st;
-    if (h->grouped_ok && T >= kTcRouterMinTokens) {
+    const int ex = choose_executor(h, T);
+    // Expert GEMMs on CTA pairs (256-row tiles) once the batch averages 128
+    // rows per expert; below that most tile rows would be empty and single
+    // CTAs (128-row tiles) stream the weights faster.
+    const bool pair = ex == COLIBRI_EXEC_GROUPED && npairs >= 128 * E;
+    const int tile_rows = pair ? tc_gemm_pair_rows() : tc_gemm_block_m();
+    // Small batch: router, top-k, softmax, dispatch and gather in one CTA.
+    const bool fused_routing = route_small_fits(T, d, E, k);
+    if (fused_routing) {
+        Stage g(h, COLIBRI_STAGE_ROUTER, s);
+        st = g.done(launch_route_small(h->dt, x, h->wr, h->bias, T, d, E, k, h->topk_idx,
+                                       h->topk_w, h->counts, h->offsets, h->perm, h->inv,
+                                       tile_rows, h->tile_expert, h->tile_row, h->tile_info,
+                                       h->num_tiles, h->status,
+                                       ex == COLIBRI_EXEC_GROUPED ? h->xp : nullptr, s), 1);
+        if (st != COLIBRI_OK) return st;
+    } else if (h->grouped_ok && T >= kTcRouterMinTokens) {
         // Large batch: the router logits are a [T, d] x [d, E] GEMM on the
         // tensor cores, top-k and softmax in its epilogue.
         CUtensorMap tm_x;
@@ -271,7 +291,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.stall_producer = h->stall_tma ? 1 : 0;
         const int grid = std::min((T + tc_gemm_block_m() - 1) / tc_gemm_block_m(), h->num_sms);
         Stage g(h, COLIBRI_STAGE_ROUTER, s);
-        st = g.done(launch_tc_gemm(kRouter, tm_x, h->tm_wr, a, grid, s), 1);
+        st = g.done(launch_tc_gemm(kRouter, false, tm_x, h->tm_wr, a, grid, s), 1);
         if (st != COLIBRI_OK) return st;
     } else {
         Stage g(h, COLIBRI_STAGE_ROUTER, s);
@@ -279,14 +299,21 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
                                        h->topk_w, s), 1);
         if (st != COLIBRI_OK) return st;
     }
-    {
+    if (!fused_routing && npairs > kMultiDispatchPairs) {
+        // many pairs: the counting sort over many CTAs (three launches)
+        Stage g(h, COLIBRI_STAGE_DISPATCH, s);
+        st = g.done(launch_dispatch_multi(h->topk_idx, npairs, E, h->block_counts, h->counts,
+                                          h->offsets, h->perm, h->inv, tile_rows,
+                                          h->tile_expert, h->tile_row, h->tile_info,
+                                          h->num_tiles, h->status, s), 3);
+        if (st != COLIBRI_OK) return st;
+    } else if (!fused_routing) {
         Stage g(h, COLIBRI_STAGE_DISPATCH, s);
         st = g.done(launch_dispatch(h->topk_idx, npairs, E, h->counts, h->offsets, h->perm,
-                                    h->inv, tc_gemm_pair_rows(), h->tile_expert, h->tile_row,
+                                    h->inv, tile_rows, h->tile_expert, h->tile_row,
                                     h->tile_info, h->num_tiles, h->status, s), 1);
         if (st != COLIBRI_OK) return st;
     }
-    const int ex = choose_executor(h, T);
     int nsplit = 1;
     size_t split_stride = 0;
     if (ex == COLIBRI_EXEC_STREAM) {
@@ -303,15 +330,20 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             if (st != COLIBRI_OK) return st;
         }
     } else {
-        {
+        // Expert tiles: 256 rows per CTA pair (each CTA 128), or 128 rows per CTA.
+        const int tiles_ub = (npairs + tile_rows - 1) / tile_rows + std::min(E, npairs);
+        // resident work units: CTA pairs, or single CTAs
+        const int units = pair ? (h->max_resident_pairs > 0 ? h->max_resident_pairs : h->num_sms / 2)
+                               : h->num_sms;
+        const int cta_per_unit = pair ? 2 : 1;
+        if (!fused_routing) {
+            // token rows in expert order (the gate/up GEMM's A operand); TMA
+            // boxes of 128 consecutive rows read it far faster than per-row
+            // gathers inside the GEMM
             Stage g(h, COLIBRI_STAGE_GATHER, s);
             st = g.done(launch_gather(h->esz, x, h->perm, k, d, npairs, h->xp, s), 1);
             if (st != COLIBRI_OK) return st;
         }
-        // Expert tiles of 256 rows, one per CTA pair (each CTA 128 rows).
-        const int tiles_ub =
-            (npairs + tc_gemm_pair_rows() - 1) / tc_gemm_pair_rows() + std::min(E, npairs);
-        const int max_pairs = h->max_resident_pairs > 0 ? h->max_resident_pairs : h->num_sms / 2;
         TcGemmArgs a{};
         a.tile_expert = h->tile_expert;
         a.tile_row = h->tile_row;
@@ -329,9 +361,11 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.out = h->H;
         a.out_ld = f;
         {
-            const int grid = 2 * (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks, max_pairs);
+            const int grid =
+                cta_per_unit * (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks, units);
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
-            st = g.done(launch_tc_gemm(kGateUp, h->tm_xp, h->tm_wgu, a, grid, s), 1);
+            st = g.done(launch_tc_gemm(kGateUp, pair, h->tm_xp, pair ? h->tm_wgu : h->tm_wgu1, a,
+                                       grid, s), 1);
             if (st != COLIBRI_OK) return st;
         }
         // down: N = d in blocks of 256, K = f.  Few pairs leave too few
@@ -345,17 +379,18 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.k_splits = 1;
         if (npairs <= kSplitMaxPairs) {
             const int64_t items = (int64_t)tiles_ub * a.n_blocks;
-            int ks = (int)std::min<int64_t>(kMaxKSplit, (2 * max_pairs + items - 1) / items);
+            int ks = (int)std::min<int64_t>(kMaxKSplit, (2 * units + items - 1) / items);
             ks = std::max(1, std::min(ks, a.k_blocks));
             const int per = (a.k_blocks + ks - 1) / ks;
             a.k_splits = (a.k_blocks + per - 1) / per;  // every slice non-empty
         }
         a.out_split_stride = (size_t)npairs * d;
         {
-            const int grid =
-                2 * (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks * a.k_splits, max_pairs);
+            const int grid = cta_per_unit * (int)std::min<int64_t>(
+                                                    (int64_t)tiles_ub * a.n_blocks * a.k_splits, units);
             Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
-            st = g.done(launch_tc_gemm(kDown, h->tm_h, h->tm_wdT, a, grid, s), 1);
+            st = g.done(launch_tc_gemm(kDown, pair, h->tm_h, pair ? h->tm_wdT : h->tm_wdT1, a, grid,
+                                       s), 1);
             if (st != COLIBRI_OK) return st;
         }
         nsplit = a.k_splits;
@@ -488,6 +523,7 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
                  o_off = carve((size_t)(E + 1) * 4), o_perm = carve(P * 4), o_inv = carve(P * 4),
                  o_te = carve((size_t)h->max_tiles * 4), o_tr = carve((size_t)h->max_tiles * 4),
                  o_tinfo = carve((size_t)h->max_tiles * 4), o_nt = carve(4), o_st = carve(4),
+                 o_bc = carve((size_t)dispatch_blocks(h->max_pairs) * E * 4),
                  o_xp = h->grouped_ok ? carve(P * d * h->esz) : 0, o_h = carve(P * f * h->esz),
                  o_y = carve(std::max(P, (size_t)kMaxKSplit * std::min<size_t>(P, kSplitMaxPairs)) *
                              d * 4),
@@ -507,6 +543,7 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     h->tile_info = (int32_t*)(b + o_tinfo);
     h->num_tiles = (int32_t*)(b + o_nt);
     h->status = (int*)(b + o_st);
+    h->block_counts = (int32_t*)(b + o_bc);
     h->xp = h->grouped_ok ? (void*)(b + o_xp) : nullptr;
     h->H = b + o_h;
     h->Y = (float*)(b + o_y);
@@ -520,6 +557,8 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
                   make_tmap_bf16(&h->tm_wgu, h->wgu, (uint64_t)E * 2 * f, d, 128) &&
                   make_tmap_bf16(&h->tm_h, h->H, P, f, 128) &&
                   make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 128) &&
+                  make_tmap_bf16(&h->tm_wgu1, h->wgu, (uint64_t)E * 2 * f, d, 256) &&
+                  make_tmap_bf16(&h->tm_wdT1, h->wdT, (uint64_t)E * d, f, 256) &&
                   make_tmap_bf16(&h->tm_wr, h->wr, (uint64_t)h->e_pad, d, (uint32_t)h->e_pad);
         if (!ok) {
             if (cfg->executor == COLIBRI_EXEC_GROUPED) return fail(COLIBRI_ERR_CUDA);

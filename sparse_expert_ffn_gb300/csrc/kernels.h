@@ -10,6 +10,10 @@ namespace colibri {
 
 enum class DType : int;
 
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel and size:
+// a host-side cache keeps it off the per-launch path.
+cudaError_t smem_attr(const void* kernel, int bytes);
+
 cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const float* bias,
                                int ntok, int d, int E, int k, int32_t* idx, float* w,
                                cudaStream_t s);
@@ -19,6 +23,25 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int n, int E, int32_t* coun
                             int32_t* offsets, int32_t* perm, int32_t* inv, int bm,
                             int32_t* tile_expert, int32_t* tile_row, int32_t* tile_info,
                             int32_t* num_tiles, int* status, cudaStream_t s);
+
+// The same dispatch over ceil(n / 2048) CTAs (three launches); block_counts
+// holds dispatch_blocks(n) * E int32.
+int dispatch_blocks(int n);
+cudaError_t launch_dispatch_multi(const int32_t* topk_idx, int n, int E, int32_t* block_counts,
+                                  int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                  int bm, int32_t* tile_expert, int32_t* tile_row,
+                                  int32_t* tile_info, int32_t* num_tiles, int* status,
+                                  cudaStream_t s);
+
+// Router + top-k + softmax + dispatch (+ gather when xp != null) in one CTA,
+// for batches where route_small_fits().
+bool route_small_fits(int ntok, int d, int E, int k);
+cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const float* bias,
+                               int ntok, int d, int E, int k, int32_t* topk_idx, float* topk_w,
+                               int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                               int bm, int32_t* tile_expert, int32_t* tile_row,
+                               int32_t* tile_info, int32_t* num_tiles, int* status, void* xp,
+                               cudaStream_t s);
 
 cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* counts,
                                  const int32_t* offsets, const int32_t* perm, int k, int d, int f,

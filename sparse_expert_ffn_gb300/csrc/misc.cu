@@ -1,4 +1,7 @@
 // Gather, combine, RMSNorm and the init-time weight repack.
+#include <mutex>
+#include <unordered_map>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -122,6 +125,23 @@ cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, in
     const int row_vecs = d * elem_bytes / 16;
     gather_rows<<<npairs, 128, 0, s>>>((const uint4*)x, perm, k, row_vecs, (uint4*)xp);
     return cudaGetLastError();
+}
+
+cudaError_t smem_attr(const void* kernel, int bytes) {
+    // keyed by (device, kernel): the attribute belongs to the kernel's
+    // instance on the current device
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> done;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t key = (reinterpret_cast<uint64_t>(kernel) << 8) ^ (uint64_t)dev;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[key] = bytes;
+    return e;
 }
 
 cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const int32_t* inv,

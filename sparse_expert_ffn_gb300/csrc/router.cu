@@ -13,21 +13,13 @@
 // selected logits, with the largest subtracted first.
 #include "common.cuh"
 #include "kernels.h"
+#include "routing.cuh"
 
 namespace colibri {
 
 namespace {
 
 constexpr int kRouterWarps = 8;
-
-// Total order on float logits as an unsigned key: larger value -> larger key,
-// -0 == +0, NaN below -inf.
-__device__ __forceinline__ uint32_t order_key(float v) {
-    if (v != v) return 0u;
-    if (v == 0.0f) v = 0.0f;
-    uint32_t b = __float_as_uint(v);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
 
 // One CTA of kRouterWarps warps routes kRouterWarps / kWarpsPerToken tokens;
 // the kWarpsPerToken warps of a token split its experts (e = sub, sub + W, ...).
@@ -78,37 +70,7 @@ router_topk_simt(const T* __restrict__ x, const T* __restrict__ wr, const float*
     __syncthreads();
     if (!live || sub != 0) return;
 
-    // k rounds of a warp arg-max; each lane owns experts lane, lane+32, ...
-    uint32_t taken = 0;
-    int sel_e[8];
-    float sel_l[8];
-    for (int j = 0; j < k; ++j) {
-        unsigned long long best = 0ull;
-        for (int s = 0, e = lane; e < E; ++s, e += 32) {
-            if (taken & (1u << s)) continue;
-            unsigned long long key =
-                ((unsigned long long)order_key(logit[e]) << 32) | (uint32_t)(~(uint32_t)e);
-            best = key > best ? key : best;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-            best = other > best ? other : best;
-        }
-        const int e = (int)(~(uint32_t)(best & 0xffffffffull));
-        if ((e & 31) == lane) taken |= 1u << (e >> 5);
-        sel_e[j] = e;
-        sel_l[j] = logit[e];
-    }
-    if (lane == 0) {
-        const float m = sel_l[0];
-        float sum = 0.f;
-        for (int j = 0; j < k; ++j) sum += expf(sel_l[j] - m);
-        for (int j = 0; j < k; ++j) {
-            topk_idx[(size_t)t * k + j] = sel_e[j];
-            topk_w[(size_t)t * k + j] = expf(sel_l[j] - m) / sum;
-        }
-    }
+    warp_topk_softmax(logit, E, k, lane, topk_idx + (size_t)t * k, topk_w + (size_t)t * k);
 }
 
 template <typename T, int kWarpsPerToken>
@@ -118,7 +80,7 @@ cudaError_t launch_router_t(const void* x, const void* wr, const float* bias, in
     const dim3 grid((ntok + kTokens - 1) / kTokens), block(kRouterWarps * 32);
     const size_t smem = (size_t)kTokens * (d + 256) * sizeof(float);
     auto kern = router_topk_simt<T, kWarpsPerToken>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    smem_attr((const void*)kern, (int)smem);
     kern<<<grid, block, smem, s>>>((const T*)x, (const T*)wr, bias, ntok, d, E, k, idx, w);
     return cudaGetLastError();
 }

@@ -53,19 +53,22 @@ def test_injected_allocation_failure_rolls_back(lib, monkeypatch):
     layer.close()
 
 
-def test_bounded_wait_times_out_and_context_survives(lib, monkeypatch):
+# 256 tokens run the expert GEMMs on single CTAs, 1024 on CTA pairs
+# (at least 128 (token, slot) pairs per expert on average).
+@pytest.mark.parametrize("T", [256, 1024], ids=["single_cta", "cta_pairs"])
+def test_bounded_wait_times_out_and_context_survives(lib, monkeypatch, T):
     sef = lib
     dev = torch.device("cuda", 0)
     ws = _weights(dev)
-    x = synth.tokens(SHAPE, 256, 3, 0, dev)
+    x = synth.tokens(SHAPE, T, 3, 0, dev)
 
-    ref_layer = sef.MoELayer(*ws, SHAPE.top_k, max_tokens=256, executor="grouped")
+    ref_layer = sef.MoELayer(*ws, SHAPE.top_k, max_tokens=T, executor="grouped")
     y_ref = ref_layer.forward(x)
     assert ref_layer.check() == sef.OK
 
     monkeypatch.setenv("COLIBRI_WAIT_LIMIT_NS", "20000000")
     monkeypatch.setenv("COLIBRI_TEST_STALL_TMA", "1")
-    short = sef.MoELayer(*ws, SHAPE.top_k, max_tokens=256, executor="grouped")
+    short = sef.MoELayer(*ws, SHAPE.top_k, max_tokens=T, executor="grouped")
     monkeypatch.delenv("COLIBRI_WAIT_LIMIT_NS")
     monkeypatch.delenv("COLIBRI_TEST_STALL_TMA")
     short.forward(x)
