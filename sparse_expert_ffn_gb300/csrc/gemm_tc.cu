@@ -58,6 +58,8 @@ template <bool kPair> struct Ring {
     static constexpr uint32_t kStageB = (kPair ? 128 : 256) * 64 * 2;
 };
 constexpr int kThreads = 192;
+constexpr uint32_t kRingBytes = 192 * 1024;   // shared-memory ring of every instantiation
+constexpr int kMaxRouterStages = 12;
 constexpr int kAccCols = 256;     // TMEM columns per accumulator
 constexpr int kTmemCols = 512;    // two accumulators
 constexpr uint32_t kStageA = kBM * kBK * 2;   // 16 KB
@@ -362,8 +364,13 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // 1024-byte alignment for the 128-byte swizzle atoms.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    constexpr int kStages = Ring<kPair>::kStages;
-    constexpr uint32_t kStageB = Ring<kPair>::kStageB;
+    // The router's B tile is only E_pad rows: its ring is as deep as fits
+    // (up to kMaxRouterStages) in the same bytes; the expert GEMMs use Ring.
+    constexpr int kMaxSt = kMode == kRouter ? kMaxRouterStages : Ring<kPair>::kStages;
+    const uint32_t kStageB = kMode == kRouter ? (uint32_t)args.bn_rows * kBK * 2 : Ring<kPair>::kStageB;
+    const int kStages = kMode == kRouter
+                            ? min(kMaxRouterStages, (int)(kRingBytes / (kStageA + kStageB)))
+                            : Ring<kPair>::kStages;
     uint8_t* stage_a = smem;
     uint8_t* stage_b = smem + kStages * kStageA;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * (kStageA + kStageB));
@@ -421,8 +428,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            bool issued[kStages];
-            uint32_t issued_phase[kStages];
+            bool issued[kMaxSt];
+            uint32_t issued_phase[kMaxSt];
             for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
             for (int w = unit; w < total && !*abort_flag && !args.stall_producer; w += n_units) {
                 const Work wk = get_work<kMode>(w, args);
