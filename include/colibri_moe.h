@@ -139,6 +139,21 @@ colibri_status_t colibri_rmsnorm_moe_residual(colibri_moe_t* h, void* hidden, in
 colibri_status_t colibri_get_routing(colibri_moe_t* h, int32_t* topk_idx, float* topk_w,
                                      int32_t* counts, int32_t* perm, void* stream);
 
+/*
+ * colibri_set_capacity - hard expert capacity for later forwards (cf-1.com
+ * section 2.3: an expert's capacity is the most tokens it handles in one
+ * batch; section 4.2: --expert-capacity is a hard limit and tokens past it are
+ * dropped; zskr.cn section 2.2: hard_capacity).  Each expert accepts at most
+ * `capacity` (token, slot) pairs, in token order and then slot order; a
+ * dropped pair adds nothing to its token's output and the token's other gates
+ * are left unchanged.  capacity < 0 (the default) removes the limit; 0 drops
+ * every pair (y = 0, or y = hidden for the residual layer).
+ * colibri_get_routing still reports every routed pair: counts are before the
+ * limit, and expert e kept perm[offsets[e] .. offsets[e] + min(counts[e],
+ * capacity)) with offsets the exclusive prefix sum of counts.
+ */
+colibri_status_t colibri_set_capacity(colibri_moe_t* h, int32_t capacity);
+
 /* colibri_set_executor - choose the expert executor for later forwards.
  * GROUPED needs dtype BF16 (UNSUPPORTED otherwise). */
 colibri_status_t colibri_set_executor(colibri_moe_t* h, int32_t executor);

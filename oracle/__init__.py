@@ -20,6 +20,7 @@ from .moe import (  # noqa: F401
     topk_select,
     softmax_selected,
     dispatch,
+    capacity_keep,
     silu,
     swiglu_expert,
     combine,

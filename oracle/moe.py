@@ -19,7 +19,8 @@ Readings where the pages are silent (each is also listed in the design notes):
   descending logit order.  NaN ranks below -inf.
 * No learned router bias; an optional per-expert offset (Zipf skew or a
   -inf mask) is added to the logits before top-k and softmax.
-* No capacity limit: every (token, slot) pair is computed.
+* No capacity limit unless one is given; with a hard capacity C an expert
+  accepts its pairs in token order, then slot order, up to C (capacity_keep).
 * Arithmetic is float64 throughout; ``round_h`` optionally rounds the
   SwiGLU hidden activation to bfloat16 the way a bf16 tensor-core operand is.
 """
@@ -167,6 +168,31 @@ def dispatch(idx: np.ndarray, n_experts: int):
     return counts, offsets, perm, inv
 
 
+def capacity_keep(idx: np.ndarray, n_experts: int, capacity=None) -> np.ndarray:
+    """Boolean [T, k]: the (token, slot) pairs their experts accept under a
+    hard capacity of `capacity` pairs per expert (None: no limit).
+
+    cf-1.com section 2.3 (an expert's capacity is the most tokens it handles in
+    one batch) and section 4.2 (--expert-capacity is a hard limit: tokens past
+    it are dropped); zskr.cn "Colibri：面向MoE架构的C语言高效推理引擎解析"
+    section 2.2 (hard_capacity).  Reading: each expert accepts its pairs in
+    increasing r = t*k + j (token order, then slot) until it holds `capacity`;
+    a dropped pair adds nothing to its token's output and the other gates are
+    left as they are.
+    """
+    T, k = idx.shape
+    keep = np.ones((T, k), dtype=bool)
+    if capacity is None:
+        return keep
+    held = np.zeros(n_experts, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            keep[t, j] = held[e] < capacity
+            held[e] += 1
+    return keep
+
+
 # ----------------------------------------------------------------------------
 # Step 5: the expert FFN.
 
@@ -194,17 +220,19 @@ def swiglu_expert(xs: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray,
 # Step 6: combine.
 
 
-def combine(y_perm: np.ndarray, g: np.ndarray, inv: np.ndarray) -> np.ndarray:
+def combine(y_perm: np.ndarray, g: np.ndarray, inv: np.ndarray, keep=None) -> np.ndarray:
     """y[t] = sum_j g[t, j] * y_perm[inv[t*k + j]], j = 0..k-1 in order.
 
     zskr.cn section 3.3 stage 5 (aggregate_kernel adds every expert's output
-    slice, weighted by its score, into the output buffer).
+    slice, weighted by its score, into the output buffer).  Pairs with
+    keep[t, j] False (dropped by an expert's capacity) add nothing.
     """
     T, k = g.shape
     y = np.zeros((T, y_perm.shape[1]), dtype=np.float64)
     for j in range(k):
         rows = inv[np.arange(T) * k + j]
-        y += g[:, j:j + 1] * y_perm[rows]
+        w = g[:, j:j + 1] if keep is None else np.where(keep[:, j:j + 1], g[:, j:j + 1], 0.0)
+        y += w * y_perm[rows]
     return y
 
 
@@ -213,14 +241,15 @@ def combine(y_perm: np.ndarray, g: np.ndarray, inv: np.ndarray) -> np.ndarray:
 
 
 def moe_layer(x, w_router, w_gate, w_up, w_down, top_k, offset=None,
-              round_h=False):
+              round_h=False, capacity=None):
     """The full layer: logits, top-k, softmax, dispatch, experts, combine.
 
     pnsm.cn section 2.2 (one MoE forward: router logits, top-k indices,
     gather of the chosen experts, expert forward, gate-weighted sum) with the
     steps as zskr.cn section 3.3 stages 2-5 run them.  Arguments are float64
     arrays in the library's input layout: x [T,d], W_r [d,E],
-    W_g/W_u [E,d,f], W_d [E,f,d].
+    W_g/W_u [E,d,f], W_d [E,f,d].  `capacity` limits the pairs each expert
+    accepts (capacity_keep).
     """
     E = w_router.shape[1]
     l = router_logits(x, w_router, offset)
@@ -235,19 +264,23 @@ def moe_layer(x, w_router, w_gate, w_up, w_down, top_k, offset=None,
             continue
         rows = perm[lo:hi] // top_k
         y_perm[lo:hi] = swiglu_expert(x[rows], w_gate[e], w_up[e], w_down[e], round_h)
-    y = combine(y_perm, g, inv)
+    keep = capacity_keep(idx, E, capacity)
+    y = combine(y_perm, g, inv, keep)
     return {"logits": l, "topk_idx": idx, "topk_w": g, "counts": counts,
-            "offsets": offsets, "perm": perm, "inv": inv, "y": y}
+            "offsets": offsets, "perm": perm, "inv": inv, "keep": keep, "y": y}
 
 
-def token_outputs(x_rows, idx_rows, g_rows, expert, round_h=False):
+def token_outputs(x_rows, idx_rows, g_rows, expert, round_h=False, keep_rows=None):
     """y for a few tokens given their routing: sum_j g_j * FFN_{idx_j}(x).
 
     The same sum as dispatch followed by combine, evaluated token by token,
     for checking sampled rows of a large layer.  ``expert(e)`` returns the
-    float64 (W_g, W_u, W_d) of expert e.
+    float64 (W_g, W_u, W_d) of expert e; ``keep_rows`` (capacity_keep of the
+    whole batch, rows of these tokens) drops pairs.
     """
     n, k = idx_rows.shape
+    if keep_rows is not None:
+        g_rows = np.where(keep_rows, g_rows, 0.0)
     y = np.zeros((n, x_rows.shape[1]), dtype=np.float64)
     for e in sorted(set(int(v) for v in idx_rows.reshape(-1))):
         wg, wu, wd = expert(e)

@@ -55,6 +55,7 @@ def _load():
         "colibri_rmsnorm_moe_residual": ([P, P, I32, P, ctypes.c_float, P], I32),
         "colibri_get_routing": ([P, P, P, P, P, P], I32),
         "colibri_set_executor": ([P, I32], I32),
+        "colibri_set_capacity": ([P, I32], I32),
         "colibri_check": ([P, P], I32),
         "colibri_launch_count": ([P, U64P], I32),
         "colibri_workspace_bytes": ([P, U64P, U64P], I32),
@@ -74,6 +75,7 @@ def _load():
 _lib = None
 _C_NAMES = ("colibri_init", "colibri_forward", "colibri_forward_host",
             "colibri_rmsnorm_moe_residual", "colibri_get_routing", "colibri_set_executor",
+            "colibri_set_capacity",
             "colibri_check", "colibri_launch_count", "colibri_workspace_bytes",
             "colibri_profile_enable", "colibri_profile_read", "colibri_route_static",
             "colibri_free")
@@ -210,6 +212,11 @@ class MoELayer:
 
     def set_executor(self, executor: str):
         _check(library().colibri_set_executor(self._h, _EXEC[executor]), "colibri_set_executor")
+
+    def set_capacity(self, capacity: Optional[int]):
+        """Hard per-expert capacity for later forwards (None: no limit)."""
+        _check(library().colibri_set_capacity(self._h, -1 if capacity is None else int(capacity)),
+               "colibri_set_capacity")
 
     def check(self, stream=None) -> int:
         """Wait for the stream; returns the library status (0 = OK)."""

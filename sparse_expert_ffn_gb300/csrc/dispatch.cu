@@ -18,10 +18,11 @@ dispatch_kernel(const int32_t* __restrict__ topk_idx, int n, int E, int32_t* __r
                 int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                 int32_t* __restrict__ inv, int bm, int32_t* __restrict__ tile_expert,
                 int32_t* __restrict__ tile_row, int32_t* __restrict__ tile_info,
-                int32_t* __restrict__ num_tiles, int* __restrict__ status) {
+                int32_t* __restrict__ num_tiles, int* __restrict__ status, int cap,
+                int32_t* __restrict__ kept) {
     extern __shared__ int32_t sh[];
     dispatch_block(topk_idx, n, E, counts, offsets, perm, inv, bm, tile_expert, tile_row,
-                   tile_info, num_tiles, status, sh);
+                   tile_info, num_tiles, status, cap, kept, sh);
 }
 
 // ---- Multi-CTA dispatch for large batches: CTA b owns the pairs
@@ -53,7 +54,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_scan_kernel(int32_t* __restrict__ block_counts, int nb, int E,
                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int bm,
                      int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row,
-                     int32_t* __restrict__ tile_info, int32_t* __restrict__ num_tiles) {
+                     int32_t* __restrict__ tile_info, int32_t* __restrict__ num_tiles, int cap,
+                     int32_t* __restrict__ kept) {
     __shared__ int32_t ecount[256], eoff[257], tbase[257];
     const int e = threadIdx.x;
     if (e < E) {
@@ -68,7 +70,7 @@ dispatch_scan_kernel(int32_t* __restrict__ block_counts, int nb, int E,
             eoff[i] = acc;
             tbase[i] = tacc;
             acc += ecount[i];
-            tacc += (ecount[i] + bm - 1) / bm;
+            tacc += (min(ecount[i], cap) + bm - 1) / bm;
         }
         eoff[E] = acc;
         *num_tiles = tacc;
@@ -83,16 +85,20 @@ dispatch_scan_kernel(int32_t* __restrict__ block_counts, int nb, int E,
             run += c;
         }
         counts[e] = ecount[e];
+        kept[e] = min(ecount[e], cap);
         offsets[e] = eoff[e];
-        write_tiles(e, ecount[e], eoff[e], tbase[e], bm, tile_expert, tile_row, tile_info);
+        write_tiles(e, min(ecount[e], cap), eoff[e], tbase[e], bm, tile_expert, tile_row,
+                    tile_info);
     }
 }
 
 // 3. per CTA: the warps' bases from the CTA's bases, then the positions
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_scatter_kernel(const int32_t* __restrict__ topk_idx, int n, int E,
-                        const int32_t* __restrict__ block_base, int32_t* __restrict__ perm,
-                        int32_t* __restrict__ inv, int* __restrict__ status) {
+                        const int32_t* __restrict__ block_base,
+                        const int32_t* __restrict__ offsets, int cap,
+                        int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                        int* __restrict__ status) {
     extern __shared__ int32_t wcnt[];  // [kDispatchWarps][E]
     const int warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) wcnt[i] = 0;
@@ -111,7 +117,7 @@ dispatch_scatter_kernel(const int32_t* __restrict__ topk_idx, int n, int E,
         }
     }
     __syncthreads();
-    warp_scatter_pass(topk_idx, lo, hi, E, my, perm, inv);
+    warp_scatter_pass(topk_idx, lo, hi, E, my, offsets, cap, perm, inv);
 }
 
 }  // namespace
@@ -124,28 +130,30 @@ cudaError_t launch_dispatch_multi(const int32_t* topk_idx, int n, int E, int32_t
                                   int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                                   int bm, int32_t* tile_expert, int32_t* tile_row,
                                   int32_t* tile_info, int32_t* num_tiles, int* status,
-                                  cudaStream_t s) {
+                                  int cap, int32_t* kept, cudaStream_t s) {
     const int nb = dispatch_blocks(n);
     const size_t smem = (size_t)kDispatchWarps * E * sizeof(int32_t);
     dispatch_count_kernel<<<nb, kDispatchWarps * 32, smem, s>>>(topk_idx, n, E, block_counts,
                                                                 status);
     dispatch_scan_kernel<<<1, kDispatchWarps * 32, 0, s>>>(block_counts, nb, E, counts, offsets,
                                                            bm, tile_expert, tile_row, tile_info,
-                                                           num_tiles);
-    dispatch_scatter_kernel<<<nb, kDispatchWarps * 32, smem, s>>>(topk_idx, n, E, block_counts,
-                                                                  perm, inv, status);
+                                                           num_tiles, cap, kept);
+    dispatch_scatter_kernel<<<nb, kDispatchWarps * 32, smem, s>>>(
+        topk_idx, n, E, block_counts, offsets, cap, perm, inv, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int n, int E, int32_t* counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int bm,
                             int32_t* tile_expert, int32_t* tile_row, int32_t* tile_info,
-                            int32_t* num_tiles, int* status, cudaStream_t s) {
+                            int32_t* num_tiles, int* status, int cap, int32_t* kept,
+                            cudaStream_t s) {
     const size_t smem = dispatch_smem(E);
     smem_attr((const void*)dispatch_kernel, (int)smem);
     dispatch_kernel<<<1, kDispatchWarps * 32, smem, s>>>(topk_idx, n, E, counts, offsets, perm,
                                                          inv, bm, tile_expert, tile_row,
-                                                         tile_info, num_tiles, status);
+                                                         tile_info, num_tiles, status, cap,
+                                                         kept);
     return cudaGetLastError();
 }
 

@@ -14,7 +14,8 @@
 //                    (contiguous over d_ff) dotted with the H rows of the
 //                    expert's pairs; Y[p, c] in float32.
 // Pairs p are in expert order (the dispatch permutation), so the tokens of
-// one expert are consecutive rows of H and Y.
+// one expert are consecutive rows of H and Y; an expert computes the first
+// kept[e] rows of its segment (all of them unless a capacity drops some).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -37,13 +38,13 @@ __device__ __forceinline__ size_t gu_row(int e, int n, int which, int f) {
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 ffn_up_stream(const T* __restrict__ x, const T* __restrict__ wgu,
-              const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+              const int32_t* __restrict__ kept, const int32_t* __restrict__ offsets,
               const int32_t* __restrict__ perm, int k, int d, int f, int E, T* __restrict__ H) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = blockIdx.x * kWarps + warp;
     if (n >= f) return;
     for (int e = 0; e < E; ++e) {
-        const int c = counts[e];
+        const int c = kept[e];
         if (c == 0) continue;
         const int off = offsets[e];
         const T* g_row = wgu + gu_row(e, n, 0, f) * d;
@@ -98,13 +99,13 @@ ffn_up_stream(const T* __restrict__ x, const T* __restrict__ wgu,
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 ffn_down_stream(const T* __restrict__ H, const T* __restrict__ wdT,
-                const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets, int d,
+                const int32_t* __restrict__ kept, const int32_t* __restrict__ offsets, int d,
                 int f, int E, float* __restrict__ Y) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col = blockIdx.x * kWarps + warp;
     if (col >= d) return;
     for (int e = 0; e < E; ++e) {
-        const int c = counts[e];
+        const int c = kept[e];
         if (c == 0) continue;
         const int off = offsets[e];
         const T* w_row = wdT + ((size_t)e * d + col) * f;
@@ -146,29 +147,29 @@ ffn_down_stream(const T* __restrict__ H, const T* __restrict__ wdT,
 
 }  // namespace
 
-cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* counts,
+cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* kept,
                                  const int32_t* offsets, const int32_t* perm, int k, int d, int f,
                                  int E, void* H, cudaStream_t s) {
     const dim3 block(kWarps * 32), grid((f + kWarps - 1) / kWarps);
     if (dt == DType::BF16)
         ffn_up_stream<__nv_bfloat16><<<grid, block, 0, s>>>(
-            (const __nv_bfloat16*)x, (const __nv_bfloat16*)wgu, counts, offsets, perm, k, d, f,
+            (const __nv_bfloat16*)x, (const __nv_bfloat16*)wgu, kept, offsets, perm, k, d, f,
             E, (__nv_bfloat16*)H);
     else
-        ffn_up_stream<float><<<grid, block, 0, s>>>((const float*)x, (const float*)wgu, counts,
+        ffn_up_stream<float><<<grid, block, 0, s>>>((const float*)x, (const float*)wgu, kept,
                                                     offsets, perm, k, d, f, E, (float*)H);
     return cudaGetLastError();
 }
 
-cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, const int32_t* counts,
+cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, const int32_t* kept,
                                    const int32_t* offsets, int d, int f, int E, float* Y,
                                    cudaStream_t s) {
     const dim3 block(kWarps * 32), grid((d + kWarps - 1) / kWarps);
     if (dt == DType::BF16)
         ffn_down_stream<__nv_bfloat16><<<grid, block, 0, s>>>(
-            (const __nv_bfloat16*)H, (const __nv_bfloat16*)wdT, counts, offsets, d, f, E, Y);
+            (const __nv_bfloat16*)H, (const __nv_bfloat16*)wdT, kept, offsets, d, f, E, Y);
     else
-        ffn_down_stream<float><<<grid, block, 0, s>>>((const float*)H, (const float*)wdT, counts,
+        ffn_down_stream<float><<<grid, block, 0, s>>>((const float*)H, (const float*)wdT, kept,
                                                       offsets, d, f, E, Y);
     return cudaGetLastError();
 }

@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -48,6 +49,7 @@ struct colibri_moe {
     int32_t* topk_idx = nullptr;
     float* topk_w = nullptr;
     int32_t* counts = nullptr;
+    int32_t* kept = nullptr;     // [E] pairs each expert accepted (counts capped)
     int32_t* offsets = nullptr;
     int32_t* perm = nullptr;
     int32_t* inv = nullptr;
@@ -72,6 +74,7 @@ struct colibri_moe {
     uint64_t wait_limit_ns = 2000000000ull;
     bool stall_tma = false;  // failure-detection tests (COLIBRI_TEST_STALL_TMA=1)
     int last_T = 0;
+    int capacity = -1;   // hard expert capacity; < 0: no limit
     uint64_t launches = 0;
     colibri_status_t sticky = COLIBRI_OK;
     // opt-in per-stage event profiling
@@ -262,12 +265,13 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     const int tile_rows = pair ? tc_gemm_pair_rows() : tc_gemm_block_m();
     // Small batch: router, top-k, softmax, dispatch and gather in one CTA.
     const bool fused_routing = route_small_fits(T, d, E, k);
+    const int cap = h->capacity < 0 ? INT_MAX : h->capacity;
     if (fused_routing) {
         Stage g(h, COLIBRI_STAGE_ROUTER, s);
         st = g.done(launch_route_small(h->dt, x, h->wr, h->bias, T, d, E, k, h->topk_idx,
                                        h->topk_w, h->counts, h->offsets, h->perm, h->inv,
                                        tile_rows, h->tile_expert, h->tile_row, h->tile_info,
-                                       h->num_tiles, h->status,
+                                       h->num_tiles, h->status, cap, h->kept,
                                        ex == COLIBRI_EXEC_GROUPED ? h->xp : nullptr, s), 1);
         if (st != COLIBRI_OK) return st;
     } else if (h->grouped_ok && T >= kTcRouterMinTokens) {
@@ -305,13 +309,14 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         st = g.done(launch_dispatch_multi(h->topk_idx, npairs, E, h->block_counts, h->counts,
                                           h->offsets, h->perm, h->inv, tile_rows,
                                           h->tile_expert, h->tile_row, h->tile_info,
-                                          h->num_tiles, h->status, s), 3);
+                                          h->num_tiles, h->status, cap, h->kept, s), 3);
         if (st != COLIBRI_OK) return st;
     } else if (!fused_routing) {
         Stage g(h, COLIBRI_STAGE_DISPATCH, s);
         st = g.done(launch_dispatch(h->topk_idx, npairs, E, h->counts, h->offsets, h->perm,
                                     h->inv, tile_rows, h->tile_expert, h->tile_row,
-                                    h->tile_info, h->num_tiles, h->status, s), 1);
+                                    h->tile_info, h->num_tiles, h->status, cap, h->kept, s),
+                    1);
         if (st != COLIBRI_OK) return st;
     }
     int nsplit = 1;
@@ -319,13 +324,13 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     if (ex == COLIBRI_EXEC_STREAM) {
         {
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
-            st = g.done(launch_ffn_up_stream(h->dt, x, h->wgu, h->counts, h->offsets, h->perm, k,
+            st = g.done(launch_ffn_up_stream(h->dt, x, h->wgu, h->kept, h->offsets, h->perm, k,
                                              d, f, E, h->H, s), 1);
             if (st != COLIBRI_OK) return st;
         }
         {
             Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
-            st = g.done(launch_ffn_down_stream(h->dt, h->H, h->wdT, h->counts, h->offsets, d, f,
+            st = g.done(launch_ffn_down_stream(h->dt, h->H, h->wdT, h->kept, h->offsets, d, f,
                                                E, h->Y, s), 1);
             if (st != COLIBRI_OK) return st;
         }
@@ -520,6 +525,7 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
         return o;
     };
     const size_t o_idx = carve(P * 4), o_w = carve(P * 4), o_cnt = carve((size_t)E * 4),
+                 o_kept = carve((size_t)E * 4),
                  o_off = carve((size_t)(E + 1) * 4), o_perm = carve(P * 4), o_inv = carve(P * 4),
                  o_te = carve((size_t)h->max_tiles * 4), o_tr = carve((size_t)h->max_tiles * 4),
                  o_tinfo = carve((size_t)h->max_tiles * 4), o_nt = carve(4), o_st = carve(4),
@@ -535,6 +541,7 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     h->topk_idx = (int32_t*)(b + o_idx);
     h->topk_w = (float*)(b + o_w);
     h->counts = (int32_t*)(b + o_cnt);
+    h->kept = (int32_t*)(b + o_kept);
     h->offsets = (int32_t*)(b + o_off);
     h->perm = (int32_t*)(b + o_perm);
     h->inv = (int32_t*)(b + o_inv);
@@ -645,6 +652,12 @@ colibri_status_t colibri_set_executor(colibri_moe_t* h, int32_t executor) {
         return COLIBRI_ERR_INVALID_ARG;
     if (executor == COLIBRI_EXEC_GROUPED && !h->grouped_ok) return COLIBRI_ERR_UNSUPPORTED;
     h->cfg.executor = executor;
+    return COLIBRI_OK;
+}
+
+colibri_status_t colibri_set_capacity(colibri_moe_t* h, int32_t capacity) {
+    if (!h) return COLIBRI_ERR_INVALID_ARG;
+    h->capacity = capacity < 0 ? -1 : capacity;
     return COLIBRI_OK;
 }
 

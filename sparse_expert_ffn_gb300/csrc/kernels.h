@@ -22,7 +22,8 @@ size_t dispatch_smem(int E);
 cudaError_t launch_dispatch(const int32_t* topk_idx, int n, int E, int32_t* counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv, int bm,
                             int32_t* tile_expert, int32_t* tile_row, int32_t* tile_info,
-                            int32_t* num_tiles, int* status, cudaStream_t s);
+                            int32_t* num_tiles, int* status, int cap, int32_t* kept,
+                            cudaStream_t s);
 
 // The same dispatch over ceil(n / 2048) CTAs (three launches); block_counts
 // holds dispatch_blocks(n) * E int32.
@@ -31,7 +32,7 @@ cudaError_t launch_dispatch_multi(const int32_t* topk_idx, int n, int E, int32_t
                                   int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                                   int bm, int32_t* tile_expert, int32_t* tile_row,
                                   int32_t* tile_info, int32_t* num_tiles, int* status,
-                                  cudaStream_t s);
+                                  int cap, int32_t* kept, cudaStream_t s);
 
 // Router + top-k + softmax + dispatch (+ gather when xp != null) in one CTA,
 // for batches where route_small_fits().
@@ -40,13 +41,14 @@ cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const fl
                                int ntok, int d, int E, int k, int32_t* topk_idx, float* topk_w,
                                int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                                int bm, int32_t* tile_expert, int32_t* tile_row,
-                               int32_t* tile_info, int32_t* num_tiles, int* status, void* xp,
-                               cudaStream_t s);
+                               int32_t* tile_info, int32_t* num_tiles, int* status, int cap,
+                               int32_t* kept, void* xp, cudaStream_t s);
 
-cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* counts,
+// `kept` = pairs each expert accepted (its first kept[e] segment rows).
+cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* kept,
                                  const int32_t* offsets, const int32_t* perm, int k, int d, int f,
                                  int E, void* H, cudaStream_t s);
-cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, const int32_t* counts,
+cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, const int32_t* kept,
                                    const int32_t* offsets, int d, int f, int E, float* Y,
                                    cudaStream_t s);
 

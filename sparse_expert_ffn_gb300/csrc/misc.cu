@@ -25,7 +25,8 @@ __global__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restri
 // with `resid`, y[t, c] = resid[t, c] + that sum (one rounding at the end).
 // zskr.cn section 3.3 stage 5 (aggregation weighted by the expert scores).
 // When the down projection was split over K, Y holds `nsplit` partial slices
-// `split_stride` floats apart; they are added first, in slice order.
+// `split_stride` floats apart; they are added first, in slice order.  A pair
+// with inv < 0 was dropped by its expert's capacity and adds nothing.
 template <typename T>
 __global__ void combine_kernel(const float* __restrict__ Y, const float* __restrict__ topk_w,
                                const int32_t* __restrict__ inv, int k, int d, int nsplit,
@@ -36,8 +37,10 @@ __global__ void combine_kernel(const float* __restrict__ Y, const float* __restr
     if (c >= d) return;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
+        const int pos = inv[(size_t)t * k + j];
+        if (pos < 0) continue;                      // dropped by the expert's capacity
         const float w = topk_w[(size_t)t * k + j];
-        const float* row = Y + (size_t)inv[(size_t)t * k + j] * d + c;
+        const float* row = Y + (size_t)pos * d + c;
         float4 v = *reinterpret_cast<const float4*>(row);
         for (int sp = 1; sp < nsplit; ++sp) {
             const float4 p = *reinterpret_cast<const float4*>(row + sp * split_stride);

@@ -28,7 +28,8 @@ route_small_kernel(const T* __restrict__ x, const T* __restrict__ wr,
                    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int bm,
                    int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row,
                    int32_t* __restrict__ tile_info, int32_t* __restrict__ num_tiles,
-                   int* __restrict__ status, uint4* __restrict__ xp, int nq) {
+                   int* __restrict__ status, int cap, int32_t* __restrict__ kept,
+                   uint4* __restrict__ xp, int nq) {
     extern __shared__ int32_t sh[];
     float* logit = reinterpret_cast<float*>(sh);                 // [ntok][E]
     float* part = logit + ((ntok * E + 63) & ~63);               // [ntok * E][nq]
@@ -66,7 +67,7 @@ route_small_kernel(const T* __restrict__ x, const T* __restrict__ wr,
                           topk_w + (size_t)t * k);
     __syncthreads();
     dispatch_block(topk_idx, ntok * k, E, counts, offsets, perm, inv, bm, tile_expert, tile_row,
-                   tile_info, num_tiles, status, dsh);
+                   tile_info, num_tiles, status, cap, kept, dsh);
     if (xp) {
         __syncthreads();
         const int vecs = d * (int)sizeof(T) / 16;
@@ -100,8 +101,8 @@ cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const fl
                                int ntok, int d, int E, int k, int32_t* topk_idx, float* topk_w,
                                int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                                int bm, int32_t* tile_expert, int32_t* tile_row,
-                               int32_t* tile_info, int32_t* num_tiles, int* status, void* xp,
-                               cudaStream_t s) {
+                               int32_t* tile_info, int32_t* num_tiles, int* status, int cap,
+                               int32_t* kept, void* xp, cudaStream_t s) {
     const int nq = slices_for(ntok, E, d);
     const size_t smem = (size_t)((ntok * E + 63) & ~63) * 4 +
                         (size_t)((ntok * E * nq + 63) & ~63) * 4 + dispatch_smem_bytes(E);
@@ -111,14 +112,15 @@ cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const fl
         smem_attr((const void*)kern, (int)smem);
         kern<<<1, block, smem, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)wr, bias, ntok,
                                     d, E, k, topk_idx, topk_w, counts, offsets, perm, inv, bm,
-                                    tile_expert, tile_row, tile_info, num_tiles, status,
-                                    (uint4*)xp, nq);
+                                    tile_expert, tile_row, tile_info, num_tiles, status, cap,
+                                    kept, (uint4*)xp, nq);
     } else {
         auto kern = route_small_kernel<float>;
         smem_attr((const void*)kern, (int)smem);
         kern<<<1, block, smem, s>>>((const float*)x, (const float*)wr, bias, ntok, d, E, k,
                                     topk_idx, topk_w, counts, offsets, perm, inv, bm, tile_expert,
-                                    tile_row, tile_info, num_tiles, status, (uint4*)xp, nq);
+                                    tile_row, tile_info, num_tiles, status, cap, kept,
+                                    (uint4*)xp, nq);
     }
     return cudaGetLastError();
 }

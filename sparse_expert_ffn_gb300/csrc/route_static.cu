@@ -9,8 +9,8 @@
 // colibri_route_static runs the routing stage — router logits, top-k,
 // softmax over the k, and the dispatch permutation — on the caller's own
 // buffers, keeping its intermediate data (the repacked router weights, the
-// pair-to-position map, the per-expert offsets and the grouped-GEMM tile
-// list) in one file-scope device array of fixed size.
+// pair-to-position map, the per-expert offsets and kept counts, and the
+// grouped-GEMM tile list) in one file-scope device array of fixed size.
 //
 // The array is static device memory: every GPU that loads this library holds
 // it (kStaticScratchBytes, about 4.7 MiB) until the process exits.  All calls
@@ -21,6 +21,7 @@
 // in the same call.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <mutex>
 
 #include "colibri_moe.h"
@@ -44,7 +45,8 @@ constexpr size_t kOffTileExpert = kOffInv + round256((size_t)kStaticMaxPairs * 4
 constexpr size_t kOffTileRow = kOffTileExpert + round256((size_t)kStaticMaxTiles * 4);
 constexpr size_t kOffTileInfo = kOffTileRow + round256((size_t)kStaticMaxTiles * 4);
 constexpr size_t kOffNumTiles = kOffTileInfo + round256((size_t)kStaticMaxTiles * 4);
-constexpr size_t kOffStatus = kOffNumTiles + 256;
+constexpr size_t kOffKept = kOffNumTiles + 256;
+constexpr size_t kOffStatus = kOffKept + round256(256 * 4);
 constexpr size_t kStaticScratchBytes = kOffStatus + 256;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
@@ -112,6 +114,7 @@ extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_ro
     int32_t* tile_row = reinterpret_cast<int32_t*>(s + kOffTileRow);
     int32_t* tile_info = reinterpret_cast<int32_t*>(s + kOffTileInfo);
     int32_t* num_tiles = reinterpret_cast<int32_t*>(s + kOffNumTiles);
+    int32_t* kept = reinterpret_cast<int32_t*>(s + kOffKept);
     int* status = reinterpret_cast<int*>(s + kOffStatus);
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -126,6 +129,7 @@ extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_ro
         e = launch_router_simt(dt, x, wr_packed, router_bias, T, d, E, k, topk_idx, topk_w, cs);
     if (e == cudaSuccess)
         e = launch_dispatch(topk_idx, T * k, E, counts, offsets, perm, inv, kStaticTileRows,
-                            tile_expert, tile_row, tile_info, num_tiles, status, cs);
+                            tile_expert, tile_row, tile_info, num_tiles, status, INT_MAX, kept,
+                            cs);
     return e == cudaSuccess ? COLIBRI_OK : COLIBRI_ERR_CUDA;
 }

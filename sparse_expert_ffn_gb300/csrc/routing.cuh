@@ -86,9 +86,12 @@ __device__ __forceinline__ void warp_count_pass(const int32_t* __restrict__ topk
 }
 
 // Pass 2: the same walk; my[e] holds the warp's next position inside expert
-// e's segment.  perm[p] = r and inv[r] = p, in increasing r within a warp.
+// e's segment (which starts at seg_start[e]).  perm[p] = r, and inv[r] = p —
+// or -1 when p is the segment's cap-th pair or later (dropped by the expert's
+// capacity; cf-1.com sections 2.3 and 4.2: a hard per-expert token limit).
 __device__ __forceinline__ void warp_scatter_pass(const int32_t* __restrict__ topk_idx, int lo,
                                                   int hi, int E, int32_t* my,
+                                                  const int32_t* seg_start, int cap,
                                                   int32_t* __restrict__ perm,
                                                   int32_t* __restrict__ inv) {
     const int lane = threadIdx.x & 31;
@@ -104,15 +107,15 @@ __device__ __forceinline__ void warp_scatter_pass(const int32_t* __restrict__ to
         if (e >= 0) {
             const int p = start + __popc(m & lt_mask);
             perm[p] = r;
-            inv[r] = p;
+            inv[r] = p - seg_start[e] < cap ? p : -1;
             if (lane == __ffs(m) - 1) my[e] = start + __popc(m);
         }
         __syncwarp();
     }
 }
 
-// The grouped GEMM's tile list for expert e (count c, first pair eoff, first
-// tile tb): one entry per block of `bm` consecutive pairs, grouped into raster
+// The grouped GEMM's tile list for expert e (kept pairs c, first pair eoff,
+// first tile tb): one entry per block of `bm` consecutive pairs, grouped into raster
 // bands that never cross an expert boundary (at most kMaxBand tiles of one
 // expert per band), so the GEMM walks all of a band's m-tiles against one
 // weight block at a time and every weight block is streamed from HBM once.
@@ -132,7 +135,8 @@ __device__ __forceinline__ void write_tiles(int e, int c, int eoff, int tb, int 
 }
 
 // Dispatch of n = T*k pairs by one block of kDispatchWarps warps: counts[E],
-// offsets[E+1] (exclusive scan), perm[p] = r, inv[r] = p and the tile list.
+// offsets[E+1] (exclusive scan), perm[p] = r, inv[r] = p (-1 when dropped),
+// kept[E] = min(counts, cap) and the tile list over the kept pairs.
 // Warp w owns a contiguous range of r; after pass 1 the per-warp counts are
 // turned into each warp's base inside every expert segment (warps in order),
 // and pass 2 writes the positions.
@@ -142,7 +146,7 @@ __device__ __forceinline__ void dispatch_block(
     int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv, int bm,
     int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row,
     int32_t* __restrict__ tile_info, int32_t* __restrict__ num_tiles, int* __restrict__ status,
-    int32_t* sh) {
+    int cap, int32_t* __restrict__ kept, int32_t* sh) {
     int32_t* wcnt = sh;                           // [kDispatchWarps][E]
     int32_t* ecount = wcnt + kDispatchWarps * E;  // [E]
     int32_t* eoff = ecount + E;                   // [E + 1]
@@ -172,7 +176,7 @@ __device__ __forceinline__ void dispatch_block(
             eoff[e] = acc;
             tbase[e] = tacc;
             acc += ecount[e];
-            tacc += (ecount[e] + bm - 1) / bm;
+            tacc += (min(ecount[e], cap) + bm - 1) / bm;
         }
         eoff[E] = acc;
         tbase[E] = tacc;
@@ -188,13 +192,15 @@ __device__ __forceinline__ void dispatch_block(
             run += c;
         }
         counts[e] = ecount[e];
+        kept[e] = min(ecount[e], cap);
         offsets[e] = eoff[e];
-        write_tiles(e, ecount[e], eoff[e], tbase[e], bm, tile_expert, tile_row, tile_info);
+        write_tiles(e, min(ecount[e], cap), eoff[e], tbase[e], bm, tile_expert, tile_row,
+                    tile_info);
     }
     if (threadIdx.x == 0) offsets[E] = eoff[E];
     __syncthreads();
 
-    warp_scatter_pass(topk_idx, lo, hi, E, my, perm, inv);
+    warp_scatter_pass(topk_idx, lo, hi, E, my, eoff, cap, perm, inv);
 }
 
 }  // namespace colibri

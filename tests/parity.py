@@ -113,14 +113,23 @@ def check_routing(case: Case, x64, r, allow_near_ties: bool = True):
     return l, near
 
 
-def check_output(case: Case, x64, y, r, l, tokens=None):
-    """max|err|/max|ref| of y on `tokens` (all by default); returns the error."""
+def check_output(case: Case, x64, y, r, l, tokens=None, capacity=None):
+    """max|err|/max|ref| of y on `tokens` (all by default); returns the error.
+
+    With a capacity, the pairs kept are the oracle's capacity_keep of the
+    GPU's own topk_idx (an integer function of the routing, like dispatch)."""
     T = x64.shape[0]
     tok = np.arange(T) if tokens is None else np.asarray(tokens)
     gidx = r["topk_idx"][tok]
     g = oracle.softmax_selected(l[tok], gidx)
-    y_ref = oracle.token_outputs(x64[tok], gidx, g, case.experts)
+    keep = None
+    if capacity is not None:
+        keep = oracle.capacity_keep(r["topk_idx"], case.shape.n_experts, capacity)[tok]
+    y_ref = oracle.token_outputs(x64[tok], gidx, g, case.experts, keep_rows=keep)
     y_gpu = oracle.to_f64(y[torch.as_tensor(tok, device=y.device)].cpu())
+    if np.abs(y_ref).max() == 0.0:
+        assert np.all(y_gpu == 0.0), "every pair dropped: y must be exactly 0"
+        return 0.0
     err = np.abs(y_gpu - y_ref).max() / max(np.abs(y_ref).max(), 1e-30)
     tol = Y_RTOL[case.shape.dtype]
     assert err <= tol, f"max|err|/max|ref| = {err:.3e} > {tol}"

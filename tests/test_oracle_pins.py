@@ -330,3 +330,55 @@ def test_near_tie_flags_exact_ties_only_when_close():
     w2 = np.array([[1.0, 0.5, 0.0], [0.0, 0.0, 0.0]])
     assert oracle.near_tie_tokens(x, w, l, 1).tolist() == [True, True]
     assert oracle.near_tie_tokens(x, w2, x @ w2, 1).tolist() == [False, False]
+
+
+# ---------------------------------------------------------------- capacity (hard)
+
+
+@pytest.mark.parametrize("T,E,k,C", [(40, 8, 2, 3), (64, 4, 2, 20), (33, 16, 4, 1), (20, 8, 2, 0)])
+def test_capacity_keep_is_the_first_C_of_each_expert_segment(T, E, k, C):
+    rng = np.random.default_rng(T * C + E)
+    l = rng.standard_normal((T, E))
+    l[:, 0] += 2.0            # a hot expert that overflows
+    idx = oracle.topk_select(l, k)
+    keep = oracle.capacity_keep(idx, E, C)
+    # second route: the dispatch permutation's segments, first C entries
+    counts, offsets, perm, inv = oracle.dispatch(idx, E)
+    expect = np.zeros(T * k, dtype=bool)
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        expect[seg[:C]] = True
+    assert np.array_equal(keep.reshape(-1), expect)
+    kept_per_expert = np.bincount(idx.reshape(-1)[keep.reshape(-1)], minlength=E)
+    assert np.all(kept_per_expert == np.minimum(counts, C))
+
+
+def test_capacity_limits_are_monotone_and_reach_no_limit():
+    rng = np.random.default_rng(5)
+    idx = oracle.topk_select(rng.standard_normal((50, 6)), 2)
+    prev = oracle.capacity_keep(idx, 6, 0)
+    assert not prev.any()
+    for C in range(1, 60):
+        cur = oracle.capacity_keep(idx, 6, C)
+        assert np.all(prev <= cur)              # raising C never drops a kept pair
+        prev = cur
+    counts = np.bincount(idx.reshape(-1), minlength=6)
+    assert oracle.capacity_keep(idx, 6, int(counts.max())).all()
+    assert oracle.capacity_keep(idx, 6, None).all()
+
+
+def test_layer_under_capacity_drops_exactly_the_rejected_pairs():
+    p = _small_layer(E=4, T=12)
+    base = oracle.moe_layer(p["x"], p["w_router"], p["w_gate"], p["w_up"], p["w_down"], 2)
+    none = oracle.moe_layer(p["x"], p["w_router"], p["w_gate"], p["w_up"], p["w_down"], 2,
+                            capacity=int(base["counts"].max()))
+    assert np.array_equal(none["y"], base["y"])
+    zero = oracle.moe_layer(p["x"], p["w_router"], p["w_gate"], p["w_up"], p["w_down"], 2, capacity=0)
+    assert np.all(zero["y"] == 0.0)
+    cap = oracle.moe_layer(p["x"], p["w_router"], p["w_gate"], p["w_up"], p["w_down"], 2, capacity=3)
+    # token-wise: sum over the kept slots only, with the unchanged gates
+    g = np.where(cap["keep"], cap["topk_w"], 0.0)
+    y = oracle.token_outputs(p["x"], cap["topk_idx"], g,
+                             lambda e: (p["w_gate"][e], p["w_up"][e], p["w_down"][e]))
+    assert np.allclose(cap["y"], y, rtol=1e-13, atol=1e-14)
+    assert not np.allclose(cap["y"], base["y"])

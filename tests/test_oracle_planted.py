@@ -39,8 +39,8 @@ def _topk_ascending(l, k):                # the k smallest
     return om.__dict__["_orig_topk"](-l, k)
 
 
-def _combine_reversed(y_perm, g, inv):    # gates applied to the wrong slot
-    return om.__dict__["_orig_combine"](y_perm, g[:, ::-1].copy(), inv)
+def _combine_reversed(y_perm, g, inv, keep=None):    # gates applied to the wrong slot
+    return om.__dict__["_orig_combine"](y_perm, g[:, ::-1].copy(), inv, keep)
 
 
 def _dispatch_unstable(idx, E):           # pairs of one expert in decreasing r
@@ -56,6 +56,11 @@ def _dispatch_unstable(idx, E):           # pairs of one expert in decreasing r
 def _up_transposed(xs, wg, wu, wd, round_h=False):   # gate and up swapped
     h = om.silu(xs @ wu) * (xs @ wg)
     return h @ wd
+
+
+def _capacity_last_C(idx, E, capacity=None):   # keeps the last C pairs of an expert
+    keep = om.__dict__["_orig_capacity_keep"](idx[::-1], E, capacity)
+    return keep[::-1].copy()
 
 
 def _rmsnorm_no_mean(h, gamma, eps):      # sum instead of mean
@@ -77,12 +82,14 @@ CASES = [
     ("swiglu_expert", _up_transposed, [pins.test_one_expert_k1_equals_dense_swiglu,
                                        pins.test_hand_worked_example]),
     ("rmsnorm", _rmsnorm_no_mean, [pins.test_rmsnorm_closed_forms]),
+    ("capacity_keep", _capacity_last_C,
+     [lambda: pins.test_capacity_keep_is_the_first_C_of_each_expert_segment(40, 8, 2, 3)]),
 ]
 
 
 @pytest.mark.parametrize("name,bad,checks", CASES, ids=[f"{c[0]}-{c[1].__name__}" for c in CASES])
 def test_planted_mistake_is_caught(monkeypatch, name, bad, checks):
-    for orig in ("topk_select", "combine", "dispatch"):
+    for orig in ("topk_select", "combine", "dispatch", "capacity_keep"):
         monkeypatch.setitem(om.__dict__, "_orig_" + orig.replace("_select", ""), getattr(om, orig))
     monkeypatch.setattr(om, name, bad)
     monkeypatch.setattr(oracle, name, bad)
