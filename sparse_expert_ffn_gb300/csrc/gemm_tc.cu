@@ -59,6 +59,13 @@ template <bool kPair> struct Ring {
 };
 constexpr int kThreads = 192;
 constexpr uint32_t kRingBytes = 192 * 1024;   // shared-memory ring of every instantiation
+// Per epilogue warp, a 32-row tile of one 32-column accumulator chunk in
+// shared memory (rows padded to 36 floats): the warp turns its 32 per-thread
+// rows into 128-byte row segments for the global stores, and the router reads
+// its logits back with a rolled loop instead of a fully unrolled one.
+constexpr uint32_t kStagingOffset = kRingBytes + 512;   // after the ring and the barriers
+constexpr int kStgStride = 36;                           // floats per staged row
+constexpr uint32_t kStgWarpBytes = 32 * kStgStride * 4;  // 4608
 constexpr int kMaxRouterStages = 12;
 constexpr int kAccCols = 256;     // TMEM columns per accumulator
 constexpr int kTmemCols = 512;    // two accumulators
@@ -534,6 +541,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int my_row = (int)rank * kBM + row;          // row inside the tile
             const bool live = my_row < wk.rows;
             const size_t orow = (size_t)(wk.row0 + my_row);
+            float* stg = reinterpret_cast<float*>(smem + kStagingOffset) + (warp - 2) * 32 * kStgStride;
             if constexpr (kMode == kRouter) {
                 // Logits of this thread's token: the E accumulator columns
                 // (+ offset).  Top-k by insertion over a key that puts the
@@ -544,28 +552,30 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                 for (int j = 0; j < 8; ++j) key[j] = 0ull, val[j] = 0.f;
                 const int E = args.n_experts;
+                float* mine = stg + lane * 33;     // own row, stride 33: conflict-free
 #pragma unroll 1
                 for (int c = 0; c < bn; c += 32) {
                     uint32_t v[32];
                     tmem_ld32(tbase + c, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                    for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
+                    const int n = min(32, E - c);
+#pragma unroll 1
+                    for (int i = 0; i < n; ++i) {
                         const int e = c + i;
-                        if (e < E) {
-                            float l = __uint_as_float(v[i]);
-                            if (args.bias) l += args.bias[e];
-                            unsigned long long kk =
-                                ((unsigned long long)logit_order_key(l) << 32) | (uint32_t)(~(uint32_t)e);
-                            float vv = l;
+                        float l = mine[i];
+                        if (args.bias) l += args.bias[e];
+                        unsigned long long kk =
+                            ((unsigned long long)logit_order_key(l) << 32) | (uint32_t)(~(uint32_t)e);
+                        float vv = l;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                if (kk > key[j]) {
-                                    const unsigned long long tk = key[j];
-                                    const float tv = val[j];
-                                    key[j] = kk, val[j] = vv;
-                                    kk = tk, vv = tv;
-                                }
+                        for (int j = 0; j < 8; ++j) {
+                            if (kk > key[j]) {
+                                const unsigned long long tk = key[j];
+                                const float tv = val[j];
+                                key[j] = kk, val[j] = vv;
+                                kk = tk, vv = tv;
                             }
                         }
                     }
@@ -586,6 +596,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                 }
             } else if constexpr (kMode == kGateUp) {
+                // H = silu(G) * U for this thread's row, 32 columns per chunk,
+                // stored straight from registers: each row's 64 bytes are two
+                // whole sectors, so staging them buys nothing here.
                 __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
 #pragma unroll 1
                 for (int c = 0; c < 128 / 32; ++c) {
@@ -611,21 +624,32 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                 }
             } else {
+                // Y (float32) for this thread's row, 32 columns per chunk,
+                // staged and stored as 128-byte row segments, 4 rows per warp
+                // instruction.
                 float* Y = reinterpret_cast<float*>(args.out) + wk.split * args.out_split_stride;
+                const int row_base = (int)rank * kBM + q * 32;
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32(tbase + c * 32, v);
                     tmem_ld_wait();
-                    if (live) {
-                        float4* dst = reinterpret_cast<float4*>(Y + orow * args.out_ld +
-                                                                wk.nblk * kBN + c * 32);
+                    float4* mine = reinterpret_cast<float4*>(stg + lane * kStgStride);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                                 __uint_as_float(v[4 * i + 2]),
-                                                 __uint_as_float(v[4 * i + 3]));
+                    for (int i = 0; i < 8; ++i)
+                        mine[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                              __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                    __syncwarp();
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = it * 4 + (lane >> 3), c4 = lane & 7;
+                        if (row_base + rr < wk.rows) {
+                            const float4 val = reinterpret_cast<const float4*>(stg + rr * kStgStride)[c4];
+                            reinterpret_cast<float4*>(Y + (size_t)(wk.row0 + row_base + rr) * args.out_ld +
+                                                      wk.nblk * kBN + c * 32)[c4] = val;
+                        }
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -669,9 +693,8 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 size_t tc_gemm_smem_bytes() {
-    const size_t single = (size_t)Ring<false>::kStages * (kStageA + Ring<false>::kStageB);
-    const size_t pair = (size_t)Ring<true>::kStages * (kStageA + Ring<true>::kStageB);
-    return (single > pair ? single : pair) + 1024 + 256;
+    // ring + barriers (512 B) + 4 epilogue staging tiles + 1024-byte alignment slack
+    return (size_t)kStagingOffset + 4 * kStgWarpBytes + 1024;
 }
 int tc_gemm_block_m() { return kBM; }
 int tc_gemm_pair_rows() { return 2 * kBM; }
