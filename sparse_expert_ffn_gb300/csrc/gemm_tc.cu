@@ -315,7 +315,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 // ---------------------------------------------------------------- work decode
 
 struct Work {
-    int expert, row0, rows, nblk, split;
+    int expert, row0, rows, nblk, split, tile;
 };
 
 // Work w -> (m-tile, n-block).  Bands of m-tiles (one expert each, from the
@@ -341,6 +341,7 @@ __device__ __forceinline__ Work decode_work(int w, int n_blocks, int k_splits,
     r.rows = tile_info[m] & 0x3FF;
     r.nblk = nblk / k_splits;
     r.split = nblk - r.nblk * k_splits;
+    r.tile = m;
     return r;
 }
 
@@ -352,6 +353,7 @@ __device__ __forceinline__ Work dense_work(int w, int rows_total) {
     r.rows = min(kBM, rows_total - r.row0);
     r.nblk = 0;
     r.split = 0;
+    r.tile = w;
     return r;
 }
 
@@ -359,6 +361,43 @@ template <int kMode>
 __device__ __forceinline__ Work get_work(int w, const TcGemmArgs& a) {
     if constexpr (kMode == kRouter) return dense_work(w, a.dense_rows);
     else return decode_work(w, a.n_blocks, a.k_splits, a.tile_expert, a.tile_row, a.tile_info);
+}
+
+// Gate/up with K split into slices (single CTAs, few rows): every epilogue
+// warp of every slice counts itself in on the (m-tile, n-block) counter after
+// its partial rows are globally visible; the warp that arrives last adds the
+// slices in slice order (so the sum does not depend on arrival order), applies
+// SiLU(G)*U and writes the tile's H rows, then rearms the counter.  Nothing
+// waits on another CTA.
+__device__ __noinline__ void gate_up_split_fixup(const TcGemmArgs& args, const Work& wk, int lane) {
+    __threadfence();
+    __syncwarp();
+    int* ctr = args.tile_counter + (size_t)wk.tile * args.n_blocks + wk.nblk;
+    int old = 0;
+    if (lane == 0) old = atomicAdd(ctr, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != 4 * args.k_splits - 1) return;
+    __threadfence();
+    const int pld = args.n_blocks * 256;
+    __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
+    for (int r = 0; r < wk.rows; ++r) {
+        const size_t prow = (size_t)(wk.row0 + r) * pld + (size_t)wk.nblk * 256;
+        float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int sl = 0; sl < args.k_splits; ++sl) {
+            const float* ps = args.partial + sl * args.partial_split_stride + prow;
+            const float4 gs = __ldcg(reinterpret_cast<const float4*>(ps) + lane);
+            const float4 us = __ldcg(reinterpret_cast<const float4*>(ps + 128) + lane);
+            g[0] += gs.x, g[1] += gs.y, g[2] += gs.z, g[3] += gs.w;
+            u[0] += us.x, u[1] += us.y, u[2] += us.z, u[3] += us.w;
+        }
+        __nv_bfloat162 h01 = __floats2bfloat162_rn(silu(g[0]) * u[0], silu(g[1]) * u[1]);
+        __nv_bfloat162 h23 = __floats2bfloat162_rn(silu(g[2]) * u[2], silu(g[3]) * u[3]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&h01);
+        pk.y = *reinterpret_cast<uint32_t*>(&h23);
+        *reinterpret_cast<uint2*>(H + (size_t)(wk.row0 + r) * args.out_ld + wk.nblk * 128 + lane * 4) = pk;
+    }
+    if (lane == 0) *ctr = 0;   // rearmed for the next launch
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -596,6 +635,27 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                 }
             } else if constexpr (kMode == kGateUp) {
+              if (args.k_splits > 1) {
+                // One K slice: the float32 partial of this thread's G|U row
+                // (256 columns) goes to the slice's partial buffer; H is
+                // written after the accumulator is released (below).
+                float* P = args.partial + wk.split * args.partial_split_stride;
+                const int pld = args.n_blocks * 256;
+#pragma unroll 1
+                for (int c = 0; c < 256 / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    if (live) {
+                        float4* dst = reinterpret_cast<float4*>(P + orow * pld + wk.nblk * 256 + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                 __uint_as_float(v[4 * i + 2]),
+                                                 __uint_as_float(v[4 * i + 3]));
+                    }
+                }
+              } else {
                 // H = silu(G) * U for this thread's row, 32 columns per chunk,
                 // stored straight from registers: each row's 64 bytes are two
                 // whole sectors, so staging them buys nothing here.
@@ -623,6 +683,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         for (int i = 0; i < 4; ++i) dst[i] = pk[i];
                     }
                 }
+              }
             } else {
                 // Y (float32) for this thread's row, 32 columns per chunk,
                 // staged and stored as 128-byte row segments, 4 rows per warp
@@ -658,6 +719,9 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const uint32_t ae = acc_empty_leader0 + acc * 8;   // &acc_empty[acc] in the leader
                 if constexpr (kPair) mbar_arrive_cluster(ae);
                 else mbar_arrive(ae);
+            }
+            if constexpr (kMode == kGateUp) {
+                if (args.k_splits > 1) gate_up_split_fixup(args, wk, lane);
             }
             if (++acc == 2) acc = 0, acc_phase ^= 1;
         }
@@ -739,6 +803,9 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcG
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;
+    // the split gate/up fixup counts the four epilogue warps of one CTA per slice
+    if (mode == kGateUp && args.k_splits > 1 && (pair || !args.partial || !args.tile_counter))
+        return cudaErrorInvalidValue;
     cudaError_t e;
     if (mode == kGateUp)
         e = pair ? launch_one<kGateUp, true>(tmA, tmB, args, grid & ~1, s)

@@ -17,11 +17,17 @@ struct TcGemmArgs {
     int n_blocks;                // n-blocks per expert
     int k_blocks;                // K / 64
     int k_splits;                // K split into this many slices (1 = none); every slice
-                                 // non-empty; slice s writes out + s * out_split_stride
+                                 // non-empty; kDown: slice s writes out + s * out_split_stride
     int b_rows_per_expert;       // rows of the packed B operand per expert
     void* out;                   // H (bf16, kGateUp) or Y (float32, kDown)
     int out_ld;                  // row stride of `out` in elements
     size_t out_split_stride;     // elements between the outputs of two K slices
+    // kGateUp with k_splits > 1 (single CTAs only): float32 G|U partials
+    // [k_splits][pairs][2 f] and one arrival counter per (m-tile, n-block),
+    // zero between launches
+    float* partial;
+    size_t partial_split_stride; // elements between two slices' partials
+    int32_t* tile_counter;
     int* status;                 // device status word (DEV_TIMEOUT on a wait that gave up)
     uint64_t wait_limit_ns;      // bound of every mbarrier wait
     // router mode (kRouter): dense tiles over dense_rows tokens, MMA N = bn_rows

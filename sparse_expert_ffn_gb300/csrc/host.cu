@@ -58,6 +58,9 @@ struct colibri_moe {
     int32_t* tile_info = nullptr;
     int32_t* num_tiles = nullptr;
     int32_t* block_counts = nullptr;  // multi-CTA dispatch: per-CTA counts, then bases
+    int32_t* gu_counter = nullptr;    // split gate/up: arrivals per (m-tile, n-block), zero at rest
+    size_t gu_counter_bytes = 0;
+    size_t y_floats = 0;              // capacity of Y (also the split gate/up partials)
     int* status = nullptr;
     void* H = nullptr;      // [max_pairs, f]
     void* xp = nullptr;     // [max_pairs, d] token rows in expert order
@@ -117,7 +120,26 @@ constexpr int kSplitMaxPairs = 2048;
 constexpr int kMultiDispatchPairs = 12288;
 // Batches from this many tokens route on the tensor cores.
 constexpr int kTcRouterMinTokens = 512;
-constexpr int kMaxKSplit = 8;
+constexpr int kMaxKSplit = 16;
+// The gate/up GEMM splits K only for batches of at most this many pairs.
+constexpr int kGateUpSplitMaxPairs = 64;
+
+// K slices of a GEMM with `items` (m-tile, n-block) work items of kb K blocks
+// each, on `units` resident work units: the count (every slice non-empty)
+// that minimises the number of waves times the slice length, with two K
+// blocks of fixed cost per work item (pipeline fill and epilogue).
+int choose_k_splits(int64_t items, int kb, int units, int max_splits) {
+    int best = 1;
+    double best_cost = 0.0;
+    for (int ks = 1; ks <= std::max(1, std::min(max_splits, kb)); ++ks) {
+        const int per = (kb + ks - 1) / ks;
+        const int eff = (kb + per - 1) / per;
+        const int64_t waves = (items * eff + units - 1) / units;
+        const double cost = (double)waves * (per + 2);
+        if (ks == 1 || cost < best_cost) best = eff, best_cost = cost;
+    }
+    return best;
+}
 
 struct DeviceGuard {
     int prev = -1;
@@ -357,7 +379,12 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.status = h->status;
         a.wait_limit_ns = h->wait_limit_ns;
         a.stall_producer = h->stall_tma ? 1 : 0;
-        // gate/up: N = 2f in blocks of 256 rows (128 gate + 128 up), K = d
+        // Work items the GEMMs will see: with at most one tile per expert,
+        // an expert per distinct routed expert (exactly k for one token).
+        const int64_t tiles_est = npairs <= tile_rows ? std::min(E, npairs) : tiles_ub;
+        // gate/up: N = 2f in blocks of 256 rows (128 gate + 128 up), K = d.
+        // A decode-sized batch leaves a fraction of a wave in the last round
+        // of items: split K, the last slice to finish writes H.
         a.n_blocks = f / 128;
         a.k_blocks = d / 64;
         a.k_splits = 1;
@@ -365,9 +392,16 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.b_rows_per_expert = 2 * f;
         a.out = h->H;
         a.out_ld = f;
+        if (!pair && npairs <= kGateUpSplitMaxPairs) {
+            const int fit = (int)std::min<size_t>(kMaxKSplit, h->y_floats / ((size_t)npairs * 2 * f));
+            a.k_splits = choose_k_splits(tiles_est * a.n_blocks, a.k_blocks, units, fit);
+            a.partial = h->Y;
+            a.partial_split_stride = (size_t)npairs * 2 * f;
+            a.tile_counter = h->gu_counter;
+        }
         {
-            const int grid =
-                cta_per_unit * (int)std::min<int64_t>((int64_t)tiles_ub * a.n_blocks, units);
+            const int grid = cta_per_unit * (int)std::min<int64_t>(
+                                                    (int64_t)tiles_ub * a.n_blocks * a.k_splits, units);
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
             st = g.done(launch_tc_gemm(kGateUp, pair, h->tm_xp, pair ? h->tm_wgu : h->tm_wgu1, a,
                                        grid, s), 1);
@@ -382,12 +416,12 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.out = h->Y;
         a.out_ld = d;
         a.k_splits = 1;
+        a.partial = nullptr;
+        a.partial_split_stride = 0;
+        a.tile_counter = nullptr;
         if (npairs <= kSplitMaxPairs) {
-            const int64_t items = (int64_t)tiles_ub * a.n_blocks;
-            int ks = (int)std::min<int64_t>(kMaxKSplit, (2 * units + items - 1) / items);
-            ks = std::max(1, std::min(ks, a.k_blocks));
-            const int per = (a.k_blocks + ks - 1) / ks;
-            a.k_splits = (a.k_blocks + per - 1) / per;  // every slice non-empty
+            const int fit = (int)std::min<size_t>(kMaxKSplit, h->y_floats / ((size_t)npairs * d));
+            a.k_splits = choose_k_splits(tiles_est * a.n_blocks, a.k_blocks, units, fit);
         }
         a.out_split_stride = (size_t)npairs * d;
         {
@@ -518,6 +552,11 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     h->grouped_ok = grouped_shape_ok(*cfg);
     if (cfg->executor == COLIBRI_EXEC_GROUPED && !h->grouped_ok) return fail(COLIBRI_ERR_UNSUPPORTED);
     const size_t P = (size_t)h->max_pairs;
+    // Y: the down projection's float32 rows, or up to 8 K slices of them for
+    // batches of at most kSplitMaxPairs pairs; the split gate/up partials of
+    // small batches reuse it.
+    const size_t y_floats = std::max(P, (size_t)8 * std::min<size_t>(P, kSplitMaxPairs)) * d;
+    const size_t gu_counter_bytes = (size_t)h->max_tiles * (f / 128) * 4;
     size_t off = 0;
     auto carve = [&](size_t bytes) {
         const size_t o = off;
@@ -531,8 +570,7 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
                  o_tinfo = carve((size_t)h->max_tiles * 4), o_nt = carve(4), o_st = carve(4),
                  o_bc = carve((size_t)dispatch_blocks(h->max_pairs) * E * 4),
                  o_xp = h->grouped_ok ? carve(P * d * h->esz) : 0, o_h = carve(P * f * h->esz),
-                 o_y = carve(std::max(P, (size_t)kMaxKSplit * std::min<size_t>(P, kSplitMaxPairs)) *
-                             d * 4),
+                 o_y = carve(y_floats * 4), o_guc = carve(gu_counter_bytes),
                  o_u = carve((size_t)M * d * h->esz),
                  o_xs = carve((size_t)M * d * h->esz), o_ys = carve((size_t)M * d * h->esz);
     h->ws_bytes = off;
@@ -554,6 +592,9 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     h->xp = h->grouped_ok ? (void*)(b + o_xp) : nullptr;
     h->H = b + o_h;
     h->Y = (float*)(b + o_y);
+    h->y_floats = y_floats;
+    h->gu_counter = (int32_t*)(b + o_guc);
+    h->gu_counter_bytes = gu_counter_bytes;
     h->u = b + o_u;
     h->x_stage = b + o_xs;
     h->y_stage = b + o_ys;
@@ -676,6 +717,8 @@ colibri_status_t colibri_check(colibri_moe_t* h, void* stream) {
     if (e != cudaSuccess) return COLIBRI_ERR_CUDA;
     if (dev_status != DEV_OK) {
         cudaMemset(h->status, 0, sizeof(int));
+        // a launch that gave up may have left split gate/up counters armed
+        cudaMemset(h->gu_counter, 0, h->gu_counter_bytes);
         if (st == COLIBRI_OK) st = dev_status == DEV_TIMEOUT ? COLIBRI_ERR_TIMEOUT : COLIBRI_ERR_CUDA;
     }
     return st;

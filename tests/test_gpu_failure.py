@@ -53,9 +53,10 @@ def test_injected_allocation_failure_rolls_back(lib, monkeypatch):
     layer.close()
 
 
-# 256 tokens run the expert GEMMs on single CTAs, 1024 on CTA pairs
-# (at least 128 (token, slot) pairs per expert on average).
-@pytest.mark.parametrize("T", [256, 1024], ids=["single_cta", "cta_pairs"])
+# 2 tokens split the gate/up GEMM over K (last-slice fixup), 256 tokens run
+# the expert GEMMs on single CTAs, 1024 on CTA pairs (at least 128
+# (token, slot) pairs per expert on average).
+@pytest.mark.parametrize("T", [2, 256, 1024], ids=["split_k", "single_cta", "cta_pairs"])
 def test_bounded_wait_times_out_and_context_survives(lib, monkeypatch, T):
     sef = lib
     dev = torch.device("cuda", 0)
