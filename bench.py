@@ -312,10 +312,16 @@ def run_ours(args):
     torch.cuda.synchronize()
     if clocks:
         clocks.mark("timed_start")
-    ms, launches, stages = time_steps(layer, x, y, args.steps, args.warmup, world, stream, profile=True)
+    ms, launches, _ = time_steps(layer, x, y, args.steps, args.warmup, world, stream)
     if clocks:
         clocks.mark("timed_end")
     ms = max_over_ranks(ms, world)
+    # Per-stage kernel times: the same K steps again with an event pair around
+    # every launch (the events also stop consecutive kernels from overlapping
+    # their launch, so this pass runs a little slower than the headline one).
+    time.sleep(1.0)   # same power state as the headline pass
+    ms_prof, _, stages = time_steps(layer, x, y, args.steps, 1, world, stream, profile=True)
+    ms_prof = max_over_ranks(ms_prof, world)
     r = layer.routing()
     counts = r["counts"].cpu().numpy()
     alg = algorithmic(shape, T, counts)
@@ -374,7 +380,8 @@ def run_ours(args):
             layer.set_executor(ex)
             xs = synth.tokens(shape, Ts, seed, 0, dev)
             ys = torch.empty_like(xs)
-            ms_s, _, st_s = time_steps(layer, xs, ys, args.steps, args.warmup, world, stream, profile=True)
+            ms_s, _, _ = time_steps(layer, xs, ys, args.steps, args.warmup, world, stream)
+            _, _, st_s = time_steps(layer, xs, ys, args.steps, 1, world, stream, profile=True)
             layer.set_executor("auto")
             ms_s = max_over_ranks(ms_s, world)
             cs = layer.routing()["counts"].cpu().numpy()
@@ -406,6 +413,7 @@ def run_ours(args):
         "roofline": roof,
         "layer_roofline": whole,
         "stages_us_per_step": {k: round(v["ms_total"] * 1e3 / args.steps, 1) for k, v in stages.items()},
+        "ms_per_step_profiled": round(ms_prof / args.steps, 4),
         "active_experts": alg["active_experts"],
         "gpu_launches": int(launches),
         "e2e": e2e,
@@ -457,21 +465,27 @@ def run_stack(args):
         h.copy_(h0)
         step()
     torch.cuda.synchronize()
-    for layer in layers:
-        lib.colibri_profile_enable(layer.handle, 1)
-    n0 = sum(l.launch_count for l in layers)
     stream = torch.cuda.current_stream()
-    barrier(world)
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    ms = max_over_ranks(a.elapsed_time(b), world)
-    launches = sum(l.launch_count for l in layers) - n0
+
+    def timed(profile):
+        for layer in layers:
+            lib.colibri_profile_enable(layer.handle, 1 if profile else 0)
+        n0 = sum(l.launch_count for l in layers)
+        barrier(world)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(a.elapsed_time(b), world), sum(l.launch_count for l in layers) - n0
+
+    ms, launches = timed(False)
+    # per-stage kernel times from a second pass with an event pair per launch
+    time.sleep(1.0)
+    ms_prof, _ = timed(True)
     stages = {}
     active = 0
     for layer in layers:
@@ -503,6 +517,7 @@ def run_stack(args):
                            "frac": round(step_bytes / step_s / 1e9 / pk["hbm_gbs"], 4),
                            "active_experts_per_step": active},
         "stages_us_per_step": {k: round(v["ms_total"] * 1e3 / args.steps, 1) for k, v in stages.items()},
+        "ms_per_step_profiled": round(ms_prof / args.steps, 4),
         "gpu_launches": int(launches),
     }
     if rank == 0:

@@ -91,6 +91,85 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Coherent 8-element load (through L2): for rows this kernel wrote itself.
+__device__ __forceinline__ void load8_cg(const __nv_bfloat16* p, float (&v)[8]) {
+    uint4 u = __ldcg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __bfloat1622float2(b[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void load8_cg(const float* p, float (&v)[8]) {
+    float4 a = __ldcg(reinterpret_cast<const float4*>(p));
+    float4 b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// RMSNorm of one row by one warp (Zhang & Sennrich, 2019):
+// u = h / sqrt(mean(h^2) + eps) * gamma in float32.  Lane l adds the squares
+// of elements 8l + 256j .. 8l + 256j + 7 in order, then the butterfly sum;
+// every kernel that normalises a row uses this routine, so the result does
+// not depend on which one ran.  d is a multiple of 8.
+template <typename T>
+__device__ __forceinline__ void rmsnorm_row_warp(const T* __restrict__ hr, const T* __restrict__ gamma,
+                                                 int d, float eps, T* __restrict__ ur, int lane) {
+    float ss = 0.f;
+    for (int i = lane * 8; i < d; i += 256) {
+        float v[8];
+        load8(hr + i, v);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) ss = fmaf(v[c], v[c], ss);
+    }
+    ss = warp_sum(ss);
+    const float inv_rms = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int i = lane * 8; i < d; i += 256) {
+        float v[8], g[8];
+        load8(hr + i, v);
+        load8(gamma + i, g);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) ur[i + c] = from_f32<T>(v[c] * inv_rms * g[c]);
+    }
+}
+
+// Programmatic dependent launch.  Every kernel of the layer is launched with
+// programmatic stream serialization, so it may be scheduled while the kernel
+// before it on the stream is still running: it sets up what touches no global
+// memory (shared memory, barriers, tensor memory), then pdl_wait() blocks
+// until the previous kernel has completed and its writes are visible, and only
+// then does it read or write global memory.  pdl_launch_dependents() is called
+// after pdl_wait(), so at most one further kernel is scheduled early.  Both
+// are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_launch_dependents();
+}
+
+// Launch with programmatic stream serialization (see pdl_wait); the kernel
+// must call pdl_wait() before its first global memory access.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Device status word values (written by kernels, read by colibri_check).
 enum : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
 

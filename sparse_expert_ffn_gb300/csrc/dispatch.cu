@@ -20,6 +20,7 @@ dispatch_kernel(const int32_t* __restrict__ topk_idx, int n, int E, int32_t* __r
                 int32_t* __restrict__ tile_row, int32_t* __restrict__ tile_info,
                 int32_t* __restrict__ num_tiles, int* __restrict__ status, int cap,
                 int32_t* __restrict__ kept) {
+    pdl_enter();
     extern __shared__ int32_t sh[];
     dispatch_block(topk_idx, n, E, counts, offsets, perm, inv, bm, tile_expert, tile_row,
                    tile_info, num_tiles, status, cap, kept, sh);
@@ -33,6 +34,7 @@ dispatch_kernel(const int32_t* __restrict__ topk_idx, int n, int E, int32_t* __r
 __global__ void __launch_bounds__(kDispatchWarps * 32)
 dispatch_count_kernel(const int32_t* __restrict__ topk_idx, int n, int E,
                       int32_t* __restrict__ block_counts, int* __restrict__ status) {
+    pdl_enter();
     extern __shared__ int32_t wcnt[];  // [kDispatchWarps][E]
     const int warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) wcnt[i] = 0;
@@ -56,6 +58,7 @@ dispatch_scan_kernel(int32_t* __restrict__ block_counts, int nb, int E,
                      int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row,
                      int32_t* __restrict__ tile_info, int32_t* __restrict__ num_tiles, int cap,
                      int32_t* __restrict__ kept) {
+    pdl_enter();
     __shared__ int32_t ecount[256], eoff[257], tbase[257];
     const int e = threadIdx.x;
     if (e < E) {
@@ -99,6 +102,7 @@ dispatch_scatter_kernel(const int32_t* __restrict__ topk_idx, int n, int E,
                         const int32_t* __restrict__ offsets, int cap,
                         int32_t* __restrict__ perm, int32_t* __restrict__ inv,
                         int* __restrict__ status) {
+    pdl_enter();
     extern __shared__ int32_t wcnt[];  // [kDispatchWarps][E]
     const int warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) wcnt[i] = 0;
@@ -133,14 +137,16 @@ cudaError_t launch_dispatch_multi(const int32_t* topk_idx, int n, int E, int32_t
                                   int cap, int32_t* kept, cudaStream_t s) {
     const int nb = dispatch_blocks(n);
     const size_t smem = (size_t)kDispatchWarps * E * sizeof(int32_t);
-    dispatch_count_kernel<<<nb, kDispatchWarps * 32, smem, s>>>(topk_idx, n, E, block_counts,
-                                                                status);
-    dispatch_scan_kernel<<<1, kDispatchWarps * 32, 0, s>>>(block_counts, nb, E, counts, offsets,
-                                                           bm, tile_expert, tile_row, tile_info,
-                                                           num_tiles, cap, kept);
-    dispatch_scatter_kernel<<<nb, kDispatchWarps * 32, smem, s>>>(
-        topk_idx, n, E, block_counts, offsets, cap, perm, inv, status);
-    return cudaGetLastError();
+    const dim3 block(kDispatchWarps * 32);
+    cudaError_t e = launch_pdl(dispatch_count_kernel, nb, block, smem, s, topk_idx, n, E,
+                               block_counts, status);
+    if (e == cudaSuccess)
+        e = launch_pdl(dispatch_scan_kernel, 1, block, 0, s, block_counts, nb, E, counts, offsets,
+                       bm, tile_expert, tile_row, tile_info, num_tiles, cap, kept);
+    if (e == cudaSuccess)
+        e = launch_pdl(dispatch_scatter_kernel, nb, block, smem, s, topk_idx, n, E, block_counts,
+                       offsets, cap, perm, inv, status);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_dispatch(const int32_t* topk_idx, int n, int E, int32_t* counts,
@@ -150,11 +156,10 @@ cudaError_t launch_dispatch(const int32_t* topk_idx, int n, int E, int32_t* coun
                             cudaStream_t s) {
     const size_t smem = dispatch_smem(E);
     smem_attr((const void*)dispatch_kernel, (int)smem);
-    dispatch_kernel<<<1, kDispatchWarps * 32, smem, s>>>(topk_idx, n, E, counts, offsets, perm,
-                                                         inv, bm, tile_expert, tile_row,
-                                                         tile_info, num_tiles, status, cap,
-                                                         kept);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(dispatch_kernel, 1, kDispatchWarps * 32, smem, s, topk_idx, n,
+                                     E, counts, offsets, perm, inv, bm, tile_expert, tile_row,
+                                     tile_info, num_tiles, status, cap, kept);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace colibri

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 ffn_up_stream(const T* __restrict__ x, const T* __restrict__ wgu,
               const int32_t* __restrict__ kept, const int32_t* __restrict__ offsets,
               const int32_t* __restrict__ perm, int k, int d, int f, int E, T* __restrict__ H) {
+    pdl_enter();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = blockIdx.x * kWarps + warp;
     if (n >= f) return;
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 ffn_down_stream(const T* __restrict__ H, const T* __restrict__ wdT,
                 const int32_t* __restrict__ kept, const int32_t* __restrict__ offsets, int d,
                 int f, int E, float* __restrict__ Y) {
+    pdl_enter();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col = blockIdx.x * kWarps + warp;
     if (col >= d) return;
@@ -151,27 +153,29 @@ cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const
                                  const int32_t* offsets, const int32_t* perm, int k, int d, int f,
                                  int E, void* H, cudaStream_t s) {
     const dim3 block(kWarps * 32), grid((f + kWarps - 1) / kWarps);
+    cudaError_t e;
     if (dt == DType::BF16)
-        ffn_up_stream<__nv_bfloat16><<<grid, block, 0, s>>>(
-            (const __nv_bfloat16*)x, (const __nv_bfloat16*)wgu, kept, offsets, perm, k, d, f,
-            E, (__nv_bfloat16*)H);
+        e = launch_pdl(ffn_up_stream<__nv_bfloat16>, grid, block, 0, s, (const __nv_bfloat16*)x,
+                       (const __nv_bfloat16*)wgu, kept, offsets, perm, k, d, f, E,
+                       (__nv_bfloat16*)H);
     else
-        ffn_up_stream<float><<<grid, block, 0, s>>>((const float*)x, (const float*)wgu, kept,
-                                                    offsets, perm, k, d, f, E, (float*)H);
-    return cudaGetLastError();
+        e = launch_pdl(ffn_up_stream<float>, grid, block, 0, s, (const float*)x, (const float*)wgu,
+                       kept, offsets, perm, k, d, f, E, (float*)H);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, const int32_t* kept,
                                    const int32_t* offsets, int d, int f, int E, float* Y,
                                    cudaStream_t s) {
     const dim3 block(kWarps * 32), grid((d + kWarps - 1) / kWarps);
+    cudaError_t e;
     if (dt == DType::BF16)
-        ffn_down_stream<__nv_bfloat16><<<grid, block, 0, s>>>(
-            (const __nv_bfloat16*)H, (const __nv_bfloat16*)wdT, kept, offsets, d, f, E, Y);
+        e = launch_pdl(ffn_down_stream<__nv_bfloat16>, grid, block, 0, s, (const __nv_bfloat16*)H,
+                       (const __nv_bfloat16*)wdT, kept, offsets, d, f, E, Y);
     else
-        ffn_down_stream<float><<<grid, block, 0, s>>>((const float*)H, (const float*)wdT, kept,
-                                                      offsets, d, f, E, Y);
-    return cudaGetLastError();
+        e = launch_pdl(ffn_down_stream<float>, grid, block, 0, s, (const float*)H,
+                       (const float*)wdT, kept, offsets, d, f, E, Y);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace colibri

@@ -437,9 +437,6 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int n_units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
-    const int num_tiles =
-        kMode == kRouter ? (args.dense_rows + kBM - 1) / kBM : *args.num_tiles;
-    const int total = num_tiles * args.n_blocks * args.k_splits;
     // Rows of B this CTA loads per stage (= MMA N, or half of it for a pair).
     const int bn = kMode == kRouter ? args.bn_rows : kBN;
     const int b_rows_cta = kPair ? bn / 2 : bn;
@@ -468,6 +465,12 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if constexpr (kPair) cluster_sync();   // the peer's barriers exist before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above touched only this CTA's shared and tensor memory; the
+    // tile list and the operands come from the kernels before this one.
+    pdl_enter();
+    const int num_tiles =
+        kMode == kRouter ? (args.dense_rows + kBM - 1) / kBM : *args.num_tiles;
+    const int total = num_tiles * args.n_blocks * args.k_splits;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -790,13 +793,15 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcG
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kPair ? 2 : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k, tmA, tmB, args);
 }
 

@@ -272,9 +272,11 @@ struct Stage {
     }
 };
 
-// The layer on device buffers; `resid` (may equal y) adds a residual.
+// The layer on device buffers; `resid` (may equal y) adds a residual.  With
+// `gamma` the layer input is u = RMSNorm(x) * gamma (written to h->u): fused
+// into the small-batch routing kernel when that runs, else its own launch.
 colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, const void* resid,
-                           cudaStream_t s) {
+                           cudaStream_t s, const void* gamma = nullptr, float eps = 0.f) {
     const auto& c = h->cfg;
     const int E = c.n_experts, k = c.top_k, d = c.d_model, f = c.d_ff;
     const int npairs = T * k;
@@ -288,14 +290,22 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     // Small batch: router, top-k, softmax, dispatch and gather in one CTA.
     const bool fused_routing = route_small_fits(T, d, E, k);
     const int cap = h->capacity < 0 ? INT_MAX : h->capacity;
+    if (gamma && !fused_routing) {
+        Stage g(h, COLIBRI_STAGE_RMSNORM, s);
+        st = g.done(launch_rmsnorm(h->dt, x, gamma, T, d, eps, h->u, s), 1);
+        if (st != COLIBRI_OK) return st;
+        x = h->u;
+    }
     if (fused_routing) {
         Stage g(h, COLIBRI_STAGE_ROUTER, s);
         st = g.done(launch_route_small(h->dt, x, h->wr, h->bias, T, d, E, k, h->topk_idx,
                                        h->topk_w, h->counts, h->offsets, h->perm, h->inv,
                                        tile_rows, h->tile_expert, h->tile_row, h->tile_info,
                                        h->num_tiles, h->status, cap, h->kept,
-                                       ex == COLIBRI_EXEC_GROUPED ? h->xp : nullptr, s), 1);
+                                       ex == COLIBRI_EXEC_GROUPED ? h->xp : nullptr, gamma, eps,
+                                       h->u, s), 1);
         if (st != COLIBRI_OK) return st;
+        if (gamma) x = h->u;
     } else if (h->grouped_ok && T >= kTcRouterMinTokens) {
         // Large batch: the router logits are a [T, d] x [d, E] GEMM on the
         // tensor cores, top-k and softmax in its epilogue.
@@ -553,9 +563,12 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     if (cfg->executor == COLIBRI_EXEC_GROUPED && !h->grouped_ok) return fail(COLIBRI_ERR_UNSUPPORTED);
     const size_t P = (size_t)h->max_pairs;
     // Y: the down projection's float32 rows, or up to 8 K slices of them for
-    // batches of at most kSplitMaxPairs pairs; the split gate/up partials of
-    // small batches reuse it.
-    const size_t y_floats = std::max(P, (size_t)8 * std::min<size_t>(P, kSplitMaxPairs)) * d;
+    // batches of at most kSplitMaxPairs pairs (kMaxKSplit for decode-sized
+    // ones); the split gate/up partials of decode-sized batches reuse it.
+    const size_t dec = std::min<size_t>(P, kGateUpSplitMaxPairs);
+    const size_t y_floats =
+        std::max({P * d, (size_t)8 * std::min<size_t>(P, kSplitMaxPairs) * d,
+                  (size_t)kMaxKSplit * dec * std::max<size_t>(d, (size_t)2 * f)});
     const size_t gu_counter_bytes = (size_t)h->max_tiles * (f / 128) * 4;
     size_t off = 0;
     auto carve = [&](size_t bytes) {
@@ -658,14 +671,10 @@ colibri_status_t colibri_rmsnorm_moe_residual(colibri_moe_t* h, void* hidden, in
     if (T == 0) return COLIBRI_OK;
     DeviceGuard g(h->cfg.device);
     if (!g.ok) return COLIBRI_ERR_CUDA;
-    cudaStream_t s = (cudaStream_t)stream;
-    {
-        Stage g(h, COLIBRI_STAGE_RMSNORM, s);
-        const colibri_status_t st =
-            g.done(launch_rmsnorm(h->dt, hidden, gamma, T, h->cfg.d_model, eps, h->u, s), 1);
-        if (st != COLIBRI_OK) return st;
-    }
-    return run_layer(h, h->u, T, hidden, hidden, s);
+    const colibri_status_t st =
+        run_layer(h, hidden, T, hidden, hidden, (cudaStream_t)stream, gamma, eps);
+    if (st != COLIBRI_OK && h->sticky == COLIBRI_OK) h->sticky = st;
+    return st;
 }
 
 colibri_status_t colibri_get_routing(colibri_moe_t* h, int32_t* topk_idx, float* topk_w,

@@ -42,7 +42,8 @@ cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const fl
                                int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                                int bm, int32_t* tile_expert, int32_t* tile_row,
                                int32_t* tile_info, int32_t* num_tiles, int* status, int cap,
-                               int32_t* kept, void* xp, cudaStream_t s);
+                               int32_t* kept, void* xp, const void* gamma, float eps, void* u,
+                               cudaStream_t s);
 
 // `kept` = pairs each expert accepted (its first kept[e] segment rows).
 cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* kept,

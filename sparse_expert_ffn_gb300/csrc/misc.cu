@@ -14,6 +14,7 @@ namespace {
 // vectors.
 __global__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k,
                             int row_vecs, uint4* __restrict__ xp) {
+    pdl_enter();
     const int p = blockIdx.x;
     const int t = perm[p] / k;
     const uint4* src = x + (size_t)t * row_vecs;
@@ -32,6 +33,7 @@ __global__ void combine_kernel(const float* __restrict__ Y, const float* __restr
                                const int32_t* __restrict__ inv, int k, int d, int nsplit,
                                size_t split_stride,
                                const T* resid, T* y) {  // resid may alias y (in-place residual)
+    pdl_enter();
     const int t = blockIdx.y;
     const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (c >= d) return;
@@ -68,30 +70,14 @@ __global__ void combine_kernel(const float* __restrict__ Y, const float* __restr
 }
 
 // RMSNorm: u = h / sqrt(mean(h^2) + eps) * gamma, float32 arithmetic, one
-// CTA per token (Zhang & Sennrich, 2019).
+// warp per token (rmsnorm_row_warp), 8 tokens per CTA.
 template <typename T>
-__global__ void rmsnorm_kernel(const T* __restrict__ h, const T* __restrict__ gamma, int d,
-                               float eps, T* __restrict__ u) {
-    __shared__ float red[32];
-    const int t = blockIdx.x;
-    const T* hr = h + (size_t)t * d;
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) {
-        const float v = to_f32(hr[i]);
-        ss = fmaf(v, v, ss);
-    }
-    ss = warp_sum(ss);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-        v = warp_sum(v);
-        if (threadIdx.x == 0) red[0] = v;
-    }
-    __syncthreads();
-    const float inv_rms = 1.0f / sqrtf(red[0] / (float)d + eps);
-    for (int i = threadIdx.x; i < d; i += blockDim.x)
-        u[(size_t)t * d + i] = from_f32<T>(to_f32(hr[i]) * inv_rms * to_f32(gamma[i]));
+__global__ void rmsnorm_kernel(const T* __restrict__ h, const T* __restrict__ gamma, int T_,
+                               int d, float eps, T* __restrict__ u) {
+    pdl_enter();
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= T_) return;
+    rmsnorm_row_warp(h + (size_t)t * d, gamma, d, eps, u + (size_t)t * d, threadIdx.x & 31);
 }
 
 // Batched transpose with a row remap, for the init-time weight repack:
@@ -126,8 +112,9 @@ cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, in
                           int npairs, void* xp, cudaStream_t s) {
     if (npairs <= 0) return cudaSuccess;
     const int row_vecs = d * elem_bytes / 16;
-    gather_rows<<<npairs, 128, 0, s>>>((const uint4*)x, perm, k, row_vecs, (uint4*)xp);
-    return cudaGetLastError();
+    const cudaError_t e =
+        launch_pdl(gather_rows, npairs, 128, 0, s, (const uint4*)x, perm, k, row_vecs, (uint4*)xp);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t smem_attr(const void* kernel, int bytes) {
@@ -152,27 +139,28 @@ cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const 
                            const void* resid, void* y, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const dim3 block(128), grid((d / 4 + 127) / 128, T);
+    cudaError_t e;
     if (dt == DType::BF16)
-        combine_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
-            Y, topk_w, inv, k, d, nsplit, split_stride, (const __nv_bfloat16*)resid,
-            (__nv_bfloat16*)y);
+        e = launch_pdl(combine_kernel<__nv_bfloat16>, grid, block, 0, s, Y, topk_w, inv, k, d,
+                       nsplit, split_stride, (const __nv_bfloat16*)resid, (__nv_bfloat16*)y);
     else
-        combine_kernel<float><<<grid, block, 0, s>>>(Y, topk_w, inv, k, d, nsplit, split_stride,
-                                                      (const float*)resid, (float*)y);
-    return cudaGetLastError();
+        e = launch_pdl(combine_kernel<float>, grid, block, 0, s, Y, topk_w, inv, k, d, nsplit,
+                       split_stride, (const float*)resid, (float*)y);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm(DType dt, const void* h, const void* gamma, int T, int d, float eps,
                            void* u, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
+    const int grid = (T + 7) / 8;
+    cudaError_t e;
     if (dt == DType::BF16)
-        rmsnorm_kernel<__nv_bfloat16><<<T, 256, 0, s>>>((const __nv_bfloat16*)h,
-                                                        (const __nv_bfloat16*)gamma, d, eps,
-                                                        (__nv_bfloat16*)u);
+        e = launch_pdl(rmsnorm_kernel<__nv_bfloat16>, grid, 256, 0, s, (const __nv_bfloat16*)h,
+                       (const __nv_bfloat16*)gamma, T, d, eps, (__nv_bfloat16*)u);
     else
-        rmsnorm_kernel<float><<<T, 256, 0, s>>>((const float*)h, (const float*)gamma, d, eps,
-                                                (float*)u);
-    return cudaGetLastError();
+        e = launch_pdl(rmsnorm_kernel<float>, grid, 256, 0, s, (const float*)h, (const float*)gamma,
+                       T, d, eps, (float*)u);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_transpose_remap(int elem_bytes, const void* in, void* out, int batch, int R,

@@ -11,6 +11,8 @@
 //   2. top-k + softmax: warp w routes tokens w, w + 32, ...
 //   3. dispatch_block: the same deterministic counting sort as the dispatch kernel
 //   4. gather: Xp[p] = x[perm[p] / k] with 16-byte vectors.
+// For a pre-norm layer it first normalises the token rows (RMSNorm * gamma)
+// into u and routes u.
 #include "common.cuh"
 #include "kernels.h"
 #include "routing.cuh"
@@ -29,12 +31,24 @@ route_small_kernel(const T* __restrict__ x, const T* __restrict__ wr,
                    int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row,
                    int32_t* __restrict__ tile_info, int32_t* __restrict__ num_tiles,
                    int* __restrict__ status, int cap, int32_t* __restrict__ kept,
-                   uint4* __restrict__ xp, int nq) {
+                   uint4* __restrict__ xp, int nq, const T* __restrict__ gamma, float eps,
+                   T* __restrict__ u) {
+    pdl_enter();
     extern __shared__ int32_t sh[];
     float* logit = reinterpret_cast<float*>(sh);                 // [ntok][E]
     float* part = logit + ((ntok * E + 63) & ~63);               // [ntok * E][nq]
     int32_t* dsh = reinterpret_cast<int32_t*>(part + ((ntok * E * nq + 63) & ~63));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // 0. (pre-norm layer) u = RMSNorm(x) * gamma, one warp per token; the
+    // rest of the kernel routes and gathers u, read back through L2.
+    const T* src = x;
+    if (gamma) {
+        for (int t = warp; t < ntok; t += kDispatchWarps)
+            rmsnorm_row_warp(x + (size_t)t * d, gamma, d, eps, u + (size_t)t * d, lane);
+        __syncthreads();
+        src = u;
+    }
 
     // Logit p over d slice q (the d range is cut into nq slices so that the
     // 32 warps stay busy when T x E is small); slices are added in order.
@@ -42,12 +56,12 @@ route_small_kernel(const T* __restrict__ x, const T* __restrict__ wr,
     for (int u = warp; u < ntok * E * nq; u += kDispatchWarps) {
         const int p = u / nq, q = u - p * nq;
         const int t = p / E, e = p - t * E;
-        const T* xr = x + (size_t)t * d + q * seg;
+        const T* xr = src + (size_t)t * d + q * seg;
         const T* w = wr + (size_t)e * d + q * seg;
         float s = 0.f;
         for (int i = lane * 8; i < seg; i += 256) {
             float xv[8], wv[8];
-            load8(xr + i, xv);
+            load8_cg(xr + i, xv);
             load8(w + i, wv);
 #pragma unroll
             for (int c = 0; c < 8; ++c) s = fmaf(xv[c], wv[c], s);
@@ -71,10 +85,10 @@ route_small_kernel(const T* __restrict__ x, const T* __restrict__ wr,
     if (xp) {
         __syncthreads();
         const int vecs = d * (int)sizeof(T) / 16;
-        const uint4* xs = reinterpret_cast<const uint4*>(x);
+        const uint4* xs = reinterpret_cast<const uint4*>(src);
         for (int i = threadIdx.x; i < ntok * k * vecs; i += blockDim.x) {
             const int p = i / vecs, v = i - p * vecs;
-            xp[(size_t)p * vecs + v] = xs[(size_t)(perm[p] / k) * vecs + v];
+            xp[(size_t)p * vecs + v] = __ldcg(xs + (size_t)(perm[p] / k) * vecs + v);
         }
     }
 }
@@ -102,27 +116,29 @@ cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const fl
                                int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                                int bm, int32_t* tile_expert, int32_t* tile_row,
                                int32_t* tile_info, int32_t* num_tiles, int* status, int cap,
-                               int32_t* kept, void* xp, cudaStream_t s) {
+                               int32_t* kept, void* xp, const void* gamma, float eps, void* u,
+                               cudaStream_t s) {
     const int nq = slices_for(ntok, E, d);
     const size_t smem = (size_t)((ntok * E + 63) & ~63) * 4 +
                         (size_t)((ntok * E * nq + 63) & ~63) * 4 + dispatch_smem_bytes(E);
     const dim3 block(kDispatchWarps * 32);
+    cudaError_t e;
     if (dt == DType::BF16) {
         auto kern = route_small_kernel<__nv_bfloat16>;
         smem_attr((const void*)kern, (int)smem);
-        kern<<<1, block, smem, s>>>((const __nv_bfloat16*)x, (const __nv_bfloat16*)wr, bias, ntok,
-                                    d, E, k, topk_idx, topk_w, counts, offsets, perm, inv, bm,
-                                    tile_expert, tile_row, tile_info, num_tiles, status, cap,
-                                    kept, (uint4*)xp, nq);
+        e = launch_pdl(kern, 1, block, smem, s, (const __nv_bfloat16*)x, (const __nv_bfloat16*)wr,
+                       bias, ntok, d, E, k, topk_idx, topk_w, counts, offsets, perm, inv, bm,
+                       tile_expert, tile_row, tile_info, num_tiles, status, cap, kept, (uint4*)xp,
+                       nq, (const __nv_bfloat16*)gamma, eps, (__nv_bfloat16*)u);
     } else {
         auto kern = route_small_kernel<float>;
         smem_attr((const void*)kern, (int)smem);
-        kern<<<1, block, smem, s>>>((const float*)x, (const float*)wr, bias, ntok, d, E, k,
-                                    topk_idx, topk_w, counts, offsets, perm, inv, bm, tile_expert,
-                                    tile_row, tile_info, num_tiles, status, cap, kept,
-                                    (uint4*)xp, nq);
+        e = launch_pdl(kern, 1, block, smem, s, (const float*)x, (const float*)wr, bias, ntok, d, E,
+                       k, topk_idx, topk_w, counts, offsets, perm, inv, bm, tile_expert, tile_row,
+                       tile_info, num_tiles, status, cap, kept, (uint4*)xp, nq, (const float*)gamma,
+                       eps, (float*)u);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace colibri

@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 router_topk_simt(const T* __restrict__ x, const T* __restrict__ wr, const float* __restrict__ bias,
                  int ntok, int d, int E, int k, int32_t* __restrict__ topk_idx,
                  float* __restrict__ topk_w) {
+    pdl_enter();
     extern __shared__ float smem[];
     constexpr int kTokens = kRouterWarps / kWarpsPerToken;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -81,8 +82,9 @@ cudaError_t launch_router_t(const void* x, const void* wr, const float* bias, in
     const size_t smem = (size_t)kTokens * (d + 256) * sizeof(float);
     auto kern = router_topk_simt<T, kWarpsPerToken>;
     smem_attr((const void*)kern, (int)smem);
-    kern<<<grid, block, smem, s>>>((const T*)x, (const T*)wr, bias, ntok, d, E, k, idx, w);
-    return cudaGetLastError();
+    const cudaError_t e =
+        launch_pdl(kern, grid, block, smem, s, (const T*)x, (const T*)wr, bias, ntok, d, E, k, idx, w);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
