@@ -30,3 +30,9 @@ from .moe import (  # noqa: F401
     stack_layer,
     near_tie_tokens,
 )
+from .quant import (  # noqa: F401
+    quantize_int8_block64,
+    dequantize_int8_block64,
+    quantize_experts,
+    dequantize_experts,
+)

@@ -8,7 +8,9 @@ import pytest
 
 import oracle
 import oracle.moe as om
+import oracle.quant as oq
 import test_oracle_pins as pins
+import test_oracle_quant as qpins
 
 
 def _wrong_silu(z):                       # sign slip: z / (1 + e^z)
@@ -93,6 +95,60 @@ def test_planted_mistake_is_caught(monkeypatch, name, bad, checks):
         monkeypatch.setitem(om.__dict__, "_orig_" + orig.replace("_select", ""), getattr(om, orig))
     monkeypatch.setattr(om, name, bad)
     monkeypatch.setattr(oracle, name, bad)
+    for check in checks:
+        with pytest.raises(AssertionError):
+            check()
+
+
+# ---------------------------------------------------------------- int8 quantiser
+
+
+def _quant_variant(levels=254, widen=True, per_matrix=False, rounding=np.rint):
+    """A block quantiser with one plausible mistake switched on."""
+    def quant(w):
+        w = np.asarray(w, dtype=np.float64)
+        R, C = w.shape
+        if R % 64 or C % 64:
+            raise ValueError("ragged")
+        q = np.empty((R, C), np.int8)
+        s = np.empty((R // 64, C // 64), np.float32)
+        z = np.empty((R // 64, C // 64), np.int32)
+        for bi in range(R // 64):
+            for bj in range(C // 64):
+                blk = w[bi * 64:(bi + 1) * 64, bj * 64:(bj + 1) * 64]
+                src = w if per_matrix else blk
+                lo, hi = float(src.min()), float(src.max())
+                if widen:
+                    lo, hi = min(lo, 0.0), max(hi, 0.0)
+                s32 = np.float32(1.0) if hi == lo else np.float32((hi - lo) / levels)
+                zz = 0 if hi == lo else int(rounding(-127 - lo / np.float64(s32)))
+                q[bi * 64:(bi + 1) * 64, bj * 64:(bj + 1) * 64] = np.clip(
+                    rounding(blk / np.float64(s32)) + zz, -127, 127).astype(np.int8)
+                s[bi, bj], z[bi, bj] = s32, zz
+        return q, s, z
+    return quant
+
+
+def _dequant_plus_zp(q, scale, zp):        # sign slip on the zero point
+    return oq.__dict__["_orig_dequantize_int8_block64"](q, scale, -np.asarray(zp))
+
+
+QUANT_CASES = [
+    ("quantize_int8_block64", _quant_variant(levels=255), [qpins.test_worked_block_symmetric_range]),
+    ("quantize_int8_block64", _quant_variant(per_matrix=True), [qpins.test_blocks_are_quantised_independently]),
+    ("quantize_int8_block64", _quant_variant(widen=False), [qpins.test_all_positive_block_keeps_zero_exact]),
+    ("quantize_int8_block64", _quant_variant(rounding=np.floor),
+     [qpins.test_codes_are_the_nearest_grid_points_brute_force,
+      lambda: qpins.test_half_step_error_bound_and_ranges((128, 192))]),
+    ("dequantize_int8_block64", _dequant_plus_zp, [qpins.test_worked_block_positive_range]),
+]
+
+
+@pytest.mark.parametrize("name,bad,checks", QUANT_CASES,
+                         ids=[f"{c[0]}-{i}" for i, c in enumerate(QUANT_CASES)])
+def test_planted_quantiser_mistake_is_caught(monkeypatch, name, bad, checks):
+    monkeypatch.setitem(oq.__dict__, "_orig_dequantize_int8_block64", oq.dequantize_int8_block64)
+    monkeypatch.setattr(oq, name, bad)
     for check in checks:
         with pytest.raises(AssertionError):
             check()
