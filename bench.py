@@ -60,6 +60,9 @@ def parse_args(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="tokens per step (default per workload; batch per step for the stack)")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--weights", choices=["bf16", "int8"], default="bf16",
+                    help="expert weight format: bf16, or int8 64x64 blocks (converted on the host, "
+                         "streamed and dequantised on CUDA cores)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the decode-size sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -81,20 +84,33 @@ def peaks():
             "source": "fallback"}
 
 
-def algorithmic(shape, T, counts):
-    """Algorithmic bytes and FLOPs of one layer call (active experts only)."""
+def algorithmic(shape, T, counts, weights="bf16"):
+    """Algorithmic bytes and FLOPs of one layer call (active experts only).
+
+    int8 expert weights: one byte per weight plus 8 bytes (scale, zero point)
+    per 64x64 block."""
     d, f, E, k = shape.d_model, shape.d_ff, shape.n_experts, shape.top_k
     s = 2 if shape.dtype == "bf16" else 4
+    w = d * f * (1.0 + 8.0 / 4096) if weights == "int8" else d * f * s   # one expert matrix
     active = int((counts > 0).sum())
     return {
         "active_experts": active,
-        "bytes": active * 3 * d * f * s + d * E * s + 2 * T * d * s + T * k * 8,
+        "bytes": int(active * 3 * w + d * E * s + 2 * T * d * s + T * k * 8),
         "flops": 2 * T * d * E + 6 * T * k * d * f,
         # per kernel
         "up_flops": 4 * T * k * d * f, "down_flops": 2 * T * k * d * f,
-        "up_bytes": active * 2 * d * f * s + T * d * s + T * k * f * s,
-        "down_bytes": active * d * f * s + T * k * f * s + T * k * d * 4,
+        "up_bytes": int(active * 2 * w + T * d * s + T * k * f * s),
+        "down_bytes": int(active * w + T * k * f * s + T * k * d * 4),
     }
+
+
+def make_layer(sef, shape, wr, wg, wu, wd, weights, **kw):
+    """A library handle over bf16 weights, or over their int8 conversion
+    (the library's converter, on the host)."""
+    if weights == "int8":
+        parts = [tuple(t.to(wr.device) for t in sef.quantize_int8_block64(w)) for w in (wg, wu, wd)]
+        return sef.MoELayer(wr, None, None, None, shape.top_k, int8=parts, **kw)
+    return sef.MoELayer(wr, wg, wu, wd, shape.top_k, **kw)
 
 
 def source_sha(*rel):
@@ -297,9 +313,9 @@ def run_ours(args):
     wr = synth.router_weight(shape, seed, 0, dev)
     wg, wu, wd = synth.expert_weights(shape, seed, 0, dev)
     max_t = max(T, 128)
-    layer = sef.MoELayer(wr, wg, wu, wd, shape.top_k, router_bias=synth.router_offset(shape),
-                         max_tokens=max_t)
-    weight_gb = (wg.numel() + wu.numel() + wd.numel()) * wg.element_size() / 1e9
+    layer = make_layer(sef, shape, wr, wg, wu, wd, args.weights,
+                       router_bias=synth.router_offset(shape), max_tokens=max_t)
+    weight_gb = (wg.numel() + wu.numel() + wd.numel()) * (1 if args.weights == "int8" else wg.element_size()) / 1e9
     del wg, wu, wd
     torch.cuda.empty_cache()
     x = synth.tokens(shape, T, seed, 0, dev)
@@ -324,7 +340,7 @@ def run_ours(args):
     ms_prof = max_over_ranks(ms_prof, world)
     r = layer.routing()
     counts = r["counts"].cpu().numpy()
-    alg = algorithmic(shape, T, counts)
+    alg = algorithmic(shape, T, counts, args.weights)
     step_ms = ms / args.steps
     value = job_throughput(world, T, args.steps, ms)
 
@@ -332,8 +348,9 @@ def run_ours(args):
     dom = max(stages, key=lambda s: stages[s]["ms_total"])
     per_launch_s = stages[dom]["ms_total"] / stages[dom]["launches"] / 1e3
     grouped = "gather" in stages
+    i8 = "_i8" if args.weights == "int8" else ""
     kname = {("expert_up", True): "grouped_gemm_tc<kGateUp>", ("expert_down", True): "grouped_gemm_tc<kDown>",
-             ("expert_up", False): "ffn_up_stream", ("expert_down", False): "ffn_down_stream"}.get(
+             ("expert_up", False): "ffn_up_stream" + i8, ("expert_down", False): "ffn_down_stream" + i8}.get(
         (dom, grouped), dom)
     workload = f"{args.workload}_T{T}"
     if grouped and dom in ("expert_up", "expert_down"):
@@ -385,7 +402,7 @@ def run_ours(args):
             layer.set_executor("auto")
             ms_s = max_over_ranks(ms_s, world)
             cs = layer.routing()["counts"].cpu().numpy()
-            a_s = algorithmic(shape, Ts, cs)
+            a_s = algorithmic(shape, Ts, cs, args.weights)
             t_step = ms_s / args.steps / 1e3
             sweep[f"T{Ts}" + ("" if ex == "auto" else "_" + ex)] = {
                                "tokens_per_s": round(world * Ts / t_step, 1),
@@ -406,7 +423,8 @@ def run_ours(args):
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{label}, T={T} tokens",
+        "config": {"workload": f"{label}, T={T} tokens" + (", int8 expert weights" if args.weights == "int8" else ""),
+                   "weights": args.weights,
                    "d_model": shape.d_model, "d_ff": shape.d_ff, "n_experts": shape.n_experts,
                    "top_k": shape.top_k, "tokens_per_gpu": T, "parallelism": f"token-parallel x{world}",
                    "l2": f"inputs larger than L2 ({weight_gb:.2f} GB of expert weights per step)"},
@@ -449,7 +467,7 @@ def run_stack(args):
     for l in range(synth.STACK_LAYERS):
         wr = synth.router_weight(shape, seed, l, dev)
         wg, wu, wd = synth.expert_weights(shape, seed, l, dev)
-        layers.append(sef.MoELayer(wr, wg, wu, wd, shape.top_k, max_tokens=max(B, 1)))
+        layers.append(make_layer(sef, shape, wr, wg, wu, wd, args.weights, max_tokens=max(B, 1)))
         del wr, wg, wu, wd
     torch.cuda.empty_cache()
     gamma = torch.ones(shape.d_model, dtype=torch.bfloat16, device=dev)
@@ -501,14 +519,16 @@ def run_stack(args):
         assert layer.check() == 0
     step_s = ms / args.steps / 1e3
     d, f, E = shape.d_model, shape.d_ff, shape.n_experts
-    step_bytes = active * 3 * d * f * 2 + synth.STACK_LAYERS * (d * E * 2 + 4 * B * d * 2 + d * 2)
+    wbytes = d * f * (1.0 + 8.0 / 4096) if args.weights == "int8" else d * f * 2
+    step_bytes = int(active * 3 * wbytes + synth.STACK_LAYERS * (d * E * 2 + 4 * B * d * 2 + d * 2))
     out = {
         "metric": "MoE-layer tokens/s at 1 GB300; % of HBM (decode) / bf16 TC (prefill) roofline",
         "value": round(job_throughput(world, B, args.steps, ms), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{WORKLOADS['stack'][2]}, batch {B}", "layers": synth.STACK_LAYERS,
+        "config": {"workload": f"{WORKLOADS['stack'][2]}, batch {B}" + (", int8 expert weights" if args.weights == "int8" else ""),
+                   "weights": args.weights, "layers": synth.STACK_LAYERS,
                    "batch": B, "parallelism": f"token-parallel x{world}",
                    "l2": "inputs larger than L2 (90 GB of weights)"},
         "stack_roofline": {"bound": "hbm", "bytes_per_step": step_bytes,

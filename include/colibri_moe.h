@@ -93,6 +93,55 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg,
                               int weights_on_device, colibri_moe_t** out);
 
 /*
+ * Weight-only int8 expert weights (m.nxbn.cn section 3.1: every expert
+ * matrix cut into 64x64 blocks, each quantised from its own min and max into
+ * an int8 weight buffer and a scale buffer, dequantised inside the GEMM;
+ * pnsm.cn section 3.1: min-max to [-127, 127], converted on the CPU; pnsm.cn
+ * section 5.2: w = (q - zp) * scale with an int32 zero point).
+ *
+ * Per 64x64 block b of a matrix (rows and columns multiples of 64):
+ *   lo = min(min(b), 0), hi = max(max(b), 0)
+ *   scale = float32((hi - lo) / 254)           (1 for a block of zeros)
+ *   zp    = round(-127 - lo / scale)           in [-127, 127]
+ *   q     = clamp(round(w / scale) + zp, -127, 127)
+ * with round = nearest, ties to even, evaluated in double precision from the
+ * float32 scale.  Dequantised weight: (q - zp) * scale, within scale / 2 of w.
+ */
+typedef struct {
+    const int8_t* q;       /* [E, R, C] codes, in the float weight's layout */
+    const float* scale;    /* [E, R/64, C/64] */
+    const int32_t* zp;     /* [E, R/64, C/64] */
+} colibri_int8_weights_t;
+
+/*
+ * colibri_quantize_int8_block64 - the converter: quantise one row-major
+ * [rows, cols] matrix (host memory, dtype FP32 or BF16) block by block as
+ * above into caller-owned host arrays q [rows, cols], scale and zp
+ * [rows/64, cols/64].  Runs on the calling CPU thread; no device work.
+ * INVALID_ARG for NULL pointers, rows or cols not positive multiples of 64,
+ * or a non-finite weight.
+ */
+colibri_status_t colibri_quantize_int8_block64(const void* w, int32_t dtype, int32_t rows,
+                                               int32_t cols, int8_t* q, float* scale,
+                                               int32_t* zp);
+
+/*
+ * colibri_init_int8 - a layer handle whose expert weights are int8 blocks:
+ *   w_gate, w_up  R = d_model, C = d_ff   (as colibri_init's [E, d_model, d_ff])
+ *   w_down        R = d_ff,    C = d_model
+ * w_router / router_bias / cfg as in colibri_init (cfg->dtype is the
+ * activation and router type).  The expert FFN streams the int8 weights on
+ * CUDA cores and dequantises them in registers (executor STREAM; GROUPED is
+ * UNSUPPORTED for int8 weights).  weights_on_device applies to every array.
+ */
+colibri_status_t colibri_init_int8(const colibri_moe_config_t* cfg,
+                                   const void* w_router, const float* router_bias,
+                                   const colibri_int8_weights_t* w_gate,
+                                   const colibri_int8_weights_t* w_up,
+                                   const colibri_int8_weights_t* w_down,
+                                   int weights_on_device, colibri_moe_t** out);
+
+/*
  * colibri_forward - y = MoE(x) for T tokens (zskr.cn section 3.3 stages 2-5).
  *   x  [T, d_model] device, dtype, 16-byte aligned, read only
  *   y  [T, d_model] device, dtype, 16-byte aligned, written; must not overlap x

@@ -34,6 +34,10 @@ class ColibriConfig(ctypes.Structure):
                 ("device", ctypes.c_int32), ("executor", ctypes.c_int32)]
 
 
+class ColibriInt8Weights(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("zp", ctypes.c_void_p)]
+
+
 class ColibriError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -50,6 +54,10 @@ def _load():
     sig = {
         "colibri_init": ([ctypes.POINTER(ColibriConfig), P, P, P, P, P, ctypes.c_int,
                           ctypes.POINTER(P)], I32),
+        "colibri_init_int8": ([ctypes.POINTER(ColibriConfig), P, P,
+                               ctypes.POINTER(ColibriInt8Weights), ctypes.POINTER(ColibriInt8Weights),
+                               ctypes.POINTER(ColibriInt8Weights), ctypes.c_int, ctypes.POINTER(P)], I32),
+        "colibri_quantize_int8_block64": ([P, I32, I32, I32, P, P, P], I32),
         "colibri_forward": ([P, P, I32, P, P], I32),
         "colibri_forward_host": ([P, P, I32, P, P], I32),
         "colibri_rmsnorm_moe_residual": ([P, P, I32, P, ctypes.c_float, P], I32),
@@ -73,7 +81,7 @@ def _load():
 
 
 _lib = None
-_C_NAMES = ("colibri_init", "colibri_forward", "colibri_forward_host",
+_C_NAMES = ("colibri_init", "colibri_init_int8", "colibri_quantize_int8_block64", "colibri_forward", "colibri_forward_host",
             "colibri_rmsnorm_moe_residual", "colibri_get_routing", "colibri_set_executor",
             "colibri_set_capacity",
             "colibri_check", "colibri_launch_count", "colibri_workspace_bytes",
@@ -116,6 +124,32 @@ def _stream_ptr(stream) -> int:
     return stream.cuda_stream
 
 
+def quantize_int8_block64(w):
+    """The library's int8 converter on one [R, C] matrix or an [E, R, C] stack
+    (float32 or bfloat16 torch tensor; copied to the host).  Returns CPU
+    tensors (q int8, scale float32, zp int32) with scale/zp shaped
+    [..., R/64, C/64] (the block format of ``colibri_init_int8``)."""
+    import torch
+    if w.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("weights must be float32 or bfloat16")
+    wc = w.detach().to("cpu").contiguous()
+    stack = wc.dim() == 3
+    if not stack:
+        wc = wc.unsqueeze(0)
+    E, R, C = wc.shape
+    q = torch.empty((E, R, C), dtype=torch.int8)
+    sc = torch.empty((E, R // 64, C // 64), dtype=torch.float32)
+    zp = torch.empty((E, R // 64, C // 64), dtype=torch.int32)
+    dt = DTYPE_BF16 if wc.dtype == torch.bfloat16 else DTYPE_FP32
+    for e in range(E):
+        _check(library().colibri_quantize_int8_block64(_ptr(wc[e]), dt, R, C, _ptr(q[e]),
+                                                       _ptr(sc[e]), _ptr(zp[e])),
+               "colibri_quantize_int8_block64")
+    if not stack:
+        return q[0], sc[0], zp[0]
+    return q, sc, zp
+
+
 class MoELayer:
     """One MoE layer handle on one GPU.
 
@@ -127,13 +161,23 @@ class MoELayer:
     """
 
     def __init__(self, w_router, w_gate, w_up, w_down, top_k: int, router_bias=None,
-                 max_tokens: int = 4096, executor: str = "auto", device: Optional[int] = None):
+                 max_tokens: int = 4096, executor: str = "auto", device: Optional[int] = None,
+                 int8=None):
         import torch
         if w_router.dtype not in (torch.float32, torch.bfloat16):
             raise TypeError("weights must be float32 or bfloat16")
-        for w in (w_gate, w_up, w_down):
-            if w.dtype != w_router.dtype or w.device != w_router.device:
-                raise TypeError("all weights must share dtype and device")
+        if int8 is not None:
+            # int8 expert weights: ((q, scale, zp) of gate, up, down) as made by
+            # quantize_int8_block64; w_gate / w_up / w_down give only the shapes
+            w_gate, w_up, w_down = (part[0] for part in int8)
+            for part in int8:
+                for t in part:
+                    if t.device != w_router.device:
+                        raise TypeError("int8 weights must be on the router's device")
+        else:
+            for w in (w_gate, w_up, w_down):
+                if w.dtype != w_router.dtype or w.device != w_router.device:
+                    raise TypeError("all weights must share dtype and device")
         E, d, f = w_gate.shape
         if tuple(w_router.shape) != (d, E) or tuple(w_up.shape) != (E, d, f) or \
                 tuple(w_down.shape) != (E, f, d):
@@ -145,7 +189,8 @@ class MoELayer:
         self.E, self.d, self.f, self.k = E, d, f, int(top_k)
         self.max_tokens = int(max_tokens)
         on_dev = 1 if w_router.is_cuda else 0
-        ws = [w.contiguous() for w in (w_router, w_gate, w_up, w_down)]
+        ws = [w_router.contiguous()] + ([None] * 3 if int8 is not None else
+                                        [w.contiguous() for w in (w_gate, w_up, w_down)])
         bias = None
         if router_bias is not None:
             bias = router_bias.to(torch.float32).contiguous()
@@ -156,9 +201,19 @@ class MoELayer:
                             device, _EXEC[executor])
         h = ctypes.c_void_p()
         with torch.cuda.device(self.device):
-            st = library().colibri_init(ctypes.byref(cfg), *[_ptr(w) for w in ws[:1]], _ptr(bias),
-                              *[_ptr(w) for w in ws[1:]], on_dev, ctypes.byref(h))
-        _check(st, "colibri_init")
+            if int8 is None:
+                st = library().colibri_init(ctypes.byref(cfg), _ptr(ws[0]), _ptr(bias),
+                                            *[_ptr(w) for w in ws[1:]], on_dev, ctypes.byref(h))
+            else:
+                # int8 = ((q, scale, zp) of gate, up, down), each with the
+                # float weight's layout and the router's device
+                self._int8 = [tuple(t.contiguous() for t in part) for part in int8]
+                iw = [ColibriInt8Weights(*[_ptr(t) for t in part]) for part in self._int8]
+                st = library().colibri_init_int8(ctypes.byref(cfg), _ptr(ws[0]), _ptr(bias),
+                                                 *[ctypes.byref(w) for w in iw], on_dev,
+                                                 ctypes.byref(h))
+                self._int8 = None
+        _check(st, "colibri_init_int8" if int8 is not None else "colibri_init")
         self._h = h
         self.last_T = 0
 

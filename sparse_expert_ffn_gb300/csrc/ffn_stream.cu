@@ -147,7 +147,200 @@ ffn_down_stream(const T* __restrict__ H, const T* __restrict__ wdT,
     }
 }
 
+// ------------------------------------------------------------ int8 weights
+//
+// Expert weights as int8 codes in 64x64 blocks, w = (q - zp) * scale
+// (m.nxbn.cn section 3.1; pnsm.cn section 5.2).  A lane loads 16 consecutive
+// codes of a row (one 16-byte vector, all in one block); a byte permute turns
+// each code into the exact float 2^23 + 128 + q and one exact subtraction of
+// 2^23 + 128 + zp leaves q - zp, so the conversion costs two instructions per
+// weight; the block's scale multiplies the lane's 16-term partial sum once.
+// Block scales and zero points of gate/up: [E][2][f/64][d/64] (which, n-block,
+// k-block); of down: [E][d/64][f/64].
+
+constexpr int kAheadI8 = 4;   // 16-byte vectors per row in flight per lane
+
+// q - zp for the 16 codes of v, as floats.
+__device__ __forceinline__ void dequant16(const uint4& v, float off, float (&t)[16]) {
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                           v.w ^ 0x80808080u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        t[4 * i + 0] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7540)) - off;
+        t[4 * i + 1] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7541)) - off;
+        t[4 * i + 2] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7542)) - off;
+        t[4 * i + 3] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7543)) - off;
+    }
+}
+
+// 2^23 + 128 + zp: subtracting it from the permuted code gives q - zp exactly.
+__device__ __forceinline__ float code_offset(int32_t zp) { return 8388736.0f + (float)zp; }
+
+template <typename T>
+__device__ __forceinline__ float dot16(const T* xr, const float (&t)[16]) {
+    float a[8], b[8];
+    load8(xr, a);
+    load8(xr + 8, b);
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) s = fmaf(a[c], t[c], s);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) s = fmaf(b[c], t[8 + c], s);
+    return s;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+ffn_up_stream_i8(const T* __restrict__ x, const int8_t* __restrict__ wq,
+                 const float* __restrict__ sc, const int32_t* __restrict__ zpt,
+                 const int32_t* __restrict__ kept, const int32_t* __restrict__ offsets,
+                 const int32_t* __restrict__ perm, int k, int d, int f, int E, T* __restrict__ H) {
+    pdl_enter();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = blockIdx.x * kWarps + warp;
+    if (n >= f) return;
+    const int nkb = d / 64;
+    for (int e = 0; e < E; ++e) {
+        const int c = kept[e];
+        if (c == 0) continue;
+        const int off = offsets[e];
+        const int8_t* g_row = wq + gu_row(e, n, 0, f) * d;
+        const int8_t* u_row = wq + gu_row(e, n, 1, f) * d;
+        const size_t gb = ((size_t)(2 * e) * (f / 64) + n / 64) * nkb;   // gate block row
+        const size_t ub = ((size_t)(2 * e + 1) * (f / 64) + n / 64) * nkb;
+        for (int s0 = 0; s0 < c; s0 += kSlots) {
+            const int ns = min(kSlots, c - s0);
+            const T* xr[kSlots];
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s)
+                xr[s] = x + (size_t)(perm[off + s0 + (s < ns ? s : 0)] / k) * d;
+            float ag[kSlots], au[kSlots];
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) ag[s] = au[s] = 0.f;
+            for (int i0 = lane * 16; i0 < d; i0 += 512 * kAheadI8) {
+                uint4 vg[kAheadI8], vu[kAheadI8];
+#pragma unroll
+                for (int a = 0; a < kAheadI8; ++a) {
+                    if (i0 + a * 512 < d) {
+                        vg[a] = ld_stream16(g_row + i0 + a * 512);
+                        vu[a] = ld_stream16(u_row + i0 + a * 512);
+                    }
+                }
+#pragma unroll
+                for (int a = 0; a < kAheadI8; ++a) {
+                    const int i = i0 + a * 512;
+                    if (i < d) {
+                        const int kb = i >> 6;
+                        const float sg = __ldg(sc + gb + kb), su = __ldg(sc + ub + kb);
+                        float tg[16], tu[16];
+                        dequant16(vg[a], code_offset(__ldg(zpt + gb + kb)), tg);
+                        dequant16(vu[a], code_offset(__ldg(zpt + ub + kb)), tu);
+#pragma unroll
+                        for (int s = 0; s < kSlots; ++s) {
+                            if (s < ns) {
+                                ag[s] = fmaf(sg, dot16(xr[s] + i, tg), ag[s]);
+                                au[s] = fmaf(su, dot16(xr[s] + i, tu), au[s]);
+                            }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) {
+                if (s < ns) {
+                    const float g = warp_sum(ag[s]);
+                    const float u = warp_sum(au[s]);
+                    if (lane == 0) H[(size_t)(off + s0 + s) * f + n] = from_f32<T>(silu(g) * u);
+                }
+            }
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+ffn_down_stream_i8(const T* __restrict__ H, const int8_t* __restrict__ wq,
+                   const float* __restrict__ sc, const int32_t* __restrict__ zpt,
+                   const int32_t* __restrict__ kept, const int32_t* __restrict__ offsets, int d,
+                   int f, int E, float* __restrict__ Y) {
+    pdl_enter();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col = blockIdx.x * kWarps + warp;
+    if (col >= d) return;
+    const int nkb = f / 64;
+    for (int e = 0; e < E; ++e) {
+        const int c = kept[e];
+        if (c == 0) continue;
+        const int off = offsets[e];
+        const int8_t* w_row = wq + ((size_t)e * d + col) * f;
+        const size_t bb = ((size_t)e * (d / 64) + col / 64) * nkb;
+        for (int s0 = 0; s0 < c; s0 += kSlots) {
+            const int ns = min(kSlots, c - s0);
+            float acc[kSlots];
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) acc[s] = 0.f;
+            for (int i0 = lane * 16; i0 < f; i0 += 512 * kAheadI8) {
+                uint4 v[kAheadI8];
+#pragma unroll
+                for (int a = 0; a < kAheadI8; ++a)
+                    if (i0 + a * 512 < f) v[a] = ld_stream16(w_row + i0 + a * 512);
+#pragma unroll
+                for (int a = 0; a < kAheadI8; ++a) {
+                    const int i = i0 + a * 512;
+                    if (i < f) {
+                        const int kb = i >> 6;
+                        const float sw = __ldg(sc + bb + kb);
+                        float t[16];
+                        dequant16(v[a], code_offset(__ldg(zpt + bb + kb)), t);
+#pragma unroll
+                        for (int s = 0; s < kSlots; ++s)
+                            if (s < ns)
+                                acc[s] = fmaf(sw, dot16(H + (size_t)(off + s0 + s) * f + i, t), acc[s]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) {
+                if (s < ns) {
+                    const float v = warp_sum(acc[s]);
+                    if (lane == 0) Y[(size_t)(off + s0 + s) * d + col] = v;
+                }
+            }
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_ffn_up_stream_i8(DType dt, const void* x, const int8_t* wq, const float* sc,
+                                    const int32_t* zp, const int32_t* kept,
+                                    const int32_t* offsets, const int32_t* perm, int k, int d,
+                                    int f, int E, void* H, cudaStream_t s) {
+    const dim3 block(kWarps * 32), grid((f + kWarps - 1) / kWarps);
+    cudaError_t e;
+    if (dt == DType::BF16)
+        e = launch_pdl(ffn_up_stream_i8<__nv_bfloat16>, grid, block, 0, s, (const __nv_bfloat16*)x,
+                       wq, sc, zp, kept, offsets, perm, k, d, f, E, (__nv_bfloat16*)H);
+    else
+        e = launch_pdl(ffn_up_stream_i8<float>, grid, block, 0, s, (const float*)x, wq, sc, zp,
+                       kept, offsets, perm, k, d, f, E, (float*)H);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_ffn_down_stream_i8(DType dt, const void* H, const int8_t* wq, const float* sc,
+                                      const int32_t* zp, const int32_t* kept,
+                                      const int32_t* offsets, int d, int f, int E, float* Y,
+                                      cudaStream_t s) {
+    const dim3 block(kWarps * 32), grid((d + kWarps - 1) / kWarps);
+    cudaError_t e;
+    if (dt == DType::BF16)
+        e = launch_pdl(ffn_down_stream_i8<__nv_bfloat16>, grid, block, 0, s,
+                       (const __nv_bfloat16*)H, wq, sc, zp, kept, offsets, d, f, E, Y);
+    else
+        e = launch_pdl(ffn_down_stream_i8<float>, grid, block, 0, s, (const float*)H, wq, sc, zp,
+                       kept, offsets, d, f, E, Y);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* kept,
                                  const int32_t* offsets, const int32_t* perm, int k, int d, int f,

@@ -42,6 +42,17 @@ struct colibri_moe {
     float* bias = nullptr;  // [E] or null
     void* wgu = nullptr;    // [E][f/128][2][128][d]
     void* wdT = nullptr;    // [E][d][f]
+    // int8 expert weights (colibri_init_int8): codes in the same packed
+    // layouts, block scales / zero points of gate+up [E][2][f/64][d/64] and
+    // of down [E][d/64][f/64]
+    bool int8 = false;
+    int8_t* q_gu = nullptr;
+    int8_t* q_d = nullptr;
+    void* qmeta = nullptr;            // one allocation: the four arrays below
+    float* sc_gu = nullptr;
+    int32_t* zp_gu = nullptr;
+    float* sc_d = nullptr;
+    int32_t* zp_d = nullptr;
     uint64_t weight_bytes = 0;
     // workspace
     void* ws = nullptr;
@@ -187,6 +198,9 @@ void release(colibri_moe_t* h) {
     cudaFree(h->bias);
     cudaFree(h->wgu);
     cudaFree(h->wdT);
+    cudaFree(h->q_gu);
+    cudaFree(h->q_d);
+    cudaFree(h->qmeta);
     cudaFree(h->ws);
     delete h;
 }
@@ -205,20 +219,19 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
 // Copy (host or device) matrices [batch][R][C] into the packed layout through
 // the remapping transpose; host inputs go through a device staging buffer one
 // batch entry at a time.
-colibri_status_t pack(colibri_moe_t* h, const void* src, bool src_on_device,
-                      void* dst, int batch, int R, int C, size_t out_batch, int blk, int period,
-                      int which, void* staging) {
-    const size_t mat = (size_t)R * C * h->esz;
+colibri_status_t pack(int esz, const void* src, bool src_on_device, void* dst, int batch, int R,
+                      int C, size_t out_batch, int blk, int period, int which, void* staging) {
+    const size_t mat = (size_t)R * C * esz;
     if (src_on_device) {
-        return from_cuda(launch_transpose_remap(h->esz, src, dst, batch, R, C, (size_t)R * C,
+        return from_cuda(launch_transpose_remap(esz, src, dst, batch, R, C, (size_t)R * C,
                                                 out_batch, blk, period, which, 0));
     }
     for (int b = 0; b < batch; ++b) {
         cudaError_t e = cudaMemcpy(staging, (const uint8_t*)src + (size_t)b * mat, mat,
                                    cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return from_cuda(e);
-        e = launch_transpose_remap(h->esz, staging, (uint8_t*)dst + (size_t)b * out_batch * h->esz,
-                                   1, R, C, (size_t)R * C, out_batch, blk, period, which, 0);
+        e = launch_transpose_remap(esz, staging, (uint8_t*)dst + (size_t)b * out_batch * esz, 1, R,
+                                   C, (size_t)R * C, out_batch, blk, period, which, 0);
         if (e != cudaSuccess) return from_cuda(e);
         e = cudaDeviceSynchronize();
         if (e != cudaSuccess) return from_cuda(e);
@@ -356,14 +369,21 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     if (ex == COLIBRI_EXEC_STREAM) {
         {
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
-            st = g.done(launch_ffn_up_stream(h->dt, x, h->wgu, h->kept, h->offsets, h->perm, k,
-                                             d, f, E, h->H, s), 1);
+            st = g.done(h->int8 ? launch_ffn_up_stream_i8(h->dt, x, h->q_gu, h->sc_gu, h->zp_gu,
+                                                          h->kept, h->offsets, h->perm, k, d, f, E,
+                                                          h->H, s)
+                                : launch_ffn_up_stream(h->dt, x, h->wgu, h->kept, h->offsets,
+                                                       h->perm, k, d, f, E, h->H, s),
+                        1);
             if (st != COLIBRI_OK) return st;
         }
         {
             Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
-            st = g.done(launch_ffn_down_stream(h->dt, h->H, h->wdT, h->kept, h->offsets, d, f,
-                                               E, h->Y, s), 1);
+            st = g.done(h->int8 ? launch_ffn_down_stream_i8(h->dt, h->H, h->q_d, h->sc_d, h->zp_d,
+                                                            h->kept, h->offsets, d, f, E, h->Y, s)
+                                : launch_ffn_down_stream(h->dt, h->H, h->wdT, h->kept, h->offsets,
+                                                         d, f, E, h->Y, s),
+                        1);
             if (st != COLIBRI_OK) return st;
         }
     } else {
@@ -471,14 +491,31 @@ const char* colibri_status_str(colibri_status_t s) {
     return "unknown status";
 }
 
-colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_router,
-                              const float* router_bias, const void* w_gate, const void* w_up,
-                              const void* w_down, int weights_on_device, colibri_moe_t** out) {
+}  // extern "C"
+
+namespace {
+
+// Shared by colibri_init (bf16 / fp32 expert weights) and colibri_init_int8
+// (int8 blocks: qg / qu / qd non-null, w_gate / w_up / w_down unused).
+colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router,
+                           const float* router_bias, const void* w_gate, const void* w_up,
+                           const void* w_down, const colibri_int8_weights_t* qg,
+                           const colibri_int8_weights_t* qu, const colibri_int8_weights_t* qd,
+                           int weights_on_device, colibri_moe_t** out) {
     if (!out) return COLIBRI_ERR_INVALID_ARG;
     *out = nullptr;
     colibri_status_t st = validate_config(cfg);
     if (st != COLIBRI_OK) return st;
-    if (!w_router || !w_gate || !w_up || !w_down) return COLIBRI_ERR_INVALID_ARG;
+    const bool int8 = qg != nullptr;
+    if (!w_router) return COLIBRI_ERR_INVALID_ARG;
+    if (int8) {
+        if (!qu || !qd) return COLIBRI_ERR_INVALID_ARG;
+        for (const colibri_int8_weights_t* w : {qg, qu, qd})
+            if (!w->q || !w->scale || !w->zp) return COLIBRI_ERR_INVALID_ARG;
+        if (cfg->executor == COLIBRI_EXEC_GROUPED) return COLIBRI_ERR_UNSUPPORTED;
+    } else if (!w_gate || !w_up || !w_down) {
+        return COLIBRI_ERR_INVALID_ARG;
+    }
     if (weights_on_device != 0 && weights_on_device != 1) return COLIBRI_ERR_INVALID_ARG;
 
     int ndev = 0;
@@ -497,6 +534,7 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     h->esz = cfg->dtype == COLIBRI_DTYPE_BF16 ? 2 : 4;
     h->num_sms = prop.multiProcessorCount;
     h->e_pad = (cfg->n_experts + 15) / 16 * 16;
+    h->int8 = int8;
     // Failure-detection tests: a shorter bound for the device-side waits, and
     // a producer that never issues its copies (a flag that nothing sets).
     if (const char* e = std::getenv("COLIBRI_WAIT_LIMIT_NS")) h->wait_limit_ns = std::strtoull(e, nullptr, 10);
@@ -512,11 +550,24 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
 
     // ---- weights
     const size_t wr_bytes = (size_t)h->e_pad * d * h->esz;
-    const size_t wgu_bytes = (size_t)E * 2 * f * d * h->esz;
-    const size_t wd_bytes = (size_t)E * d * f * h->esz;
+    const size_t wsz = int8 ? 1 : (size_t)h->esz;       // expert weight element bytes
+    const size_t wgu_bytes = (size_t)E * 2 * f * d * wsz;
+    const size_t wd_bytes = (size_t)E * d * f * wsz;
+    const size_t nblk = (size_t)(d / 64) * (f / 64);      // 64x64 blocks per matrix
+    const size_t meta_bytes = int8 ? (size_t)E * 3 * nblk * 8 : 0;
     if ((st = from_cuda(ac.alloc(&h->wr, wr_bytes))) != COLIBRI_OK) return fail(st);
-    if ((st = from_cuda(ac.alloc(&h->wgu, wgu_bytes))) != COLIBRI_OK) return fail(st);
-    if ((st = from_cuda(ac.alloc(&h->wdT, wd_bytes))) != COLIBRI_OK) return fail(st);
+    if (int8) {
+        if ((st = from_cuda(ac.alloc((void**)&h->q_gu, wgu_bytes))) != COLIBRI_OK) return fail(st);
+        if ((st = from_cuda(ac.alloc((void**)&h->q_d, wd_bytes))) != COLIBRI_OK) return fail(st);
+        if ((st = from_cuda(ac.alloc(&h->qmeta, meta_bytes))) != COLIBRI_OK) return fail(st);
+        h->sc_gu = (float*)h->qmeta;
+        h->zp_gu = (int32_t*)(h->sc_gu + (size_t)E * 2 * nblk);
+        h->sc_d = (float*)(h->zp_gu + (size_t)E * 2 * nblk);
+        h->zp_d = (int32_t*)(h->sc_d + (size_t)E * nblk);
+    } else {
+        if ((st = from_cuda(ac.alloc(&h->wgu, wgu_bytes))) != COLIBRI_OK) return fail(st);
+        if ((st = from_cuda(ac.alloc(&h->wdT, wd_bytes))) != COLIBRI_OK) return fail(st);
+    }
     if (router_bias) {
         if ((st = from_cuda(ac.alloc((void**)&h->bias, (size_t)E * 4))) != COLIBRI_OK)
             return fail(st);
@@ -524,11 +575,13 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
             COLIBRI_OK)
             return fail(st);
     }
-    h->weight_bytes = wr_bytes + wgu_bytes + wd_bytes + (router_bias ? (size_t)E * 4 : 0);
+    h->weight_bytes =
+        wr_bytes + wgu_bytes + wd_bytes + meta_bytes + (router_bias ? (size_t)E * 4 : 0);
 
     void* staging = nullptr;
     if (!weights_on_device) {
-        const size_t stage_bytes = (size_t)std::max(d * f, d * E) * h->esz;
+        const size_t stage_bytes =
+            std::max((size_t)d * f * wsz, std::max((size_t)d * E * h->esz, nblk * 4));
         if ((st = from_cuda(ac.alloc(&staging, stage_bytes))) != COLIBRI_OK) return fail(st);
     }
     auto fail_staged = [&](colibri_status_t s) {
@@ -536,20 +589,38 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
         cudaFree(staging);
         return fail(s);
     };
+    const bool dev = weights_on_device != 0;
     if ((st = from_cuda(cudaMemset(h->wr, 0, wr_bytes))) != COLIBRI_OK) return fail_staged(st);
     // router [d, E] -> [E, d]
-    st = pack(h, w_router, weights_on_device, h->wr, 1, d, E, (size_t)h->e_pad * d, E, E, 0,
-              staging);
+    st = pack(h->esz, w_router, dev, h->wr, 1, d, E, (size_t)h->e_pad * d, E, E, 0, staging);
     if (st != COLIBRI_OK) return fail_staged(st);
-    // gate/up [E][d][f] -> [E][f/128][2][128][d]
-    st = pack(h, w_gate, weights_on_device, h->wgu, E, d, f, (size_t)2 * f * d, 128, 256, 0,
-              staging);
-    if (st != COLIBRI_OK) return fail_staged(st);
-    st = pack(h, w_up, weights_on_device, h->wgu, E, d, f, (size_t)2 * f * d, 128, 256, 1,
-              staging);
-    if (st != COLIBRI_OK) return fail_staged(st);
-    // down [E][f][d] -> [E][d][f]
-    st = pack(h, w_down, weights_on_device, h->wdT, E, f, d, (size_t)d * f, d, d, 0, staging);
+    if (!int8) {
+        // gate/up [E][d][f] -> [E][f/128][2][128][d]
+        st = pack(h->esz, w_gate, dev, h->wgu, E, d, f, (size_t)2 * f * d, 128, 256, 0, staging);
+        if (st == COLIBRI_OK)
+            st = pack(h->esz, w_up, dev, h->wgu, E, d, f, (size_t)2 * f * d, 128, 256, 1, staging);
+        // down [E][f][d] -> [E][d][f]
+        if (st == COLIBRI_OK)
+            st = pack(h->esz, w_down, dev, h->wdT, E, f, d, (size_t)d * f, d, d, 0, staging);
+    } else {
+        // codes: the bf16 layouts with one-byte elements
+        st = pack(1, qg->q, dev, h->q_gu, E, d, f, (size_t)2 * f * d, 128, 256, 0, staging);
+        if (st == COLIBRI_OK)
+            st = pack(1, qu->q, dev, h->q_gu, E, d, f, (size_t)2 * f * d, 128, 256, 1, staging);
+        if (st == COLIBRI_OK)
+            st = pack(1, qd->q, dev, h->q_d, E, f, d, (size_t)d * f, d, d, 0, staging);
+        // block scales and zero points: gate/up [E][d/64][f/64] -> [E][2][f/64][d/64],
+        // down [E][f/64][d/64] -> [E][d/64][f/64]
+        const int bd = d / 64, bf = f / 64;
+        const colibri_int8_weights_t* gu[2] = {qg, qu};
+        for (int w = 0; w < 2 && st == COLIBRI_OK; ++w) {
+            st = pack(4, gu[w]->scale, dev, h->sc_gu, E, bd, bf, 2 * nblk, bf, 2 * bf, w, staging);
+            if (st == COLIBRI_OK)
+                st = pack(4, gu[w]->zp, dev, h->zp_gu, E, bd, bf, 2 * nblk, bf, 2 * bf, w, staging);
+        }
+        if (st == COLIBRI_OK) st = pack(4, qd->scale, dev, h->sc_d, E, bf, bd, nblk, bd, bd, 0, staging);
+        if (st == COLIBRI_OK) st = pack(4, qd->zp, dev, h->zp_d, E, bf, bd, nblk, bd, bd, 0, staging);
+    }
     if (st != COLIBRI_OK) return fail_staged(st);
     if ((st = from_cuda(cudaDeviceSynchronize())) != COLIBRI_OK) return fail_staged(st);
     cudaFree(staging);
@@ -559,7 +630,7 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     const int M = cfg->max_tokens;
     h->max_pairs = M * k;
     h->max_tiles = (h->max_pairs + tc_gemm_block_m() - 1) / tc_gemm_block_m() + std::min(E, h->max_pairs);
-    h->grouped_ok = grouped_shape_ok(*cfg);
+    h->grouped_ok = !int8 && grouped_shape_ok(*cfg);
     if (cfg->executor == COLIBRI_EXEC_GROUPED && !h->grouped_ok) return fail(COLIBRI_ERR_UNSUPPORTED);
     const size_t P = (size_t)h->max_pairs;
     // Y: the down projection's float32 rows, or up to 8 K slices of them for
@@ -630,6 +701,30 @@ colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_rou
     if ((st = from_cuda(cudaDeviceSynchronize())) != COLIBRI_OK) return fail(st);
     *out = h;
     return COLIBRI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+colibri_status_t colibri_init(const colibri_moe_config_t* cfg, const void* w_router,
+                              const float* router_bias, const void* w_gate, const void* w_up,
+                              const void* w_down, int weights_on_device, colibri_moe_t** out) {
+    return init_impl(cfg, w_router, router_bias, w_gate, w_up, w_down, nullptr, nullptr, nullptr,
+                     weights_on_device, out);
+}
+
+colibri_status_t colibri_init_int8(const colibri_moe_config_t* cfg, const void* w_router,
+                                   const float* router_bias, const colibri_int8_weights_t* w_gate,
+                                   const colibri_int8_weights_t* w_up,
+                                   const colibri_int8_weights_t* w_down, int weights_on_device,
+                                   colibri_moe_t** out) {
+    if (!w_gate) {
+        if (out) *out = nullptr;
+        return COLIBRI_ERR_INVALID_ARG;
+    }
+    return init_impl(cfg, w_router, router_bias, nullptr, nullptr, nullptr, w_gate, w_up, w_down,
+                     weights_on_device, out);
 }
 
 colibri_status_t colibri_forward(colibri_moe_t* h, const void* x, int32_t T, void* y,

@@ -52,6 +52,16 @@ cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const
 cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, const int32_t* kept,
                                    const int32_t* offsets, int d, int f, int E, float* Y,
                                    cudaStream_t s);
+// Int8-weight variants (64x64 blocks, w = (q - zp) * scale); scales and zero
+// points of gate/up [E][2][f/64][d/64], of down [E][d/64][f/64].
+cudaError_t launch_ffn_up_stream_i8(DType dt, const void* x, const int8_t* wq, const float* sc,
+                                    const int32_t* zp, const int32_t* kept,
+                                    const int32_t* offsets, const int32_t* perm, int k, int d,
+                                    int f, int E, void* H, cudaStream_t s);
+cudaError_t launch_ffn_down_stream_i8(DType dt, const void* H, const int8_t* wq, const float* sc,
+                                      const int32_t* zp, const int32_t* kept,
+                                      const int32_t* offsets, int d, int f, int E, float* Y,
+                                      cudaStream_t s);
 
 cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,
                           int npairs, void* xp, cudaStream_t s);

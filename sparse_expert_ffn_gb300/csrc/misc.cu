@@ -167,7 +167,10 @@ cudaError_t launch_transpose_remap(int elem_bytes, const void* in, void* out, in
                                    int C, size_t in_batch, size_t out_batch, int blk, int period,
                                    int which, cudaStream_t s) {
     const dim3 block(32, 8), grid((C + 31) / 32, (R + 31) / 32, batch);
-    if (elem_bytes == 2)
+    if (elem_bytes == 1)
+        transpose_remap<uint8_t><<<grid, block, 0, s>>>((const uint8_t*)in, (uint8_t*)out, R, C,
+                                                        in_batch, out_batch, blk, period, which);
+    else if (elem_bytes == 2)
         transpose_remap<uint16_t><<<grid, block, 0, s>>>((const uint16_t*)in, (uint16_t*)out, R,
                                                          C, in_batch, out_batch, blk, period,
                                                          which);

@@ -85,6 +85,49 @@ class Case:
         self.layer.close()
 
 
+class Int8Experts:
+    """Per expert, the oracle's own int8 block quantisation of (W_g, W_u, W_d),
+    dequantised to float64 (oracle/quant.py), computed on demand."""
+
+    def __init__(self, wg, wu, wd):
+        self.wg, self.wu, self.wd = wg.cpu(), wu.cpu(), wd.cpu()
+        self._cache = {}
+
+    def __call__(self, e):
+        if e not in self._cache:
+            if len(self._cache) >= 2:
+                self._cache.pop(next(iter(self._cache)))
+            mats = []
+            for w in (self.wg[e], self.wu[e], self.wd[e]):
+                q, s, z = oracle.quantize_int8_block64(oracle.to_f64(w))
+                mats.append(oracle.dequantize_int8_block64(q, s, z))
+            self._cache[e] = tuple(mats)
+        return self._cache[e]
+
+
+class Int8Case(Case):
+    """A layer whose expert weights go through the library's int8 converter
+    (colibri_quantize_int8_block64) and colibri_init_int8; the oracle side
+    quantises the same float weights with its own quantiser."""
+
+    def __init__(self, shape: synth.LayerShape, seed: int, max_tokens: int,
+                 layer_idx: int = 0, bias="recipe"):
+        import sparse_expert_ffn_gb300 as sef
+        self.dev = torch.device("cuda", 0)
+        self.shape, self.seed, self.layer_idx = shape, seed, layer_idx
+        wr = synth.router_weight(shape, seed, layer_idx, self.dev)
+        wg, wu, wd = synth.expert_weights(shape, seed, layer_idx, self.dev)
+        self.bias = synth.router_offset(shape) if isinstance(bias, str) else bias
+        parts = [tuple(t.to(self.dev) for t in sef.quantize_int8_block64(w)) for w in (wg, wu, wd)]
+        self.layer = sef.MoELayer(wr, None, None, None, shape.top_k, router_bias=self.bias,
+                                  max_tokens=max_tokens, int8=parts)
+        self.wr64 = oracle.to_f64(wr)
+        self.experts = Int8Experts(wg, wu, wd)
+        self.off64 = None if self.bias is None else self.bias.double().numpy()
+        del wg, wu, wd, parts
+        torch.cuda.empty_cache()
+
+
 def check_routing(case: Case, x64, r, allow_near_ties: bool = True):
     """Compare routing to the oracle; returns (logits64, near_tie mask)."""
     k, E = case.shape.top_k, case.shape.n_experts

@@ -1,0 +1,69 @@
+"""GPU parity of the int8-weight layer (colibri_init_int8, weights converted
+by colibri_quantize_int8_block64, streamed and dequantised on CUDA cores)
+against the oracle run on its own int8 quantisation of the same weights."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from parity import Int8Case, check_output, check_routing
+
+pytestmark = pytest.mark.gpu
+
+
+def _sample(T, n, seed=0):
+    if T <= n:
+        return np.arange(T)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, T - 1), size=n - 2, replace=False)
+    return np.sort(np.concatenate([[0, T - 1], mid]))
+
+
+def test_tiny_fp32_int8_ragged():
+    c = Int8Case(synth.TINY, seed=0, max_tokens=64)
+    try:
+        for T in (1, 2, 17, 64):
+            x, x64 = c.tokens(T)
+            y, r = c.run(x)
+            l, _ = check_routing(c, x64, r)
+            check_output(c, x64, y, r, l)
+    finally:
+        c.close()
+
+
+@pytest.fixture(scope="module")
+def mixtral8(lib):
+    c = Int8Case(synth.MIXTRAL, seed=0, max_tokens=128)
+    yield c
+    c.close()
+
+
+@pytest.mark.parametrize("T", [1, 8, 16, 128])
+def test_mixtral_int8_decode(mixtral8, T):
+    x, x64 = mixtral8.tokens(T)
+    y, r = mixtral8.run(x)
+    l, _ = check_routing(mixtral8, x64, r)
+    check_output(mixtral8, x64, y, r, l, _sample(T, 24))
+    y2, _ = mixtral8.run(x)
+    assert torch.equal(y, y2)
+
+
+def test_mixtral_int8_rejects_the_grouped_executor(mixtral8):
+    import sparse_expert_ffn_gb300 as sef
+    with pytest.raises(sef.ColibriError):
+        mixtral8.layer.set_executor("grouped")
+
+
+def test_qwen_int8_zipf_with_capacity():
+    c = Int8Case(synth.QWEN2, seed=1, max_tokens=64)
+    try:
+        x, x64 = c.tokens(64)
+        y, r = c.run(x)
+        l, _ = check_routing(c, x64, r)
+        check_output(c, x64, y, r, l, _sample(64, 32))
+        c.layer.set_capacity(3)
+        y, r = c.run(x)
+        check_output(c, x64, y, r, l, _sample(64, 32), capacity=3)
+    finally:
+        c.close()
