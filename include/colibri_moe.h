@@ -130,9 +130,11 @@ colibri_status_t colibri_quantize_int8_block64(const void* w, int32_t dtype, int
  *   w_gate, w_up  R = d_model, C = d_ff   (as colibri_init's [E, d_model, d_ff])
  *   w_down        R = d_ff,    C = d_model
  * w_router / router_bias / cfg as in colibri_init (cfg->dtype is the
- * activation and router type).  The expert FFN streams the int8 weights on
- * CUDA cores and dequantises them in registers (executor STREAM; GROUPED is
- * UNSUPPORTED for int8 weights).  weights_on_device applies to every array.
+ * activation and router type).  Executors: GROUPED (bf16 activations; the
+ * default) streams the int8 codes into shared memory with TMA, converter
+ * warps dequantise each 256x64 stage to bf16 and the tcgen05 MMAs read it;
+ * STREAM dequantises in registers on CUDA cores (the only executor for fp32
+ * activations).  weights_on_device applies to every array.
  */
 colibri_status_t colibri_init_int8(const colibri_moe_config_t* cfg,
                                    const void* w_router, const float* router_bias,

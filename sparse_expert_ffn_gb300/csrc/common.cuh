@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -91,6 +92,19 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// 8 bf16 -> 8 f16 (round to nearest; exact for |v| in f16's normal range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4& v) {
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b[i]);
+        __half2 h = __floats2half2_rn(f.x, f.y);
+        o[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Coherent 8-element load (through L2): for rows this kernel wrote itself.
 __device__ __forceinline__ void load8_cg(const __nv_bfloat16* p, float (&v)[8]) {
     uint4 u = __ldcg(reinterpret_cast<const uint4*>(p));
@@ -168,6 +182,49 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Int8 weight codes (64x64 blocks, w = (q - zp) * scale).  The byte permute
+// places each code, sign bit flipped (q + 128 as an unsigned byte), in the low
+// mantissa byte of 2^23, which is the exact float 2^23 + 128 + q; subtracting
+// 2^23 + 128 + zp leaves q - zp exactly.  Two instructions per weight.
+// q - zp for the 16 codes of v, as floats.
+__device__ __forceinline__ void dequant16(const uint4& v, float off, float (&t)[16]) {
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                           v.w ^ 0x80808080u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        t[4 * i + 0] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7540)) - off;
+        t[4 * i + 1] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7541)) - off;
+        t[4 * i + 2] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7542)) - off;
+        t[4 * i + 3] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7543)) - off;
+    }
+}
+
+// 2^23 + 128 + zp: subtracting it from the permuted code gives q - zp exactly.
+__device__ __forceinline__ float code_offset(int32_t zp) { return 8388736.0f + (float)zp; }
+
+// The same in half precision, two codes per instruction: a byte permute puts
+// two codes (sign flipped) in the low bytes of two halves 1024.0 (0x6400),
+// i.e. 1024 + 128 + q each; one half2 subtraction of 1152 + zp leaves q - zp
+// exactly (|q - zp| <= 254), and one half2 multiply applies the scale.
+// 16 codes -> 16 halves (lo = codes 0..7, hi = codes 8..15).
+__device__ __forceinline__ void dequant16_h2(const uint4& v, __half2 off2, __half2 s2, uint4& lo,
+                                             uint4& hi) {
+    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                           v.w ^ 0x80808080u};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = __byte_perm(w[i], 0x64646464u, 0x5140);   // codes 0, 1 of the word
+        const uint32_t b = __byte_perm(w[i], 0x64646464u, 0x5342);   // codes 2, 3
+        __half2 ha = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&a), off2), s2);
+        __half2 hb = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&b), off2), s2);
+        o[2 * i] = *reinterpret_cast<uint32_t*>(&ha);
+        o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&hb);
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 // Device status word values (written by kernels, read by colibri_check).

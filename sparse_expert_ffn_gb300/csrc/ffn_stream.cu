@@ -155,26 +155,11 @@ ffn_down_stream(const T* __restrict__ H, const T* __restrict__ wdT,
 // each code into the exact float 2^23 + 128 + q and one exact subtraction of
 // 2^23 + 128 + zp leaves q - zp, so the conversion costs two instructions per
 // weight; the block's scale multiplies the lane's 16-term partial sum once.
-// Block scales and zero points of gate/up: [E][2][f/64][d/64] (which, n-block,
-// k-block); of down: [E][d/64][f/64].
+// Block scales and zero points are stored per 64-row block of the packed
+// weight rows (gate/up [E][f/128][2][128] rows, down [E][d] rows), k-block
+// fastest: [packed row / 64][K / 64].
 
 constexpr int kAheadI8 = 4;   // 16-byte vectors per row in flight per lane
-
-// q - zp for the 16 codes of v, as floats.
-__device__ __forceinline__ void dequant16(const uint4& v, float off, float (&t)[16]) {
-    const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
-                           v.w ^ 0x80808080u};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        t[4 * i + 0] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7540)) - off;
-        t[4 * i + 1] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7541)) - off;
-        t[4 * i + 2] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7542)) - off;
-        t[4 * i + 3] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7543)) - off;
-    }
-}
-
-// 2^23 + 128 + zp: subtracting it from the permuted code gives q - zp exactly.
-__device__ __forceinline__ float code_offset(int32_t zp) { return 8388736.0f + (float)zp; }
 
 template <typename T>
 __device__ __forceinline__ float dot16(const T* xr, const float (&t)[16]) {
@@ -206,8 +191,8 @@ ffn_up_stream_i8(const T* __restrict__ x, const int8_t* __restrict__ wq,
         const int off = offsets[e];
         const int8_t* g_row = wq + gu_row(e, n, 0, f) * d;
         const int8_t* u_row = wq + gu_row(e, n, 1, f) * d;
-        const size_t gb = ((size_t)(2 * e) * (f / 64) + n / 64) * nkb;   // gate block row
-        const size_t ub = ((size_t)(2 * e + 1) * (f / 64) + n / 64) * nkb;
+        const size_t gb = (gu_row(e, n, 0, f) >> 6) * nkb;   // gate block row
+        const size_t ub = (gu_row(e, n, 1, f) >> 6) * nkb;
         for (int s0 = 0; s0 < c; s0 += kSlots) {
             const int ns = min(kSlots, c - s0);
             const T* xr[kSlots];
@@ -273,7 +258,7 @@ ffn_down_stream_i8(const T* __restrict__ H, const int8_t* __restrict__ wq,
         if (c == 0) continue;
         const int off = offsets[e];
         const int8_t* w_row = wq + ((size_t)e * d + col) * f;
-        const size_t bb = ((size_t)e * (d / 64) + col / 64) * nkb;
+        const size_t bb ((((size_t)e * d + col) >> 6) * nkb);
         for (int s0 = 0; s0 < c; s0 += kSlots) {
             const int ns = min(kSlots, c - s0);
             float acc[kSlots];

@@ -58,6 +58,21 @@ template <bool kPair> struct Ring {
     static constexpr uint32_t kStageB = (kPair ? 128 : 256) * 64 * 2;
 };
 constexpr int kThreads = 192;
+// Int8 B operand (single CTAs).  Three rings: 5 stages of int8 B codes
+// (256 x 64 bytes, 16 KB) fed by TMA from warp 0 and released by the
+// converters as soon as they are read; 3 stages of A (16 KB) fed by TMA from
+// warp 14 and released by the MMA; 2 stages of dequantised f16 B (32 KB,
+// 128-byte swizzle) written by 8 converter warps (warps 6-13) and released by
+// the MMA.  The codes, the only HBM stream at decode sizes, thus turn over
+// without waiting for the tensor core.
+constexpr int kConvWarps = 8;
+constexpr int kAWarp = 6 + kConvWarps;                  // 14: A producer
+constexpr int kThreadsI8 = (kAWarp + 1) * 32;           // 480
+constexpr int kQStages = 5;
+constexpr int kAStagesI8 = 3;
+constexpr int kBStages = 2;
+constexpr uint32_t kStageQ = 256 * 64;        // int8 codes of one B stage
+constexpr uint32_t kStageBf = 256 * 64 * 2;   // the same stage in bf16
 constexpr uint32_t kRingBytes = 192 * 1024;   // shared-memory ring of every instantiation
 // Per epilogue warp, a 32-row tile of one 32-column accumulator chunk in
 // shared memory (rows padded to 36 floats): the warp turns its 32 per-thread
@@ -311,6 +326,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
+// The same with A and B f16 (format 0 in bits 7-9 and 10-12).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Two floats as the 16-bit H element pair: bf16, or f16 for the int8-weight
+// GEMMs (whose A operands are f16).
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    if constexpr (kF16) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
 
 // ---------------------------------------------------------------- work decode
 
@@ -369,6 +401,7 @@ __device__ __forceinline__ Work get_work(int w, const TcGemmArgs& a) {
 // slices in slice order (so the sum does not depend on arrival order), applies
 // SiLU(G)*U and writes the tile's H rows, then rearms the counter.  Nothing
 // waits on another CTA.
+template <bool kF16>
 __device__ __noinline__ void gate_up_split_fixup(const TcGemmArgs& args, const Work& wk, int lane) {
     __threadfence();
     __syncwarp();
@@ -379,7 +412,7 @@ __device__ __noinline__ void gate_up_split_fixup(const TcGemmArgs& args, const W
     if (old != 4 * args.k_splits - 1) return;
     __threadfence();
     const int pld = args.n_blocks * 256;
-    __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
+    uint16_t* H = reinterpret_cast<uint16_t*>(args.out);
     for (int r = 0; r < wk.rows; ++r) {
         const size_t prow = (size_t)(wk.row0 + r) * pld + (size_t)wk.nblk * 256;
         float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
@@ -390,11 +423,9 @@ __device__ __noinline__ void gate_up_split_fixup(const TcGemmArgs& args, const W
             g[0] += gs.x, g[1] += gs.y, g[2] += gs.z, g[3] += gs.w;
             u[0] += us.x, u[1] += us.y, u[2] += us.z, u[3] += us.w;
         }
-        __nv_bfloat162 h01 = __floats2bfloat162_rn(silu(g[0]) * u[0], silu(g[1]) * u[1]);
-        __nv_bfloat162 h23 = __floats2bfloat162_rn(silu(g[2]) * u[2], silu(g[3]) * u[3]);
         uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&h01);
-        pk.y = *reinterpret_cast<uint32_t*>(&h23);
+        pk.x = pack_h2<kF16>(silu(g[0]) * u[0], silu(g[1]) * u[1]);
+        pk.y = pack_h2<kF16>(silu(g[2]) * u[2], silu(g[3]) * u[3]);
         *reinterpret_cast<uint2*>(H + (size_t)(wk.row0 + r) * args.out_ld + wk.nblk * 128 + lane * 4) = pk;
     }
     if (lane == 0) *ctr = 0;   // rearmed for the next launch
@@ -402,30 +433,61 @@ __device__ __noinline__ void gate_up_split_fixup(const TcGemmArgs& args, const W
 
 // ---------------------------------------------------------------- the kernel
 
-template <int kMode, bool kPair>
-__global__ void __launch_bounds__(kThreads, 1)
+// Dequantise one stage of int8 B codes (256 rows x 64, row-major, 64-byte
+// rows) into the f16 128-byte-swizzled layout the MMA reads (16-byte chunk j
+// of row r at chunk j ^ (r & 7), as TMA would have written it).  Converter
+// thread ct (0..255) takes the 16-byte code chunks ct + 256 j, j = 0..3: row
+// ct/4 + 64 j (64-row block j), chunk ct % 4.  off2[j] = 1152 + zp and s2[j] =
+// scale of block j, as half2.
+__device__ __forceinline__ void convert_stage(const uint8_t* __restrict__ sq, uint8_t* __restrict__ sb,
+                                              int ct, const __half2 (&off2)[4], const __half2 (&s2)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int id = ct + 256 * j;
+        const int r = id >> 2, c = id & 3;
+        const uint4 v = *reinterpret_cast<const uint4*>(sq + r * 64 + c * 16);
+        uint4 lo, hi;
+        dequant16_h2(v, off2[j], s2[j], lo, hi);
+        uint8_t* row = sb + r * 128;
+        *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = hi;
+    }
+}
+
+template <int kMode, bool kPair, bool kI8>
+__global__ void __launch_bounds__(kI8 ? kThreadsI8 : kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 TcGemmArgs args) {
+    static_assert(!kI8 || (!kPair && kMode != kRouter), "int8 B: single-CTA expert GEMMs only");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     // The router's B tile is only E_pad rows: its ring is as deep as fits
     // (up to kMaxRouterStages) in the same bytes; the expert GEMMs use Ring.
-    constexpr int kMaxSt = kMode == kRouter ? kMaxRouterStages : Ring<kPair>::kStages;
-    const uint32_t kStageB = kMode == kRouter ? (uint32_t)args.bn_rows * kBK * 2 : Ring<kPair>::kStageB;
+    constexpr int kMaxSt = kMode == kRouter ? kMaxRouterStages : kI8 ? kQStages : Ring<kPair>::kStages;
+    // Bytes per stage of the TMA-fed B tile (int8 codes for kI8).
+    const uint32_t kStageB = kMode == kRouter ? (uint32_t)args.bn_rows * kBK * 2
+                             : kI8            ? kStageQ
+                                              : Ring<kPair>::kStageB;
     const int kStages = kMode == kRouter
                             ? min(kMaxRouterStages, (int)(kRingBytes / (kStageA + kStageB)))
-                            : Ring<kPair>::kStages;
+                            : kMaxSt;
+    // kI8: [A x 3][codes x 5][f16 B x 2]; otherwise [A x kStages][B x kStages]
     uint8_t* stage_a = smem;
-    uint8_t* stage_b = smem + kStages * kStageA;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * (kStageA + kStageB));
+    uint8_t* stage_b = smem + (kI8 ? kAStagesI8 : kStages) * kStageA;
+    uint8_t* stage_bf = stage_b + kStages * kStageB;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage_bf + (kI8 ? kBStages * kStageBf : 0));
     uint64_t* full = bars;                 // [kStages]
     uint64_t* empty = bars + kStages;      // [kStages]
     uint64_t* acc_full = bars + 2 * kStages;     // [2]
     uint64_t* acc_empty = bars + 2 * kStages + 2;  // [2]
     uint64_t* mma_done = bars + 2 * kStages + 4;   // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+    uint64_t* bf_full = bars + 2 * kStages + 5;    // [kBStages] kI8: converted B ready
+    uint64_t* bf_empty = bars + 2 * kStages + 7;   // [kBStages] kI8: converted B consumed
+    uint64_t* a_full = bars + 2 * kStages + 9;     // [kAStagesI8] kI8: A landed
+    uint64_t* a_empty = bars + 2 * kStages + 12;   // [kAStagesI8] kI8: A consumed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 15);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -440,7 +502,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // Rows of B this CTA loads per stage (= MMA N, or half of it for a pair).
     const int bn = kMode == kRouter ? args.bn_rows : kBN;
     const int b_rows_cta = kPair ? bn / 2 : bn;
-    const uint32_t cta_tx = kStageA + (uint32_t)b_rows_cta * kBK * 2;
+    const uint32_t cta_tx = kI8 ? kStageQ : kStageA + (uint32_t)b_rows_cta * kBK * 2;
     const uint32_t stage_tx = kPair ? 2 * cta_tx : cta_tx;   // bytes landing on `full`
     const int kb_per_split = (args.k_blocks + args.k_splits - 1) / args.k_splits;
     const uint64_t limit = args.wait_limit_ns;
@@ -448,7 +510,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), 1);
+            // kI8: a code stage is released by every converter warp
+            mbar_init(smem_u32(&empty[s]), kI8 ? kConvWarps : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&acc_full[a]), 1);
@@ -456,6 +519,16 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(smem_u32(&acc_empty[a]), kPair ? 8 : 4);
         }
         mbar_init(smem_u32(&mma_done[0]), 1);
+        if constexpr (kI8) {
+            for (int b = 0; b < kBStages; ++b) {
+                mbar_init(smem_u32(&bf_full[b]), kConvWarps);
+                mbar_init(smem_u32(&bf_empty[b]), 1);
+            }
+            for (int a = 0; a < kAStagesI8; ++a) {
+                mbar_init(smem_u32(&a_full[a]), 1);
+                mbar_init(smem_u32(&a_empty[a]), 1);
+            }
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -503,6 +576,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         const uint32_t fb = map_to_rank(fb_local, 0);
                         tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
                         tma_load_2d_pair(sb, &tmB, kb * kBK, b_row, fb);
+                    } else if constexpr (kI8) {
+                        // int8 codes only; warp 14 loads A into its own ring
+                        (void)sa;
+                        (void)a_row;
+                        tma_load_2d(sb, &tmB, kb * kBK, b_row, fb_local);
                     } else {
                         tma_load_2d(sa, &tmA, kb * kBK, a_row, fb_local);
                         tma_load_2d(sb, &tmB, kb * kBK, b_row, fb_local);
@@ -523,9 +601,13 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (leader)
         if (lane == 0 && leader) {
-            const uint32_t idesc = idesc_bf16(kPair ? 2 * kBM : kBM, bn);
+            // int8 B: A (Xp / H) and the dequantised B are f16
+            const uint32_t idesc =
+                kI8 ? idesc_f16(kBM, bn) : idesc_bf16(kPair ? 2 * kBM : kBM, bn);
             int stage = 0;
             uint32_t phase = 0;
+            int bs = 0;              // kI8: converted-B stage
+            uint32_t bphase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int w = unit; w < total && !*abort_flag; w += n_units) {
@@ -539,21 +621,37 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.status,
-                                   limit)) {
+                    // kI8: A from its own ring (`stage` counts A stages), B
+                    // from the converters' f16 ring
+                    const bool got =
+                        kI8 ? mbar_wait(smem_u32(&bf_full[bs]), bphase, abort_flag, args.status,
+                                        limit) &&
+                                  mbar_wait(smem_u32(&a_full[stage]), phase, abort_flag,
+                                            args.status, limit)
+                            : mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.status,
+                                        limit);
+                    if (!got) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t da = smem_desc_sw128(smem_u32(stage_a + stage * kStageA));
-                    const uint64_t db = smem_desc_sw128(smem_u32(stage_b + stage * kStageB));
+                    const uint64_t db = smem_desc_sw128(
+                        smem_u32(kI8 ? stage_bf + bs * kStageBf : stage_b + stage * kStageB));
 #pragma unroll
                     for (int ks = 0; ks < kBK / 16; ++ks)
                         // +32 bytes of K per step inside the swizzle atom (encoded >> 4)
                         mma_bf16<kPair>(d_tmem, da + 2 * ks, db + 2 * ks, idesc,
                                         (kb > kb0) || ks != 0);
-                    mma_commit<kPair>(smem_u32(&empty[stage]));
-                    if (++stage == kStages) stage = 0, phase ^= 1;
+                    if constexpr (kI8) {
+                        mma_commit<kPair>(smem_u32(&a_empty[stage]));
+                        mma_commit<kPair>(smem_u32(&bf_empty[bs]));
+                        if (++stage == kAStagesI8) stage = 0, phase ^= 1;
+                        if (++bs == kBStages) bs = 0, bphase ^= 1;
+                    } else {
+                        mma_commit<kPair>(smem_u32(&empty[stage]));
+                        if (++stage == kStages) stage = 0, phase ^= 1;
+                    }
                 }
                 if (!ok) break;
                 mma_commit<kPair>(smem_u32(&acc_full[acc]));
@@ -564,7 +662,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_wait_drain(smem_u32(&mma_done[0]), 0, kDrainLimitNs);
         }
         __syncwarp();
-    } else {
+    } else if (!kI8 || warp < 6) {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;       // row of this CTA's 128-row half
@@ -662,7 +760,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // H = silu(G) * U for this thread's row, 32 columns per chunk,
                 // stored straight from registers: each row's 64 bytes are two
                 // whole sectors, so staging them buys nothing here.
-                __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out);
+                uint16_t* H = reinterpret_cast<uint16_t*>(args.out);
 #pragma unroll 1
                 for (int c = 0; c < 128 / 32; ++c) {
                     uint32_t g[32], u[32];
@@ -677,8 +775,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                             const float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
                             const float h1 =
                                 silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
-                            pw[i] = *reinterpret_cast<uint32_t*>(&b2);
+                            pw[i] = pack_h2<kI8>(h0, h1);
                         }
                         uint4* dst = reinterpret_cast<uint4*>(H + orow * args.out_ld +
                                                               wk.nblk * 128 + c * 32);
@@ -724,9 +821,105 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 else mbar_arrive(ae);
             }
             if constexpr (kMode == kGateUp) {
-                if (args.k_splits > 1) gate_up_split_fixup(args, wk, lane);
+                if (args.k_splits > 1) gate_up_split_fixup<kI8>(args, wk, lane);
             }
             if (++acc == 2) acc = 0, acc_phase ^= 1;
+        }
+    } else if (kI8 && warp == kAWarp) {
+        // ------------------------------------------------ A producer (kI8)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool issued[kAStagesI8];
+            uint32_t issued_phase[kAStagesI8];
+            for (int s = 0; s < kAStagesI8; ++s) issued[s] = false, issued_phase[s] = 0;
+            for (int w = unit; w < total && !*abort_flag && !args.stall_producer; w += n_units) {
+                const Work wk = get_work<kMode>(w, args);
+                const int kb0 = wk.split * kb_per_split;
+                const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
+                bool ok = true;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(smem_u32(&a_empty[stage]), phase ^ 1, abort_flag, args.status,
+                                   limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t ab = smem_u32(&a_full[stage]);
+                    mbar_expect_tx(ab, kStageA);
+                    tma_load_2d(smem_u32(stage_a + stage * kStageA), &tmA, kb * kBK, wk.row0, ab);
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == kAStagesI8) stage = 0, phase ^= 1;
+                }
+                if (!ok) break;
+            }
+            for (int s = 0; s < kAStagesI8; ++s)
+                if (issued[s]) mbar_wait_drain(smem_u32(&a_full[s]), issued_phase[s], kDrainLimitNs);
+        }
+        __syncwarp();
+    } else if constexpr (kI8) {
+        // ------------------------------------------------ converters (warps 6..13)
+        // Walk the same k-blocks as the producers and the MMA issuer: wait for
+        // the stage's codes to land and for a free f16 B stage, dequantise
+        // with the 64-row blocks' scales and zero points, release the codes,
+        // make the stores visible to the tensor core's proxy, and count the
+        // warp in.
+        const int ct = threadIdx.x - 6 * 32;
+        int stage = 0;
+        uint32_t phase = 0;
+        int bs = 0;
+        uint32_t bphase = 0;
+        for (int w = unit; w < total && !*abort_flag; w += n_units) {
+            const Work wk = get_work<kMode>(w, args);
+            const int kb0 = wk.split * kb_per_split;
+            const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
+            // first packed B row of the tile; a multiple of 64 (one block row)
+            const int rb0 = (wk.expert * args.b_rows_per_expert + wk.nblk * kBN) >> 6;
+            const float* sc_row = args.q_scale + (size_t)rb0 * args.k_blocks;
+            const int32_t* zp_row = args.q_zp + (size_t)rb0 * args.k_blocks;
+            // The four 64-row blocks' scale and zero point of k-block kb; the
+            // next k-block's are loaded one stage ahead, so that their L2
+            // latency hides behind a conversion.
+            float scl[4], zpf[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                scl[j] = __ldg(sc_row + (size_t)j * args.k_blocks + kb0);
+                zpf[j] = (float)__ldg(zp_row + (size_t)j * args.k_blocks + kb0);
+            }
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                float nscl[4], nzpf[4];
+                const int kn = kb + 1 < kb1 ? kb + 1 : kb;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    nscl[j] = __ldg(sc_row + (size_t)j * args.k_blocks + kn);
+                    nzpf[j] = (float)__ldg(zp_row + (size_t)j * args.k_blocks + kn);
+                }
+                const bool got =
+                    mbar_wait(smem_u32(&full[stage]), phase, abort_flag, args.status, limit) &&
+                    mbar_wait(smem_u32(&bf_empty[bs]), bphase ^ 1, abort_flag, args.status, limit);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                __half2 off2[4], s2[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    off2[j] = __float2half2_rn(1152.0f + zpf[j]);   // exact: an integer < 2048
+                    s2[j] = __float2half2_rn(scl[j]);
+                }
+                convert_stage(stage_b + stage * kStageB, stage_bf + bs * kStageBf, ct, off2, s2);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));   // codes read
+#pragma unroll
+                for (int j = 0; j < 4; ++j) scl[j] = nscl[j], zpf[j] = nzpf[j];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bf_full[bs]));
+                if (++stage == kStages) stage = 0, phase ^= 1;
+                if (++bs == kBStages) bs = 0, bphase ^= 1;
+            }
+            if (!ok) break;
         }
     }
 
@@ -766,31 +959,48 @@ size_t tc_gemm_smem_bytes() {
 int tc_gemm_block_m() { return kBM; }
 int tc_gemm_pair_rows() { return 2 * kBM; }
 
-// Tensor map of a row-major bf16 matrix [rows, cols] with a box of
+// Tensor map of a row-major bf16 (or f16) matrix [rows, cols] with a box of
 // 64 columns x box_rows rows, 128-byte swizzle, zero fill out of bounds.
+// Tensor map of a row-major int8 matrix [rows, cols] with a box of
+// 64 columns x box_rows rows (64-byte rows, no swizzle), zero fill.
+bool make_tmap_i8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                    uint32_t box_rows) {
+                    uint32_t box_rows, bool f16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+    return fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+              const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kMode, bool kPair>
+template <int kMode, bool kPair, bool kI8 = false>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcGemmArgs& args,
                        int grid, cudaStream_t s) {
     const size_t smem = tc_gemm_smem_bytes();
-    auto k = grouped_gemm_tc<kMode, kPair>;
+    auto k = grouped_gemm_tc<kMode, kPair, kI8>;
     smem_attr((const void*)k, (int)smem);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kI8 ? kThreadsI8 : kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -806,12 +1016,21 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcG
 }
 
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const TcGemmArgs& args, int grid, cudaStream_t s) {
+                           const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b) {
     if (grid <= 0) return cudaSuccess;
     // the split gate/up fixup counts the four epilogue warps of one CTA per slice
     if (mode == kGateUp && args.k_splits > 1 && (pair || !args.partial || !args.tile_counter))
         return cudaErrorInvalidValue;
     cudaError_t e;
+    if (int8_b) {
+        // B rows are read in 64-row blocks of scales: tiles of 256 rows, single CTAs
+        if (pair || mode == kRouter || !args.q_scale || !args.q_zp || args.b_rows_per_expert % 64)
+            return cudaErrorInvalidValue;
+        e = mode == kGateUp ? launch_one<kGateUp, false, true>(tmA, tmB, args, grid, s)
+                            : launch_one<kDown, false, true>(tmA, tmB, args, grid, s);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     if (mode == kGateUp)
         e = pair ? launch_one<kGateUp, true>(tmA, tmB, args, grid & ~1, s)
                  : launch_one<kGateUp, false>(tmA, tmB, args, grid, s);
@@ -839,7 +1058,7 @@ int tc_gemm_max_pairs() {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        auto k = grouped_gemm_tc<kGateUp, true>;
+        auto k = grouped_gemm_tc<kGateUp, true, false>;
         smem_attr((const void*)k, (int)tc_gemm_smem_bytes());
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) n = 0;

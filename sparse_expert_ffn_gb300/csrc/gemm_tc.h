@@ -37,6 +37,10 @@ struct TcGemmArgs {
     const float* bias;           // [E] or null
     int32_t* topk_idx;           // [T, k]
     float* topk_w;               // [T, k]
+    // int8 B (launch_tc_gemm with int8_b): block scales and zero points per
+    // 64 packed B rows, [B rows / 64][k_blocks]
+    const float* q_scale;
+    const int32_t* q_zp;
     int stall_producer;          // failure-detection tests only: issue no TMA copy, so
                                  // the first wait on a full stage runs out its bound
 };
@@ -46,10 +50,15 @@ int tc_gemm_block_m();
 int tc_gemm_pair_rows();     // rows of one expert tile of a CTA pair (256)
 int tc_gemm_max_pairs();     // CTA pairs resident at once (0 if unknown)
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                    uint32_t box_rows);
+                    uint32_t box_rows, bool f16 = false);
+bool make_tmap_i8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows);
 // pair: run the expert GEMMs on CTA pairs (256-row tiles, B tensor map with
 // 128-row boxes) instead of single CTAs (128-row tiles, 256-row B boxes).
+// int8_b: B is int8 codes (tmB from make_tmap_i8, 256-row boxes) dequantised
+// to f16 in shared memory by converter warps; A (Xp, H) is f16 and H is
+// written as f16; single CTAs, kGateUp / kDown only.
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const TcGemmArgs& args, int grid, cudaStream_t s);
+                           const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b = false);
 
 }  // namespace colibri

@@ -43,8 +43,7 @@ struct colibri_moe {
     void* wgu = nullptr;    // [E][f/128][2][128][d]
     void* wdT = nullptr;    // [E][d][f]
     // int8 expert weights (colibri_init_int8): codes in the same packed
-    // layouts, block scales / zero points of gate+up [E][2][f/64][d/64] and
-    // of down [E][d/64][f/64]
+    // layouts, block scales / zero points per 64 packed rows, [rows / 64][K / 64]
     bool int8 = false;
     int8_t* q_gu = nullptr;
     int8_t* q_d = nullptr;
@@ -298,7 +297,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     // Expert GEMMs on CTA pairs (256-row tiles) once the batch averages 128
     // rows per expert; below that most tile rows would be empty and single
     // CTAs (128-row tiles) stream the weights faster.
-    const bool pair = ex == COLIBRI_EXEC_GROUPED && npairs >= 128 * E;
+    const bool pair = ex == COLIBRI_EXEC_GROUPED && npairs >= 128 * E && !h->int8;
     const int tile_rows = pair ? tc_gemm_pair_rows() : tc_gemm_block_m();
     // Small batch: router, top-k, softmax, dispatch and gather in one CTA.
     const bool fused_routing = route_small_fits(T, d, E, k);
@@ -316,7 +315,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
                                        tile_rows, h->tile_expert, h->tile_row, h->tile_info,
                                        h->num_tiles, h->status, cap, h->kept,
                                        ex == COLIBRI_EXEC_GROUPED ? h->xp : nullptr, gamma, eps,
-                                       h->u, s), 1);
+                                       h->u, s, h->int8), 1);
         if (st != COLIBRI_OK) return st;
         if (gamma) x = h->u;
     } else if (h->grouped_ok && T >= kTcRouterMinTokens) {
@@ -398,7 +397,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             // boxes of 128 consecutive rows read it far faster than per-row
             // gathers inside the GEMM
             Stage g(h, COLIBRI_STAGE_GATHER, s);
-            st = g.done(launch_gather(h->esz, x, h->perm, k, d, npairs, h->xp, s), 1);
+            st = g.done(launch_gather(h->esz, x, h->perm, k, d, npairs, h->xp, s, h->int8), 1);
             if (st != COLIBRI_OK) return st;
         }
         TcGemmArgs a{};
@@ -422,6 +421,8 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.b_rows_per_expert = 2 * f;
         a.out = h->H;
         a.out_ld = f;
+        a.q_scale = h->sc_gu;
+        a.q_zp = h->zp_gu;
         if (!pair && npairs <= kGateUpSplitMaxPairs) {
             const int fit = (int)std::min<size_t>(kMaxKSplit, h->y_floats / ((size_t)npairs * 2 * f));
             a.k_splits = choose_k_splits(tiles_est * a.n_blocks, a.k_blocks, units, fit);
@@ -434,7 +435,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
                                                     (int64_t)tiles_ub * a.n_blocks * a.k_splits, units);
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
             st = g.done(launch_tc_gemm(kGateUp, pair, h->tm_xp, pair ? h->tm_wgu : h->tm_wgu1, a,
-                                       grid, s), 1);
+                                       grid, s, h->int8), 1);
             if (st != COLIBRI_OK) return st;
         }
         // down: N = d in blocks of 256, K = f.  Few pairs leave too few
@@ -445,6 +446,8 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.b_rows_per_expert = d;
         a.out = h->Y;
         a.out_ld = d;
+        a.q_scale = h->sc_d;
+        a.q_zp = h->zp_d;
         a.k_splits = 1;
         a.partial = nullptr;
         a.partial_split_stride = 0;
@@ -459,7 +462,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
                                                     (int64_t)tiles_ub * a.n_blocks * a.k_splits, units);
             Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
             st = g.done(launch_tc_gemm(kDown, pair, h->tm_h, pair ? h->tm_wdT : h->tm_wdT1, a, grid,
-                                       s), 1);
+                                       s, h->int8), 1);
             if (st != COLIBRI_OK) return st;
         }
         nsplit = a.k_splits;
@@ -512,7 +515,6 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
         if (!qu || !qd) return COLIBRI_ERR_INVALID_ARG;
         for (const colibri_int8_weights_t* w : {qg, qu, qd})
             if (!w->q || !w->scale || !w->zp) return COLIBRI_ERR_INVALID_ARG;
-        if (cfg->executor == COLIBRI_EXEC_GROUPED) return COLIBRI_ERR_UNSUPPORTED;
     } else if (!w_gate || !w_up || !w_down) {
         return COLIBRI_ERR_INVALID_ARG;
     }
@@ -609,14 +611,15 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
             st = pack(1, qu->q, dev, h->q_gu, E, d, f, (size_t)2 * f * d, 128, 256, 1, staging);
         if (st == COLIBRI_OK)
             st = pack(1, qd->q, dev, h->q_d, E, f, d, (size_t)d * f, d, d, 0, staging);
-        // block scales and zero points: gate/up [E][d/64][f/64] -> [E][2][f/64][d/64],
-        // down [E][f/64][d/64] -> [E][d/64][f/64]
+        // block scales and zero points, one row per 64 packed weight rows:
+        // gate/up [E][d/64][f/64] -> [E][f/128][2][2][d/64] (two 64-row blocks
+        // of each 128-row gate or up slab), down [E][f/64][d/64] -> [E][d/64][f/64]
         const int bd = d / 64, bf = f / 64;
         const colibri_int8_weights_t* gu[2] = {qg, qu};
         for (int w = 0; w < 2 && st == COLIBRI_OK; ++w) {
-            st = pack(4, gu[w]->scale, dev, h->sc_gu, E, bd, bf, 2 * nblk, bf, 2 * bf, w, staging);
+            st = pack(4, gu[w]->scale, dev, h->sc_gu, E, bd, bf, 2 * nblk, 2, 4, w, staging);
             if (st == COLIBRI_OK)
-                st = pack(4, gu[w]->zp, dev, h->zp_gu, E, bd, bf, 2 * nblk, bf, 2 * bf, w, staging);
+                st = pack(4, gu[w]->zp, dev, h->zp_gu, E, bd, bf, 2 * nblk, 2, 4, w, staging);
         }
         if (st == COLIBRI_OK) st = pack(4, qd->scale, dev, h->sc_d, E, bf, bd, nblk, bd, bd, 0, staging);
         if (st == COLIBRI_OK) st = pack(4, qd->zp, dev, h->zp_d, E, bf, bd, nblk, bd, bd, 0, staging);
@@ -630,7 +633,7 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
     const int M = cfg->max_tokens;
     h->max_pairs = M * k;
     h->max_tiles = (h->max_pairs + tc_gemm_block_m() - 1) / tc_gemm_block_m() + std::min(E, h->max_pairs);
-    h->grouped_ok = !int8 && grouped_shape_ok(*cfg);
+    h->grouped_ok = grouped_shape_ok(*cfg);
     if (cfg->executor == COLIBRI_EXEC_GROUPED && !h->grouped_ok) return fail(COLIBRI_ERR_UNSUPPORTED);
     const size_t P = (size_t)h->max_pairs;
     // Y: the down projection's float32 rows, or up to 8 K slices of them for
@@ -685,13 +688,19 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
     if ((st = from_cuda(cudaMemset(h->ws, 0, off))) != COLIBRI_OK) return fail(st);
 
     if (h->grouped_ok) {
-        bool ok = make_tmap_bf16(&h->tm_xp, h->xp, P, d, 128) &&
-                  make_tmap_bf16(&h->tm_wgu, h->wgu, (uint64_t)E * 2 * f, d, 128) &&
-                  make_tmap_bf16(&h->tm_h, h->H, P, f, 128) &&
-                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 128) &&
-                  make_tmap_bf16(&h->tm_wgu1, h->wgu, (uint64_t)E * 2 * f, d, 256) &&
-                  make_tmap_bf16(&h->tm_wdT1, h->wdT, (uint64_t)E * d, f, 256) &&
+        // int8 handles: single-CTA tiles only, B maps over the int8 codes
+        // int8 weights: Xp and H are f16 (the A type of the int8-weight GEMMs)
+        bool ok = make_tmap_bf16(&h->tm_xp, h->xp, P, d, 128, int8) &&
+                  make_tmap_bf16(&h->tm_h, h->H, P, f, 128, int8) &&
                   make_tmap_bf16(&h->tm_wr, h->wr, (uint64_t)h->e_pad, d, (uint32_t)h->e_pad);
+        if (int8)
+            ok = ok && make_tmap_i8(&h->tm_wgu1, h->q_gu, (uint64_t)E * 2 * f, d, 256) &&
+                 make_tmap_i8(&h->tm_wdT1, h->q_d, (uint64_t)E * d, f, 256);
+        else
+            ok = ok && make_tmap_bf16(&h->tm_wgu, h->wgu, (uint64_t)E * 2 * f, d, 128) &&
+                 make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 128) &&
+                 make_tmap_bf16(&h->tm_wgu1, h->wgu, (uint64_t)E * 2 * f, d, 256) &&
+                 make_tmap_bf16(&h->tm_wdT1, h->wdT, (uint64_t)E * d, f, 256);
         if (!ok) {
             if (cfg->executor == COLIBRI_EXEC_GROUPED) return fail(COLIBRI_ERR_CUDA);
             h->grouped_ok = false;

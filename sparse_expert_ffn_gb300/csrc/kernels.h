@@ -43,7 +43,7 @@ cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const fl
                                int bm, int32_t* tile_expert, int32_t* tile_row,
                                int32_t* tile_info, int32_t* num_tiles, int* status, int cap,
                                int32_t* kept, void* xp, const void* gamma, float eps, void* u,
-                               cudaStream_t s);
+                               cudaStream_t s, bool xp_f16 = false);
 
 // `kept` = pairs each expert accepted (its first kept[e] segment rows).
 cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* kept,
@@ -53,7 +53,7 @@ cudaError_t launch_ffn_down_stream(DType dt, const void* H, const void* wdT, con
                                    const int32_t* offsets, int d, int f, int E, float* Y,
                                    cudaStream_t s);
 // Int8-weight variants (64x64 blocks, w = (q - zp) * scale); scales and zero
-// points of gate/up [E][2][f/64][d/64], of down [E][d/64][f/64].
+// points per 64-row block of the packed weight rows, [packed row / 64][K / 64].
 cudaError_t launch_ffn_up_stream_i8(DType dt, const void* x, const int8_t* wq, const float* sc,
                                     const int32_t* zp, const int32_t* kept,
                                     const int32_t* offsets, const int32_t* perm, int k, int d,
@@ -64,7 +64,7 @@ cudaError_t launch_ffn_down_stream_i8(DType dt, const void* H, const int8_t* wq,
                                       cudaStream_t s);
 
 cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,
-                          int npairs, void* xp, cudaStream_t s);
+                          int npairs, void* xp, cudaStream_t s, bool to_f16 = false);
 cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const int32_t* inv,
                            int T, int k, int d, int nsplit, size_t split_stride,
                            const void* resid, void* y, cudaStream_t s);

@@ -11,7 +11,9 @@ namespace {
 
 // Xp[p, :] = x[perm[p] / k, :] — the tokens of every expert as consecutive
 // rows (the A operand of the grouped GEMM).  One CTA per pair row, 16-byte
-// vectors.
+// vectors; with kToF16, bf16 rows are converted to f16 (the A type of the
+// int8-weight GEMMs).
+template <bool kToF16>
 __global__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k,
                             int row_vecs, uint4* __restrict__ xp) {
     pdl_enter();
@@ -19,7 +21,8 @@ __global__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restri
     const int t = perm[p] / k;
     const uint4* src = x + (size_t)t * row_vecs;
     uint4* dst = xp + (size_t)p * row_vecs;
-    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x) dst[i] = src[i];
+    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x)
+        dst[i] = kToF16 ? bf16x8_to_f16x8(src[i]) : src[i];
 }
 
 // Combine: y[t, c] = sum_j w[t, j] * Y[inv[t*k + j], c], j in order, float32;
@@ -109,11 +112,14 @@ __global__ void transpose_remap(const E* __restrict__ in, E* __restrict__ out, i
 }  // namespace
 
 cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,
-                          int npairs, void* xp, cudaStream_t s) {
+                          int npairs, void* xp, cudaStream_t s, bool to_f16) {
     if (npairs <= 0) return cudaSuccess;
     const int row_vecs = d * elem_bytes / 16;
     const cudaError_t e =
-        launch_pdl(gather_rows, npairs, 128, 0, s, (const uint4*)x, perm, k, row_vecs, (uint4*)xp);
+        to_f16 ? launch_pdl(gather_rows<true>, npairs, 128, 0, s, (const uint4*)x, perm, k, row_vecs,
+                            (uint4*)xp)
+               : launch_pdl(gather_rows<false>, npairs, 128, 0, s, (const uint4*)x, perm, k,
+                            row_vecs, (uint4*)xp);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

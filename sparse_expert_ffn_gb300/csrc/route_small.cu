@@ -10,7 +10,8 @@
 //      each cut into d slices so that all 32 warps work, into shared memory
 //   2. top-k + softmax: warp w routes tokens w, w + 32, ...
 //   3. dispatch_block: the same deterministic counting sort as the dispatch kernel
-//   4. gather: Xp[p] = x[perm[p] / k] with 16-byte vectors.
+//   4. gather: Xp[p] = x[perm[p] / k] with 16-byte vectors (converted to
+//      f16 for the int8-weight GEMMs).
 // For a pre-norm layer it first normalises the token rows (RMSNorm * gamma)
 // into u and routes u.
 #include "common.cuh"
@@ -32,7 +33,7 @@ route_small_kernel(const T* __restrict__ x, const T* __restrict__ wr,
                    int32_t* __restrict__ tile_info, int32_t* __restrict__ num_tiles,
                    int* __restrict__ status, int cap, int32_t* __restrict__ kept,
                    uint4* __restrict__ xp, int nq, const T* __restrict__ gamma, float eps,
-                   T* __restrict__ u) {
+                   T* __restrict__ u, int xp_f16) {
     pdl_enter();
     extern __shared__ int32_t sh[];
     float* logit = reinterpret_cast<float*>(sh);                 // [ntok][E]
@@ -88,7 +89,8 @@ route_small_kernel(const T* __restrict__ x, const T* __restrict__ wr,
         const uint4* xs = reinterpret_cast<const uint4*>(src);
         for (int i = threadIdx.x; i < ntok * k * vecs; i += blockDim.x) {
             const int p = i / vecs, v = i - p * vecs;
-            xp[(size_t)p * vecs + v] = __ldcg(xs + (size_t)(perm[p] / k) * vecs + v);
+            const uint4 val = __ldcg(xs + (size_t)(perm[p] / k) * vecs + v);
+            xp[(size_t)p * vecs + v] = xp_f16 ? bf16x8_to_f16x8(val) : val;
         }
     }
 }
@@ -117,7 +119,7 @@ cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const fl
                                int bm, int32_t* tile_expert, int32_t* tile_row,
                                int32_t* tile_info, int32_t* num_tiles, int* status, int cap,
                                int32_t* kept, void* xp, const void* gamma, float eps, void* u,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool xp_f16) {
     const int nq = slices_for(ntok, E, d);
     const size_t smem = (size_t)((ntok * E + 63) & ~63) * 4 +
                         (size_t)((ntok * E * nq + 63) & ~63) * 4 + dispatch_smem_bytes(E);
@@ -129,14 +131,14 @@ cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const fl
         e = launch_pdl(kern, 1, block, smem, s, (const __nv_bfloat16*)x, (const __nv_bfloat16*)wr,
                        bias, ntok, d, E, k, topk_idx, topk_w, counts, offsets, perm, inv, bm,
                        tile_expert, tile_row, tile_info, num_tiles, status, cap, kept, (uint4*)xp,
-                       nq, (const __nv_bfloat16*)gamma, eps, (__nv_bfloat16*)u);
+                       nq, (const __nv_bfloat16*)gamma, eps, (__nv_bfloat16*)u, xp_f16 ? 1 : 0);
     } else {
         auto kern = route_small_kernel<float>;
         smem_attr((const void*)kern, (int)smem);
         e = launch_pdl(kern, 1, block, smem, s, (const float*)x, (const float*)wr, bias, ntok, d, E,
                        k, topk_idx, topk_w, counts, offsets, perm, inv, bm, tile_expert, tile_row,
                        tile_info, num_tiles, status, cap, kept, (uint4*)xp, nq, (const float*)gamma,
-                       eps, (float*)u);
+                       eps, (float*)u, 0);
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -83,3 +83,31 @@ def test_bounded_wait_times_out_and_context_survives(lib, monkeypatch, T):
     assert ref_layer.check() == sef.OK
     assert torch.equal(y_ref, y2)
     ref_layer.close()
+
+
+def test_bounded_wait_times_out_on_the_int8_gemm(lib, monkeypatch):
+    """The int8-weight GEMM's extra rings (A, codes, f16 B) and roles (A
+    producer, converters) give up on a stalled producer the same way."""
+    sef = lib
+    dev = torch.device("cuda", 0)
+    wr, wg, wu, wd = _weights(dev)
+    parts = [tuple(t.to(dev) for t in sef.quantize_int8_block64(w)) for w in (wg, wu, wd)]
+    x = synth.tokens(SHAPE, 8, 3, 0, dev)
+    ref_layer = sef.MoELayer(wr, None, None, None, SHAPE.top_k, max_tokens=8, int8=parts)
+    y_ref = ref_layer.forward(x)
+    assert ref_layer.check() == sef.OK
+
+    monkeypatch.setenv("COLIBRI_WAIT_LIMIT_NS", "20000000")
+    monkeypatch.setenv("COLIBRI_TEST_STALL_TMA", "1")
+    short = sef.MoELayer(wr, None, None, None, SHAPE.top_k, max_tokens=8, int8=parts)
+    monkeypatch.delenv("COLIBRI_WAIT_LIMIT_NS")
+    monkeypatch.delenv("COLIBRI_TEST_STALL_TMA")
+    short.forward(x)
+    assert short.check() == sef.ERR_TIMEOUT
+    assert short.check() == sef.OK
+    short.close()
+
+    y2 = ref_layer.forward(x)
+    assert ref_layer.check() == sef.OK
+    assert torch.equal(y_ref, y2)
+    ref_layer.close()

@@ -1,6 +1,7 @@
 """GPU parity of the int8-weight layer (colibri_init_int8, weights converted
-by colibri_quantize_int8_block64, streamed and dequantised on CUDA cores)
-against the oracle run on its own int8 quantisation of the same weights."""
+by colibri_quantize_int8_block64) on both executors (tcgen05 with shared-
+memory dequantisation, and CUDA cores) against the oracle run on its own int8
+quantisation of the same weights."""
 
 import numpy as np
 import pytest
@@ -34,25 +35,39 @@ def test_tiny_fp32_int8_ragged():
 
 @pytest.fixture(scope="module")
 def mixtral8(lib):
-    c = Int8Case(synth.MIXTRAL, seed=0, max_tokens=128)
+    c = Int8Case(synth.MIXTRAL, seed=0, max_tokens=1024)
     yield c
     c.close()
 
 
 @pytest.mark.parametrize("T", [1, 8, 16, 128])
-def test_mixtral_int8_decode(mixtral8, T):
+@pytest.mark.parametrize("executor", ["grouped", "stream"])
+def test_mixtral_int8_decode(mixtral8, T, executor):
+    """grouped: TMA-fed int8 stages dequantised in shared memory for tcgen05
+    (split-K with the last-slice fixup at these sizes); stream: CUDA cores."""
     x, x64 = mixtral8.tokens(T)
-    y, r = mixtral8.run(x)
+    y, r = mixtral8.run(x, executor)
     l, _ = check_routing(mixtral8, x64, r)
     check_output(mixtral8, x64, y, r, l, _sample(T, 24))
-    y2, _ = mixtral8.run(x)
+    y2, _ = mixtral8.run(x, executor)
     assert torch.equal(y, y2)
 
 
-def test_mixtral_int8_rejects_the_grouped_executor(mixtral8):
+def test_mixtral_int8_prefill_1024(mixtral8):
+    x, x64 = mixtral8.tokens(1024)
+    y, r = mixtral8.run(x, "grouped")
+    l, _ = check_routing(mixtral8, x64, r)
+    check_output(mixtral8, x64, y, r, l, _sample(1024, 32))
+
+
+def test_tiny_fp32_int8_has_no_grouped_executor():
     import sparse_expert_ffn_gb300 as sef
-    with pytest.raises(sef.ColibriError):
-        mixtral8.layer.set_executor("grouped")
+    c = Int8Case(synth.TINY, seed=0, max_tokens=8)
+    try:
+        with pytest.raises(sef.ColibriError):
+            c.layer.set_executor("grouped")
+    finally:
+        c.close()
 
 
 def test_qwen_int8_zipf_with_capacity():
