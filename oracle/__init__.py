@@ -19,6 +19,7 @@ from .moe import (  # noqa: F401
     router_logits,
     topk_select,
     softmax_selected,
+    soft_route,
     dispatch,
     capacity_keep,
     silu,

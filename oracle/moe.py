@@ -137,6 +137,23 @@ def softmax_selected(l: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return ex / ex.sum(axis=1, keepdims=True)
 
 
+def soft_route(l: np.ndarray):
+    """Dense-weighted ("soft") routing: (idx [T, E] int32, g [T, E] float64).
+
+    m.nxbn.cn section 2.2: a Soft MoE router does not hard-select the top k
+    but weights and fuses the outputs of all experts; soft_route() replaces
+    hard_route() and the expert manager and executor stay as they are.
+    Reading: every token goes to every expert, the j-th pair of a token is
+    expert j (expert order), and the gate is the softmax over all E logits
+    (the largest subtracted first).
+    """
+    T, E = l.shape
+    idx = np.tile(np.arange(E, dtype=np.int32), (T, 1))
+    m = l.max(axis=1, keepdims=True)
+    ex = np.exp(l - m)
+    return idx, ex / ex.sum(axis=1, keepdims=True)
+
+
 # ----------------------------------------------------------------------------
 # Step 4: dispatch.
 
@@ -241,7 +258,7 @@ def combine(y_perm: np.ndarray, g: np.ndarray, inv: np.ndarray, keep=None) -> np
 
 
 def moe_layer(x, w_router, w_gate, w_up, w_down, top_k, offset=None,
-              round_h=False, capacity=None):
+              round_h=False, capacity=None, soft=False):
     """The full layer: logits, top-k, softmax, dispatch, experts, combine.
 
     pnsm.cn section 2.2 (one MoE forward: router logits, top-k indices,
@@ -249,12 +266,18 @@ def moe_layer(x, w_router, w_gate, w_up, w_down, top_k, offset=None,
     steps as zskr.cn section 3.3 stages 2-5 run them.  Arguments are float64
     arrays in the library's input layout: x [T,d], W_r [d,E],
     W_g/W_u [E,d,f], W_d [E,f,d].  `capacity` limits the pairs each expert
-    accepts (capacity_keep).
+    accepts (capacity_keep).  `soft` routes every token to every expert
+    (soft_route; top_k must equal E).
     """
     E = w_router.shape[1]
     l = router_logits(x, w_router, offset)
-    idx = topk_select(l, top_k)
-    g = softmax_selected(l, idx)
+    if soft:
+        if top_k != E:
+            raise ValueError("soft routing takes every expert: top_k must equal E")
+        idx, g = soft_route(l)
+    else:
+        idx = topk_select(l, top_k)
+        g = softmax_selected(l, idx)
     counts, offsets, perm, inv = dispatch(idx, E)
     T = x.shape[0]
     y_perm = np.zeros((T * top_k, x.shape[1]), dtype=np.float64)

@@ -382,3 +382,57 @@ def test_layer_under_capacity_drops_exactly_the_rejected_pairs():
                              lambda e: (p["w_gate"][e], p["w_up"][e], p["w_down"][e]))
     assert np.allclose(cap["y"], y, rtol=1e-13, atol=1e-14)
     assert not np.allclose(cap["y"], base["y"])
+
+
+# ---------------------------------------------------------------- soft routing
+
+
+def test_soft_route_gates_are_the_full_softmax():
+    rng = np.random.default_rng(21)
+    l = rng.standard_normal((6, 5)) * 3.0
+    l[2, 4] = -np.inf
+    idx, g = oracle.soft_route(l)
+    assert idx.shape == (6, 5) and np.all(idx == np.arange(5))
+    for t in range(6):
+        # closed form per token, by pure-Python exponentials
+        den = sum(math.exp(v) for v in l[t] if v != -np.inf)
+        for e in range(5):
+            want = 0.0 if l[t, e] == -np.inf else math.exp(l[t, e]) / den
+            assert abs(g[t, e] - want) <= 1e-14
+        # the ratio of two gates is the exponential of the logit difference
+        assert abs(g[t, 0] / g[t, 1] - math.exp(l[t, 0] - l[t, 1])) <= 1e-12
+
+
+def test_soft_layer_is_the_dense_mixture_of_all_experts():
+    p = _small_layer(E=4)
+    out = oracle.moe_layer(p["x"], p["w_router"], p["w_gate"], p["w_up"], p["w_down"], 4,
+                           soft=True)
+    assert np.all(out["counts"] == p["x"].shape[0])
+    for t in range(p["x"].shape[0]):
+        l = [sum(p["x"][t][i] * p["w_router"][i][e] for i in range(p["x"].shape[1]))
+             for e in range(4)]
+        m = max(l)
+        w = [math.exp(v - m) for v in l]
+        s = sum(w)
+        ref = np.zeros(p["x"].shape[1])
+        for e in range(4):
+            y_e = _dense_swiglu_loops([p["x"][t].tolist()], p["w_gate"][e].tolist(),
+                                      p["w_up"][e].tolist(), p["w_down"][e].tolist())[0]
+            ref += (w[e] / s) * np.array(y_e)
+        assert np.allclose(out["y"][t], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_soft_layer_with_one_live_expert_is_k1():
+    p = _small_layer(E=4)
+    off = np.array([-np.inf, 0.0, -np.inf, -np.inf])
+    soft = oracle.moe_layer(p["x"], p["w_router"], p["w_gate"], p["w_up"], p["w_down"], 4, off,
+                            soft=True)
+    hard = oracle.moe_layer(p["x"], p["w_router"], p["w_gate"], p["w_up"], p["w_down"], 1, off)
+    assert np.allclose(soft["y"], hard["y"], rtol=1e-13, atol=1e-14)
+    assert np.all(soft["topk_w"][:, 1] == 1.0)
+
+
+def test_soft_layer_rejects_partial_k():
+    p = _small_layer(E=4)
+    with pytest.raises(ValueError):
+        oracle.moe_layer(p["x"], p["w_router"], p["w_gate"], p["w_up"], p["w_down"], 2, soft=True)

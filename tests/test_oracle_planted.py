@@ -65,6 +65,22 @@ def _capacity_last_C(idx, E, capacity=None):   # keeps the last C pairs of an ex
     return keep[::-1].copy()
 
 
+def _soft_uniform(l):                     # every expert weighted 1/E
+    T, E = l.shape
+    return np.tile(np.arange(E, dtype=np.int32), (T, 1)), np.full((T, E), 1.0 / E)
+
+
+def _soft_top2_only(l):                   # softmax over the two largest, zeros elsewhere
+    T, E = l.shape
+    idx = np.tile(np.arange(E, dtype=np.int32), (T, 1))
+    g = np.zeros((T, E))
+    for t in range(T):
+        top = np.argsort(-l[t])[:2]
+        ex = np.exp(l[t, top] - l[t, top].max())
+        g[t, top] = ex / ex.sum()
+    return idx, g
+
+
 def _rmsnorm_no_mean(h, gamma, eps):      # sum instead of mean
     return h / np.sqrt(np.sum(h * h, axis=1, keepdims=True) + eps) * gamma[None, :]
 
@@ -84,6 +100,10 @@ CASES = [
     ("swiglu_expert", _up_transposed, [pins.test_one_expert_k1_equals_dense_swiglu,
                                        pins.test_hand_worked_example]),
     ("rmsnorm", _rmsnorm_no_mean, [pins.test_rmsnorm_closed_forms]),
+    ("soft_route", _soft_uniform, [pins.test_soft_route_gates_are_the_full_softmax,
+                                   pins.test_soft_layer_is_the_dense_mixture_of_all_experts]),
+    ("soft_route", _soft_top2_only, [pins.test_soft_route_gates_are_the_full_softmax,
+                                     pins.test_soft_layer_is_the_dense_mixture_of_all_experts]),
     ("capacity_keep", _capacity_last_C,
      [lambda: pins.test_capacity_keep_is_the_first_C_of_each_expert_segment(40, 8, 2, 3)]),
 ]
