@@ -60,6 +60,9 @@ def parse_args(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="tokens per step (default per workload; batch per step for the stack)")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--top-k", type=int, default=None,
+                    help="experts per token (default: the shape's); equal to the expert count "
+                         "selects soft routing (every expert, softmax over all logits)")
     ap.add_argument("--weights", choices=["bf16", "int8"], default="bf16",
                     help="expert weight format: bf16, or int8 64x64 blocks (converted on the host, "
                          "streamed and dequantised on CUDA cores)")
@@ -301,6 +304,10 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     shape_name, T_default, label, sweep_T = WORKLOADS[args.workload]
     shape = getattr(synth, shape_name)
+    if args.top_k:
+        from dataclasses import replace
+        shape = replace(shape, top_k=args.top_k)
+        label += ", soft routing" if args.top_k == shape.n_experts else f", top-{args.top_k}"
     T = args.tokens or T_default
     pk = peaks()
     props = torch.cuda.get_device_properties(dev)

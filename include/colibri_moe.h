@@ -55,7 +55,12 @@ typedef enum {
 } colibri_executor_t;
 
 /* Layer shape.  d_model % 64 == 0 and d_ff % 128 == 0 are required
- * (UNSUPPORTED otherwise); 1 <= top_k <= n_experts <= 256; top_k <= 8. */
+ * (UNSUPPORTED otherwise); 1 <= top_k <= n_experts <= 256; top_k <= 8, or
+ * top_k == n_experts.
+ * top_k == n_experts selects soft routing (m.nxbn.cn section 2.2: a Soft MoE
+ * router weights and fuses every expert's output instead of hard-selecting
+ * k): every token goes to every expert, pair j of a token is expert j, and
+ * the gate is the softmax over all E logits.  Otherwise routing is top-k. */
 typedef struct {
     int32_t n_experts;   /* E */
     int32_t top_k;       /* k */
@@ -277,7 +282,8 @@ colibri_status_t colibri_profile_read(colibri_moe_t* h, double* total_ms, uint64
  * Limits of the fixed array: d_model * n_experts <= 1048576 and
  * T * top_k <= 131072; larger sizes return COLIBRI_ERR_INVALID_ARG before any
  * CUDA call.  Shape rules as colibri_init (d_model % 64 == 0, n_experts <= 256,
- * top_k <= 8: COLIBRI_ERR_UNSUPPORTED otherwise).
+ * top_k <= 8 or top_k == n_experts (soft routing, as in colibri_moe_config_t):
+ * COLIBRI_ERR_UNSUPPORTED otherwise).
  *
  * Runs on the current device, ordered on `stream`, without waiting for it.
  * The first call on a device looks up the array's device address and checks

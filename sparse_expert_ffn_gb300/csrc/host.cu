@@ -175,7 +175,10 @@ colibri_status_t validate_config(const colibri_moe_config_t* c) {
     if (c->executor < COLIBRI_EXEC_AUTO || c->executor > COLIBRI_EXEC_GROUPED)
         return COLIBRI_ERR_INVALID_ARG;
     if ((int64_t)c->max_tokens * c->top_k > (int64_t)1 << 30) return COLIBRI_ERR_INVALID_ARG;
-    if (c->n_experts > 256 || c->top_k > 8) return COLIBRI_ERR_UNSUPPORTED;
+    // top_k == n_experts is soft routing (every expert, softmax over all E);
+    // otherwise the top-k kernels take up to 8 experts per token
+    if (c->n_experts > 256 || (c->top_k > 8 && c->top_k != c->n_experts))
+        return COLIBRI_ERR_UNSUPPORTED;
     if (c->d_model % 64 != 0 || c->d_ff % 128 != 0) return COLIBRI_ERR_UNSUPPORTED;
     if (c->executor == COLIBRI_EXEC_GROUPED && c->dtype != COLIBRI_DTYPE_BF16)
         return COLIBRI_ERR_UNSUPPORTED;
@@ -300,7 +303,9 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     const bool pair = ex == COLIBRI_EXEC_GROUPED && npairs >= 128 * E && !h->int8;
     const int tile_rows = pair ? tc_gemm_pair_rows() : tc_gemm_block_m();
     // Small batch: router, top-k, softmax, dispatch and gather in one CTA.
-    const bool fused_routing = route_small_fits(T, d, E, k);
+    // soft routing (k == E) runs on the CUDA-core router kernel
+    const bool soft = k == E;
+    const bool fused_routing = !soft && route_small_fits(T, d, E, k);
     const int cap = h->capacity < 0 ? INT_MAX : h->capacity;
     if (gamma && !fused_routing) {
         Stage g(h, COLIBRI_STAGE_RMSNORM, s);
@@ -318,7 +323,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
                                        h->u, s, h->int8), 1);
         if (st != COLIBRI_OK) return st;
         if (gamma) x = h->u;
-    } else if (h->grouped_ok && T >= kTcRouterMinTokens) {
+    } else if (h->grouped_ok && T >= kTcRouterMinTokens && !soft) {
         // Large batch: the router logits are a [T, d] x [d, E] GEMM on the
         // tensor cores, top-k and softmax in its epilogue.
         CUtensorMap tm_x;
@@ -344,7 +349,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     } else {
         Stage g(h, COLIBRI_STAGE_ROUTER, s);
         st = g.done(launch_router_simt(h->dt, x, h->wr, h->bias, T, d, E, k, h->topk_idx,
-                                       h->topk_w, s), 1);
+                                       h->topk_w, s, soft), 1);
         if (st != COLIBRI_OK) return st;
     }
     if (!fused_routing && npairs > kMultiDispatchPairs) {

@@ -16,7 +16,7 @@ cudaError_t smem_attr(const void* kernel, int bytes);
 
 cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const float* bias,
                                int ntok, int d, int E, int k, int32_t* idx, float* w,
-                               cudaStream_t s);
+                               cudaStream_t s, bool soft = false);
 
 size_t dispatch_smem(int E);
 cudaError_t launch_dispatch(const int32_t* topk_idx, int n, int E, int32_t* counts,

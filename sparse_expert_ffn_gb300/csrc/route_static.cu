@@ -94,7 +94,8 @@ extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_ro
     if (dtype != COLIBRI_DTYPE_FP32 && dtype != COLIBRI_DTYPE_BF16) return COLIBRI_ERR_INVALID_ARG;
     if (T < 0 || d_model <= 0 || n_experts <= 0 || top_k <= 0 || top_k > n_experts)
         return COLIBRI_ERR_INVALID_ARG;
-    if (n_experts > 256 || top_k > 8 || d_model % 64 != 0) return COLIBRI_ERR_UNSUPPORTED;
+    if (n_experts > 256 || (top_k > 8 && top_k != n_experts) || d_model % 64 != 0)
+        return COLIBRI_ERR_UNSUPPORTED;
     // Sizes beyond the fixed scratch array.
     if ((int64_t)d_model * n_experts > kStaticMaxRouterElems ||
         (int64_t)T * top_k > kStaticMaxPairs)
@@ -126,7 +127,8 @@ extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_ro
         e = launch_transpose_remap(esz, w_router, wr_packed, 1, d, E, (size_t)d * E,
                                    (size_t)E * d, E, E, 0, cs);
     if (e == cudaSuccess)
-        e = launch_router_simt(dt, x, wr_packed, router_bias, T, d, E, k, topk_idx, topk_w, cs);
+        e = launch_router_simt(dt, x, wr_packed, router_bias, T, d, E, k, topk_idx, topk_w, cs,
+                               k == E);   // top_k == n_experts: soft routing
     if (e == cudaSuccess)
         e = launch_dispatch(topk_idx, T * k, E, counts, offsets, perm, inv, kStaticTileRows,
                             tile_expert, tile_row, tile_info, num_tiles, status, INT_MAX, kept,

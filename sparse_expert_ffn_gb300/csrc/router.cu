@@ -29,7 +29,7 @@ template <typename T, int kWarpsPerToken>
 __global__ void __launch_bounds__(kRouterWarps * 32)
 router_topk_simt(const T* __restrict__ x, const T* __restrict__ wr, const float* __restrict__ bias,
                  int ntok, int d, int E, int k, int32_t* __restrict__ topk_idx,
-                 float* __restrict__ topk_w) {
+                 float* __restrict__ topk_w, int soft) {
     pdl_enter();
     extern __shared__ float smem[];
     constexpr int kTokens = kRouterWarps / kWarpsPerToken;
@@ -71,19 +71,36 @@ router_topk_simt(const T* __restrict__ x, const T* __restrict__ wr, const float*
     __syncthreads();
     if (!live || sub != 0) return;
 
+    if (soft) {
+        // soft routing (k = E): every expert, in expert order, gate = the
+        // softmax over all E logits (largest subtracted first)
+        float m = -INFINITY;
+        for (int e = lane; e < E; e += 32) m = fmaxf(m, logit[e]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float s = 0.f;
+        for (int e = lane; e < E; e += 32) s += expf(logit[e] - m);
+        s = warp_sum(s);
+        for (int e = lane; e < E; e += 32) {
+            topk_idx[(size_t)t * E + e] = e;
+            topk_w[(size_t)t * E + e] = expf(logit[e] - m) / s;
+        }
+        return;
+    }
     warp_topk_softmax(logit, E, k, lane, topk_idx + (size_t)t * k, topk_w + (size_t)t * k);
 }
 
 template <typename T, int kWarpsPerToken>
 cudaError_t launch_router_t(const void* x, const void* wr, const float* bias, int ntok, int d,
-                            int E, int k, int32_t* idx, float* w, cudaStream_t s) {
+                            int E, int k, int32_t* idx, float* w, cudaStream_t s, int soft) {
     constexpr int kTokens = kRouterWarps / kWarpsPerToken;
     const dim3 grid((ntok + kTokens - 1) / kTokens), block(kRouterWarps * 32);
     const size_t smem = (size_t)kTokens * (d + 256) * sizeof(float);
     auto kern = router_topk_simt<T, kWarpsPerToken>;
     smem_attr((const void*)kern, (int)smem);
     const cudaError_t e =
-        launch_pdl(kern, grid, block, smem, s, (const T*)x, (const T*)wr, bias, ntok, d, E, k, idx, w);
+        launch_pdl(kern, grid, block, smem, s, (const T*)x, (const T*)wr, bias, ntok, d, E, k, idx, w,
+                   soft);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -91,16 +108,17 @@ cudaError_t launch_router_t(const void* x, const void* wr, const float* bias, in
 
 cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const float* bias,
                                int ntok, int d, int E, int k, int32_t* idx, float* w,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool soft) {
     if (ntok <= 0) return cudaSuccess;
     // Few tokens: spread every token over a whole CTA; many: two warps per
     // token, four tokens per CTA (70 KB of shared memory at d = 4096).
     const bool small = ntok <= 256;
+    const int sf = soft ? 1 : 0;
     if (dt == DType::BF16)
-        return small ? launch_router_t<__nv_bfloat16, kRouterWarps>(x, wr, bias, ntok, d, E, k, idx, w, s)
-                     : launch_router_t<__nv_bfloat16, 2>(x, wr, bias, ntok, d, E, k, idx, w, s);
-    return small ? launch_router_t<float, kRouterWarps>(x, wr, bias, ntok, d, E, k, idx, w, s)
-                 : launch_router_t<float, 2>(x, wr, bias, ntok, d, E, k, idx, w, s);
+        return small ? launch_router_t<__nv_bfloat16, kRouterWarps>(x, wr, bias, ntok, d, E, k, idx, w, s, sf)
+                     : launch_router_t<__nv_bfloat16, 2>(x, wr, bias, ntok, d, E, k, idx, w, s, sf);
+    return small ? launch_router_t<float, kRouterWarps>(x, wr, bias, ntok, d, E, k, idx, w, s, sf)
+                 : launch_router_t<float, 2>(x, wr, bias, ntok, d, E, k, idx, w, s, sf);
 }
 
 }  // namespace colibri

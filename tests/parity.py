@@ -5,6 +5,7 @@ routing near-tie rule.
 Parity rules (all float tolerances are written here once):
 * topk_idx must equal the oracle's on every token that is not a near-tie
   (oracle.near_tie_tokens); near-tie tokens may differ and are counted.
+  With top_k == E (soft routing) it must equal 0..E-1 on every token.
 * counts and perm must equal the oracle's dispatch of the GPU's own topk_idx
   (an integer function: always exact), and the oracle's own dispatch when no
   token is a near-tie.
@@ -132,8 +133,13 @@ def check_routing(case: Case, x64, r, allow_near_ties: bool = True):
     """Compare routing to the oracle; returns (logits64, near_tie mask)."""
     k, E = case.shape.top_k, case.shape.n_experts
     l = oracle.router_logits(x64, case.wr64, case.off64)
-    ref_idx = oracle.topk_select(l, k)
-    near = oracle.near_tie_tokens(x64, case.wr64, l, k)
+    if k == E:
+        # soft routing: every expert in expert order, no selection to tie on
+        ref_idx = oracle.soft_route(l)[0]
+        near = np.zeros(l.shape[0], dtype=bool)
+    else:
+        ref_idx = oracle.topk_select(l, k)
+        near = oracle.near_tie_tokens(x64, case.wr64, l, k)
     if not allow_near_ties:
         assert not near.any(), f"{int(near.sum())} near-tie tokens"
     gidx = r["topk_idx"]
