@@ -362,8 +362,13 @@ def run_ours(args):
              ("expert_up", False): "ffn_up_stream" + i8, ("expert_down", False): "ffn_down_stream" + i8}.get(
         (dom, grouped), dom)
     workload = f"{args.workload}_T{T}"
-    if grouped and dom in ("expert_up", "expert_down"):
-        fl = alg["up_flops"] if dom == "expert_up" else alg["down_flops"]
+    # the kernel's bound: tensor when its FLOPs take longer at the tensor peak
+    # than its bytes at the HBM peak (prefill), HBM otherwise (decode sizes)
+    fl_dom = alg["up_flops"] if dom == "expert_up" else alg["down_flops"]
+    by_dom = {"expert_up": alg["up_bytes"], "expert_down": alg["down_bytes"]}.get(dom, alg["bytes"])
+    tensor_bound = fl_dom / (pk["bf16_tflops"] * 1e12) >= by_dom / (pk["hbm_gbs"] * 1e9)
+    if grouped and dom in ("expert_up", "expert_down") and tensor_bound:
+        fl = fl_dom
         achieved = fl / per_launch_s / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
@@ -376,8 +381,7 @@ def run_ours(args):
     roof["kernel"] = kname
     roof["share_of_step"] = round(stages[dom]["ms_total"] / sum(v["ms_total"] for v in stages.values()), 4)
     roof["traffic"] = measured_traffic(kname, workload)
-    roof["algorithmic_per_launch"] = (alg["up_flops"] if dom == "expert_up" else alg["down_flops"]) \
-        if roof["bound"] == "tensor" else None
+    roof["algorithmic_per_launch"] = fl_dom if roof["bound"] == "tensor" else by_dom
 
     whole = {"roofline_time_us": round(1e6 * max(alg["bytes"] / (pk["hbm_gbs"] * 1e9),
                                                  alg["flops"] / (pk["bf16_tflops"] * 1e12)), 1),
