@@ -184,6 +184,23 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Int8 weight codes are stored tile-major: the packed weight rows of K codes
+// each are cut into tiles of 128 rows x 64 codes, tile (row / 128, k / 64) is
+// 8 KB contiguous, tiles of one row block consecutive in k.  Inside a tile,
+// row r takes 64 bytes and its 16-byte chunk c sits at chunk c ^ ((r >> 1) & 3)
+// (the 64-byte swizzle pattern), so that one bulk copy of a tile gives a
+// shared-memory image in which the 8 rows a quarter warp reads at the same
+// chunk fall in 8 different bank groups.
+__host__ __device__ __forceinline__ size_t code_index(size_t row, int k, int K) {
+    const size_t r = row & 127;
+    return ((row >> 7) * (size_t)(K >> 6) + (size_t)(k >> 6)) * 8192 + r * 64 +
+           (size_t)((((k & 63) >> 4) ^ (int)((r >> 1) & 3)) << 4) + (size_t)(k & 15);
+}
+// Byte offset of code chunk c (16 codes) of row r inside a tile.
+__device__ __forceinline__ int code_chunk_offset(int r, int c) {
+    return (r & 127) * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
 // Int8 weight codes (64x64 blocks, w = (q - zp) * scale).  The byte permute
 // places each code, sign bit flipped (q + 128 as an unsigned byte), in the low
 // mantissa byte of 2^23, which is the exact float 2^23 + 128 + q; subtracting

@@ -189,10 +189,9 @@ ffn_up_stream_i8(const T* __restrict__ x, const int8_t* __restrict__ wq,
         const int c = kept[e];
         if (c == 0) continue;
         const int off = offsets[e];
-        const int8_t* g_row = wq + gu_row(e, n, 0, f) * d;
-        const int8_t* u_row = wq + gu_row(e, n, 1, f) * d;
-        const size_t gb = (gu_row(e, n, 0, f) >> 6) * nkb;   // gate block row
-        const size_t ub = (gu_row(e, n, 1, f) >> 6) * nkb;
+        const size_t grow = gu_row(e, n, 0, f), urow = gu_row(e, n, 1, f);
+        const size_t gb = (grow >> 6) * nkb;   // gate block row of scales
+        const size_t ub = (urow >> 6) * nkb;
         for (int s0 = 0; s0 < c; s0 += kSlots) {
             const int ns = min(kSlots, c - s0);
             const T* xr[kSlots];
@@ -206,9 +205,9 @@ ffn_up_stream_i8(const T* __restrict__ x, const int8_t* __restrict__ wq,
                 uint4 vg[kAheadI8], vu[kAheadI8];
 #pragma unroll
                 for (int a = 0; a < kAheadI8; ++a) {
-                    if (i0 + a * 512 < d) {
-                        vg[a] = ld_stream16(g_row + i0 + a * 512);
-                        vu[a] = ld_stream16(u_row + i0 + a * 512);
+                    if (i0 + a * 512 < d) {   // tile-major codes (code_index)
+                        vg[a] = ld_stream16(wq + code_index(grow, i0 + a * 512, d));
+                        vu[a] = ld_stream16(wq + code_index(urow, i0 + a * 512, d));
                     }
                 }
 #pragma unroll
@@ -257,8 +256,8 @@ ffn_down_stream_i8(const T* __restrict__ H, const int8_t* __restrict__ wq,
         const int c = kept[e];
         if (c == 0) continue;
         const int off = offsets[e];
-        const int8_t* w_row = wq + ((size_t)e * d + col) * f;
-        const size_t bb ((((size_t)e * d + col) >> 6) * nkb);
+        const size_t wrow = (size_t)e * d + col;
+        const size_t bb = (wrow >> 6) * nkb;
         for (int s0 = 0; s0 < c; s0 += kSlots) {
             const int ns = min(kSlots, c - s0);
             float acc[kSlots];
@@ -268,7 +267,8 @@ ffn_down_stream_i8(const T* __restrict__ H, const int8_t* __restrict__ wq,
                 uint4 v[kAheadI8];
 #pragma unroll
                 for (int a = 0; a < kAheadI8; ++a)
-                    if (i0 + a * 512 < f) v[a] = ld_stream16(w_row + i0 + a * 512);
+                    if (i0 + a * 512 < f)   // tile-major codes (code_index)
+                        v[a] = ld_stream16(wq + code_index(wrow, i0 + a * 512, f));
 #pragma unroll
                 for (int a = 0; a < kAheadI8; ++a) {
                     const int i = i0 + a * 512;

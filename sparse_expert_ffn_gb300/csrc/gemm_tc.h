@@ -41,6 +41,7 @@ struct TcGemmArgs {
     // 64 packed B rows, [B rows / 64][k_blocks]
     const float* q_scale;
     const int32_t* q_zp;
+    const int8_t* q_codes;       // tile-major codes (code_index), read by bulk copies
     int stall_producer;          // failure-detection tests only: issue no TMA copy, so
                                  // the first wait on a full stage runs out its bound
 };
@@ -51,14 +52,27 @@ int tc_gemm_pair_rows();     // rows of one expert tile of a CTA pair (256)
 int tc_gemm_max_pairs();     // CTA pairs resident at once (0 if unknown)
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows, bool f16 = false);
-bool make_tmap_i8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                  uint32_t box_rows);
 // pair: run the expert GEMMs on CTA pairs (256-row tiles, B tensor map with
 // 128-row boxes) instead of single CTAs (128-row tiles, 256-row B boxes).
-// int8_b: B is int8 codes (tmB from make_tmap_i8, 256-row boxes) dequantised
-// to f16 in shared memory by converter warps; A (Xp, H) is f16 and H is
-// written as f16; single CTAs, kGateUp / kDown only.
+// int8_b: B is int8 codes (args.q_codes, tile-major, two 128-row tiles per
+// stage by bulk copies; tmB unused) dequantised to f16 in shared memory by
+// converter warps; A (Xp, H) is f16 and H is written as f16; single CTAs,
+// kGateUp / kDown only.
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b = false);
+
+// Decode-sized expert GEMMs with the weights as the MMA's M operand
+// (gemm_dec.cu): tiles of 128 weight rows x 32 tokens of one expert (the tile
+// list cut with tc_gemm_dec_tile_rows() rows).  tmTok: Xp or H with 32-row
+// boxes; tmW: the packed bf16 weights with 128-row boxes, or with int8_w
+// unused: the int8 code tiles come from args.q_codes, the block scales from
+// args.q_scale / q_zp, and the tokens are f16.  kGateUp: n_blocks = f / 128,
+// b_rows_per_expert = 2 f; kDown:
+// n_blocks = d / 128, b_rows_per_expert = d.
+size_t tc_gemm_dec_smem_bytes();
+int tc_gemm_dec_tile_rows();
+int tc_gemm_dec_w_rows();
+cudaError_t launch_tc_gemm_dec(int mode, const CUtensorMap& tmTok, const CUtensorMap& tmW,
+                               const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_w);
 
 }  // namespace colibri

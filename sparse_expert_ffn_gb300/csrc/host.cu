@@ -84,6 +84,9 @@ struct colibri_moe {
     bool grouped_ok = false;
     // B operands: 128-row boxes for CTA pairs, 256-row boxes for single CTAs
     CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT, tm_wr, tm_wgu1, tm_wdT1;
+    // decode GEMM (weights as M): token rows in 32-row boxes (bf16 weights:
+    // tm_wgu / tm_wdT, 128-row boxes; int8 codes: bulk copies of tiles)
+    CUtensorMap tm_xp32, tm_h32;
     uint64_t wait_limit_ns = 2000000000ull;
     bool stall_tma = false;  // failure-detection tests (COLIBRI_TEST_STALL_TMA=1)
     int last_T = 0;
@@ -131,6 +134,9 @@ constexpr int kMultiDispatchPairs = 12288;
 // Batches from this many tokens route on the tensor cores.
 constexpr int kTcRouterMinTokens = 512;
 constexpr int kMaxKSplit = 16;
+// Batches averaging at most this many (token, slot) pairs per expert run the
+// decode GEMMs (weights as the MMA's M operand, 32-token tiles).
+constexpr int kDecMaxPairsPerExpert = 16;
 // The gate/up GEMM splits K only for batches of at most this many pairs.
 constexpr int kGateUpSplitMaxPairs = 64;
 
@@ -222,18 +228,19 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
 // the remapping transpose; host inputs go through a device staging buffer one
 // batch entry at a time.
 colibri_status_t pack(int esz, const void* src, bool src_on_device, void* dst, int batch, int R,
-                      int C, size_t out_batch, int blk, int period, int which, void* staging) {
+                      int C, size_t out_batch, int blk, int period, int which, void* staging,
+                      bool tiled = false) {
     const size_t mat = (size_t)R * C * esz;
     if (src_on_device) {
         return from_cuda(launch_transpose_remap(esz, src, dst, batch, R, C, (size_t)R * C,
-                                                out_batch, blk, period, which, 0));
+                                                out_batch, blk, period, which, 0, tiled));
     }
     for (int b = 0; b < batch; ++b) {
         cudaError_t e = cudaMemcpy(staging, (const uint8_t*)src + (size_t)b * mat, mat,
                                    cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return from_cuda(e);
         e = launch_transpose_remap(esz, staging, (uint8_t*)dst + (size_t)b * out_batch * esz, 1, R,
-                                   C, (size_t)R * C, out_batch, blk, period, which, 0);
+                                   C, (size_t)R * C, out_batch, blk, period, which, 0, tiled);
         if (e != cudaSuccess) return from_cuda(e);
         e = cudaDeviceSynchronize();
         if (e != cudaSuccess) return from_cuda(e);
@@ -300,8 +307,9 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     // Expert GEMMs on CTA pairs (256-row tiles) once the batch averages 128
     // rows per expert; below that most tile rows would be empty and single
     // CTAs (128-row tiles) stream the weights faster.
-    const bool pair = ex == COLIBRI_EXEC_GROUPED && npairs >= 128 * E && !h->int8;
-    const int tile_rows = pair ? tc_gemm_pair_rows() : tc_gemm_block_m();
+    const bool dec = ex == COLIBRI_EXEC_GROUPED && npairs <= kDecMaxPairsPerExpert * E;
+    const bool pair = ex == COLIBRI_EXEC_GROUPED && !dec && npairs >= 128 * E && !h->int8;
+    const int tile_rows = dec ? tc_gemm_dec_tile_rows() : pair ? tc_gemm_pair_rows() : tc_gemm_block_m();
     // Small batch: router, top-k, softmax, dispatch and gather in one CTA.
     // soft routing (k == E) runs on the CUDA-core router kernel
     const bool soft = k == E;
@@ -428,6 +436,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.out_ld = f;
         a.q_scale = h->sc_gu;
         a.q_zp = h->zp_gu;
+        a.q_codes = h->q_gu;
         if (!pair && npairs <= kGateUpSplitMaxPairs) {
             const int fit = (int)std::min<size_t>(kMaxKSplit, h->y_floats / ((size_t)npairs * 2 * f));
             a.k_splits = choose_k_splits(tiles_est * a.n_blocks, a.k_blocks, units, fit);
@@ -439,20 +448,24 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             const int grid = cta_per_unit * (int)std::min<int64_t>(
                                                     (int64_t)tiles_ub * a.n_blocks * a.k_splits, units);
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
-            st = g.done(launch_tc_gemm(kGateUp, pair, h->tm_xp, pair ? h->tm_wgu : h->tm_wgu1, a,
-                                       grid, s, h->int8), 1);
+            st = g.done(dec ? launch_tc_gemm_dec(kGateUp, h->tm_xp32, h->int8 ? h->tm_xp : h->tm_wgu,
+                                                 a, grid, s, h->int8)
+                            : launch_tc_gemm(kGateUp, pair, h->tm_xp, pair ? h->tm_wgu : h->tm_wgu1,
+                                             a, grid, s, h->int8),
+                        1);
             if (st != COLIBRI_OK) return st;
         }
         // down: N = d in blocks of 256, K = f.  Few pairs leave too few
         // (m-tile, n-block) items to fill the GPU: split K into slices whose
         // float32 partials the combine adds in slice order.
-        a.n_blocks = d / 256;
+        a.n_blocks = d / (dec ? tc_gemm_dec_w_rows() : 256);
         a.k_blocks = f / 64;
         a.b_rows_per_expert = d;
         a.out = h->Y;
         a.out_ld = d;
         a.q_scale = h->sc_d;
         a.q_zp = h->zp_d;
+        a.q_codes = h->q_d;
         a.k_splits = 1;
         a.partial = nullptr;
         a.partial_split_stride = 0;
@@ -466,8 +479,11 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             const int grid = cta_per_unit * (int)std::min<int64_t>(
                                                     (int64_t)tiles_ub * a.n_blocks * a.k_splits, units);
             Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
-            st = g.done(launch_tc_gemm(kDown, pair, h->tm_h, pair ? h->tm_wdT : h->tm_wdT1, a, grid,
-                                       s, h->int8), 1);
+            st = g.done(dec ? launch_tc_gemm_dec(kDown, h->tm_h32, h->int8 ? h->tm_h : h->tm_wdT, a,
+                                                 grid, s, h->int8)
+                            : launch_tc_gemm(kDown, pair, h->tm_h, pair ? h->tm_wdT : h->tm_wdT1, a,
+                                             grid, s, h->int8),
+                        1);
             if (st != COLIBRI_OK) return st;
         }
         nsplit = a.k_splits;
@@ -520,6 +536,8 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
         if (!qu || !qd) return COLIBRI_ERR_INVALID_ARG;
         for (const colibri_int8_weights_t* w : {qg, qu, qd})
             if (!w->q || !w->scale || !w->zp) return COLIBRI_ERR_INVALID_ARG;
+        // code tiles hold 128 packed rows: an expert's down rows fill whole tiles
+        if (cfg->d_model % 128) return COLIBRI_ERR_UNSUPPORTED;
     } else if (!w_gate || !w_up || !w_down) {
         return COLIBRI_ERR_INVALID_ARG;
     }
@@ -611,11 +629,13 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
             st = pack(h->esz, w_down, dev, h->wdT, E, f, d, (size_t)d * f, d, d, 0, staging);
     } else {
         // codes: the bf16 layouts with one-byte elements
-        st = pack(1, qg->q, dev, h->q_gu, E, d, f, (size_t)2 * f * d, 128, 256, 0, staging);
+        // codes: the bf16 packed rows, stored tile-major (code_index)
+        st = pack(1, qg->q, dev, h->q_gu, E, d, f, (size_t)2 * f * d, 128, 256, 0, staging, true);
         if (st == COLIBRI_OK)
-            st = pack(1, qu->q, dev, h->q_gu, E, d, f, (size_t)2 * f * d, 128, 256, 1, staging);
+            st = pack(1, qu->q, dev, h->q_gu, E, d, f, (size_t)2 * f * d, 128, 256, 1, staging,
+                      true);
         if (st == COLIBRI_OK)
-            st = pack(1, qd->q, dev, h->q_d, E, f, d, (size_t)d * f, d, d, 0, staging);
+            st = pack(1, qd->q, dev, h->q_d, E, f, d, (size_t)d * f, d, d, 0, staging, true);
         // block scales and zero points, one row per 64 packed weight rows:
         // gate/up [E][d/64][f/64] -> [E][f/128][2][2][d/64] (two 64-row blocks
         // of each 128-row gate or up slab), down [E][f/64][d/64] -> [E][d/64][f/64]
@@ -637,7 +657,9 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
     // ---- workspace arena
     const int M = cfg->max_tokens;
     h->max_pairs = M * k;
-    h->max_tiles = (h->max_pairs + tc_gemm_block_m() - 1) / tc_gemm_block_m() + std::min(E, h->max_pairs);
+    // the finest tiling is the decode GEMM's 32-row tiles
+    h->max_tiles = (h->max_pairs + tc_gemm_dec_tile_rows() - 1) / tc_gemm_dec_tile_rows() +
+                   std::min(E, h->max_pairs);
     h->grouped_ok = grouped_shape_ok(*cfg);
     if (cfg->executor == COLIBRI_EXEC_GROUPED && !h->grouped_ok) return fail(COLIBRI_ERR_UNSUPPORTED);
     const size_t P = (size_t)h->max_pairs;
@@ -698,9 +720,12 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
         bool ok = make_tmap_bf16(&h->tm_xp, h->xp, P, d, 128, int8) &&
                   make_tmap_bf16(&h->tm_h, h->H, P, f, 128, int8) &&
                   make_tmap_bf16(&h->tm_wr, h->wr, (uint64_t)h->e_pad, d, (uint32_t)h->e_pad);
+        ok = ok && make_tmap_bf16(&h->tm_xp32, h->xp, P, d, (uint32_t)tc_gemm_dec_tile_rows(), int8) &&
+             make_tmap_bf16(&h->tm_h32, h->H, P, f, (uint32_t)tc_gemm_dec_tile_rows(), int8);
         if (int8)
-            ok = ok && make_tmap_i8(&h->tm_wgu1, h->q_gu, (uint64_t)E * 2 * f, d, 256) &&
-                 make_tmap_i8(&h->tm_wdT1, h->q_d, (uint64_t)E * d, f, 256);
+            // int8 codes are read by bulk copies of whole tiles (args.q_codes);
+            // the weight tensor-map argument of those launches is not used
+            h->tm_wgu1 = h->tm_xp, h->tm_wdT1 = h->tm_h;
         else
             ok = ok && make_tmap_bf16(&h->tm_wgu, h->wgu, (uint64_t)E * 2 * f, d, 128) &&
                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 128) &&

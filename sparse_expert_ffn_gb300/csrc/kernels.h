@@ -72,6 +72,6 @@ cudaError_t launch_rmsnorm(DType dt, const void* h, const void* gamma, int T, in
                            void* u, cudaStream_t s);
 cudaError_t launch_transpose_remap(int elem_bytes, const void* in, void* out, int batch, int R,
                                    int C, size_t in_batch, size_t out_batch, int blk, int period,
-                                   int which, cudaStream_t s);
+                                   int which, cudaStream_t s, bool tiled = false);
 
 }  // namespace colibri

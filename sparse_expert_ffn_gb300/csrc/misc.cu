@@ -85,11 +85,12 @@ __global__ void rmsnorm_kernel(const T* __restrict__ h, const T* __restrict__ ga
 
 // Batched transpose with a row remap, for the init-time weight repack:
 // out[b][map(c)][r] = in[b][r][c] for an [R, C] matrix per batch entry b,
-// map(c) = (c / blk) * period + which * blk + c % blk.
+// map(c) = (c / blk) * period + which * blk + c % blk; with `tiled`, the
+// output rows of R codes are stored tile-major (code_index).
 template <typename E>
 __global__ void transpose_remap(const E* __restrict__ in, E* __restrict__ out, int R, int C,
                                 size_t in_batch, size_t out_batch, int blk, int period,
-                                int which) {
+                                int which, int tiled) {
     __shared__ E tile[32][33];
     const int b = blockIdx.z;
     const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
@@ -104,7 +105,7 @@ __global__ void transpose_remap(const E* __restrict__ in, E* __restrict__ out, i
         const int c = c0 + i, r = r0 + threadIdx.x;
         if (r < R && c < C) {
             const size_t orow = (size_t)(c / blk) * period + (size_t)which * blk + c % blk;
-            dst[orow * R + r] = tile[threadIdx.x][i];
+            dst[tiled ? code_index(orow, r, R) : orow * R + r] = tile[threadIdx.x][i];
         }
     }
 }
@@ -171,19 +172,20 @@ cudaError_t launch_rmsnorm(DType dt, const void* h, const void* gamma, int T, in
 
 cudaError_t launch_transpose_remap(int elem_bytes, const void* in, void* out, int batch, int R,
                                    int C, size_t in_batch, size_t out_batch, int blk, int period,
-                                   int which, cudaStream_t s) {
+                                   int which, cudaStream_t s, bool tiled) {
     const dim3 block(32, 8), grid((C + 31) / 32, (R + 31) / 32, batch);
+    const int t = tiled ? 1 : 0;
     if (elem_bytes == 1)
         transpose_remap<uint8_t><<<grid, block, 0, s>>>((const uint8_t*)in, (uint8_t*)out, R, C,
-                                                        in_batch, out_batch, blk, period, which);
+                                                        in_batch, out_batch, blk, period, which, t);
     else if (elem_bytes == 2)
         transpose_remap<uint16_t><<<grid, block, 0, s>>>((const uint16_t*)in, (uint16_t*)out, R,
                                                          C, in_batch, out_batch, blk, period,
-                                                         which);
+                                                         which, t);
     else
         transpose_remap<uint32_t><<<grid, block, 0, s>>>((const uint32_t*)in, (uint32_t*)out, R,
                                                          C, in_batch, out_batch, blk, period,
-                                                         which);
+                                                         which, t);
     return cudaGetLastError();
 }
 
