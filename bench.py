@@ -124,9 +124,13 @@ def source_sha(*rel):
     return h.hexdigest()[:12]
 
 
+_TC = ("sparse_expert_ffn_gb300/csrc/gemm_tc.cu", "sparse_expert_ffn_gb300/csrc/tc_common.cuh")
+_DEC = ("sparse_expert_ffn_gb300/csrc/gemm_dec.cu", "sparse_expert_ffn_gb300/csrc/tc_common.cuh")
 KERNEL_SOURCES = {
-    "grouped_gemm_tc<kGateUp>": ("sparse_expert_ffn_gb300/csrc/gemm_tc.cu",),
-    "grouped_gemm_tc<kDown>": ("sparse_expert_ffn_gb300/csrc/gemm_tc.cu",),
+    "grouped_gemm_tc<kGateUp>": _TC,
+    "grouped_gemm_tc<kDown>": _TC,
+    "grouped_gemm_dec<kGateUp>": _DEC,
+    "grouped_gemm_dec<kDown>": _DEC,
     "ffn_up_stream": ("sparse_expert_ffn_gb300/csrc/ffn_stream.cu", "sparse_expert_ffn_gb300/csrc/common.cuh"),
     "ffn_down_stream": ("sparse_expert_ffn_gb300/csrc/ffn_stream.cu", "sparse_expert_ffn_gb300/csrc/common.cuh"),
 }
@@ -358,7 +362,10 @@ def run_ours(args):
     # small batch routes and gathers in one kernel, so look at the dtype
     grouped = shape.dtype == "bf16"
     i8 = "_i8" if args.weights == "int8" else ""
-    kname = {("expert_up", True): "grouped_gemm_tc<kGateUp>", ("expert_down", True): "grouped_gemm_tc<kDown>",
+    # decode-sized batches (at most 16 pairs per expert on average) run the
+    # GEMMs with the weights as the MMA's M operand
+    gk = "grouped_gemm_dec" if T * shape.top_k <= 16 * shape.n_experts else "grouped_gemm_tc"
+    kname = {("expert_up", True): gk + "<kGateUp>", ("expert_down", True): gk + "<kDown>",
              ("expert_up", False): "ffn_up_stream" + i8, ("expert_down", False): "ffn_down_stream" + i8}.get(
         (dom, grouped), dom)
     workload = f"{args.workload}_T{T}"
