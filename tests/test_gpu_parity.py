@@ -94,6 +94,17 @@ def test_mixtral_decode_sizes(mixtral, T, executor):
     check_output(mixtral, x64, y, r, l, _sample(T, 32))
 
 
+def test_mixtral_prefill_1024_pairs_and_split_k(mixtral):
+    """~256 pairs per expert: CTA-pair tiles (some experts spill into a
+    second, mostly empty tile) and the down projection split over K."""
+    x, x64 = mixtral.tokens(1024)
+    y, r = mixtral.run(x, "grouped")
+    l, _ = check_routing(mixtral, x64, r)
+    check_output(mixtral, x64, y, r, l, _sample(1024, 48))
+    y2, _ = mixtral.run(x, "grouped")
+    assert torch.equal(y, y2)
+
+
 def test_mixtral_prefill_4096(mixtral):
     x, x64 = mixtral.tokens(4096)
     y, r = mixtral.run(x, "grouped")
