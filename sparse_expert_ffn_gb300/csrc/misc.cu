@@ -31,6 +31,22 @@ __global__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restri
 // When the down projection was split over K, Y holds `nsplit` partial slices
 // `split_stride` floats apart; they are added first, in slice order.  A pair
 // with inv < 0 was dropped by its expert's capacity and adds nothing.
+// Four consecutive outputs in one store (8 bytes of bf16, 16 of float).
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
+// Each thread owns kCombineVec float4 column groups, one block stride apart
+// (coalesced per group), and issues every group's loads of a row before it
+// adds them, so that enough bytes are in flight.
+constexpr int kCombineVec = 4;
+constexpr int kCombineThreads = 128;
+
 template <typename T>
 __global__ void combine_kernel(const float* __restrict__ Y, const float* __restrict__ topk_w,
                                const int32_t* __restrict__ inv, int k, int d, int nsplit,
@@ -38,38 +54,57 @@ __global__ void combine_kernel(const float* __restrict__ Y, const float* __restr
                                const T* resid, T* y) {  // resid may alias y (in-place residual)
     pdl_enter();
     const int t = blockIdx.y;
-    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    if (c >= d) return;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int d4 = d / 4;
+    const int g0 = blockIdx.x * kCombineThreads * kCombineVec + threadIdx.x;   // float4 index
+    float4 acc[kCombineVec];
+#pragma unroll
+    for (int u = 0; u < kCombineVec; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
         const int pos = inv[(size_t)t * k + j];
         if (pos < 0) continue;                      // dropped by the expert's capacity
         const float w = topk_w[(size_t)t * k + j];
-        const float* row = Y + (size_t)pos * d + c;
-        float4 v = *reinterpret_cast<const float4*>(row);
-        for (int sp = 1; sp < nsplit; ++sp) {
-            const float4 p = *reinterpret_cast<const float4*>(row + sp * split_stride);
-            v.x += p.x;
-            v.y += p.y;
-            v.z += p.z;
-            v.w += p.w;
+        const float4* row = reinterpret_cast<const float4*>(Y + (size_t)pos * d);
+        float4 v[kCombineVec];
+#pragma unroll
+        for (int u = 0; u < kCombineVec; ++u) {
+            const int g = g0 + u * kCombineThreads;
+            v[u] = g < d4 ? row[g] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+        for (int sp = 1; sp < nsplit; ++sp) {
+            const float4* prow = row + sp * (split_stride / 4);
+#pragma unroll
+            for (int u = 0; u < kCombineVec; ++u) {
+                const int g = g0 + u * kCombineThreads;
+                if (g < d4) {
+                    const float4 p = prow[g];
+                    v[u].x += p.x;
+                    v[u].y += p.y;
+                    v[u].z += p.z;
+                    v[u].w += p.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kCombineVec; ++u) {
+            acc[u].x = fmaf(w, v[u].x, acc[u].x);
+            acc[u].y = fmaf(w, v[u].y, acc[u].y);
+            acc[u].z = fmaf(w, v[u].z, acc[u].z);
+            acc[u].w = fmaf(w, v[u].w, acc[u].w);
+        }
     }
-    const size_t o = (size_t)t * d + c;
-    if (resid) {
-        acc.x += to_f32(resid[o]);
-        acc.y += to_f32(resid[o + 1]);
-        acc.z += to_f32(resid[o + 2]);
-        acc.w += to_f32(resid[o + 3]);
+#pragma unroll
+    for (int u = 0; u < kCombineVec; ++u) {
+        const int g = g0 + u * kCombineThreads;
+        if (g >= d4) continue;
+        const size_t o = (size_t)t * d + (size_t)g * 4;
+        if (resid) {
+            acc[u].x += to_f32(resid[o]);
+            acc[u].y += to_f32(resid[o + 1]);
+            acc[u].z += to_f32(resid[o + 2]);
+            acc[u].w += to_f32(resid[o + 3]);
+        }
+        store4(y + o, acc[u]);
     }
-    y[o] = from_f32<T>(acc.x);
-    y[o + 1] = from_f32<T>(acc.y);
-    y[o + 2] = from_f32<T>(acc.z);
-    y[o + 3] = from_f32<T>(acc.w);
 }
 
 // RMSNorm: u = h / sqrt(mean(h^2) + eps) * gamma, float32 arithmetic, one
@@ -145,7 +180,8 @@ cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const 
                            int T, int k, int d, int nsplit, size_t split_stride,
                            const void* resid, void* y, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    const dim3 block(128), grid((d / 4 + 127) / 128, T);
+    const int per_block = kCombineThreads * kCombineVec;   // float4 groups per block
+    const dim3 block(kCombineThreads), grid((d / 4 + per_block - 1) / per_block, T);
     cudaError_t e;
     if (dt == DType::BF16)
         e = launch_pdl(combine_kernel<__nv_bfloat16>, grid, block, 0, s, Y, topk_w, inv, k, d,
