@@ -112,6 +112,106 @@ __device__ __forceinline__ void convert_stage(const uint8_t* __restrict__ sq, ui
     }
 }
 
+// Router epilogue: top-k by insertion over a key that puts the larger logit
+// first and the lower expert id first on ties (as the CUDA-core router), then
+// the softmax over the k.  Logits arrive 32 at a time in shared memory (a
+// rolled loop over them keeps the instruction footprint small).
+struct RouterTopk {
+    unsigned long long key[8];
+    float val[8];
+    __device__ __forceinline__ RouterTopk() {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) key[j] = 0ull, val[j] = 0.f;
+    }
+    // logits of experts c .. c + n - 1 in l[0 .. n)
+    __device__ __forceinline__ void insert(const float* l, int c, int n, const float* bias) {
+#pragma unroll 1
+        for (int i = 0; i < n; ++i) {
+            const int e = c + i;
+            float v = l[i];
+            if (bias) v += bias[e];
+            unsigned long long kk =
+                ((unsigned long long)logit_order_key(v) << 32) | (uint32_t)(~(uint32_t)e);
+            float vv = v;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (kk > key[j]) {
+                    const unsigned long long tk = key[j];
+                    const float tv = val[j];
+                    key[j] = kk, val[j] = vv;
+                    kk = tk, vv = tv;
+                }
+            }
+        }
+    }
+    __device__ __forceinline__ void write(const TcGemmArgs& args, size_t t) const {
+        const int k = args.top_k;
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < k) sum += expf(val[j] - val[0]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < k) {
+                args.topk_idx[t * k + j] = (int)(~(uint32_t)(key[j] & 0xffffffffull));
+                args.topk_w[t * k + j] = expf(val[j] - val[0]) / sum;
+            }
+        }
+    }
+};
+
+// Router with K split into slices: every slice's epilogue warp counts itself
+// in on a counter per (tile, lane quarter) once its partial logits are
+// globally visible; the warp that arrives last adds the slices' logits of its
+// 32 rows in slice order (so the sum does not depend on arrival order), routes
+// them and rearms the counter.  Nothing waits on another CTA.
+__device__ __noinline__ void router_split_fixup(const TcGemmArgs& args, const Work& wk, int q,
+                                                int lane, float* mine) {
+    __threadfence();
+    __syncwarp();
+    int* ctr = args.tile_counter + (size_t)wk.tile * 4 + q;
+    int old = 0;
+    if (lane == 0) old = atomicAdd(ctr, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != args.k_splits - 1) return;
+    __threadfence();
+    const int E = args.n_experts;
+    const int ld = args.bn_rows;                  // partial row stride: E padded to 16
+    const int row = q * 32 + lane;
+    const size_t t = (size_t)wk.row0 + row;
+    if (row < wk.rows) {
+        RouterTopk top;
+        for (int c = 0; c < E; c += 32) {
+            const int n = min(32, E - c);
+            const int nv = min(32, ld - c) / 4;   // float4 groups present in the row
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            for (int sl = 0; sl < args.k_splits; ++sl) {
+                // the slice's 32 logits of this chunk: eight loads in flight
+                const float4* src =
+                    reinterpret_cast<const float4*>(args.partial + sl * args.partial_split_stride + t * ld + c);
+                float4 v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = i < nv ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    acc[4 * i] += v[i].x;
+                    acc[4 * i + 1] += v[i].y;
+                    acc[4 * i + 2] += v[i].z;
+                    acc[4 * i + 3] += v[i].w;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mine[i] = acc[i];
+            top.insert(mine, c, n, args.bias);
+        }
+        top.write(args, t);
+    }
+    __syncwarp();
+    if (lane == 0) *ctr = 0;
+}
+
 template <int kMode, bool kPair, bool kI8>
 __global__ void __launch_bounds__(kI8 ? kThreadsI8 : kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -345,57 +445,41 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const size_t orow = (size_t)(wk.row0 + my_row);
             float* stg = reinterpret_cast<float*>(smem + kStagingOffset) + (warp - 2) * 32 * kStgStride;
             if constexpr (kMode == kRouter) {
-                // Logits of this thread's token: the E accumulator columns
-                // (+ offset).  Top-k by insertion over a key that puts the
-                // larger logit first and the lower expert id first on ties,
-                // then the softmax over the k (as the CUDA-core router).
-                unsigned long long key[8];
-                float val[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) key[j] = 0ull, val[j] = 0.f;
-                const int E = args.n_experts;
                 float* mine = stg + lane * 33;     // own row, stride 33: conflict-free
+                if (args.k_splits > 1) {
+                    // One K slice: the thread's float32 partial logits go to
+                    // the slice's buffer [T][E padded to 16] (all bn
+                    // columns); the last slice to arrive on this quarter of
+                    // the tile routes its rows (below).
+                    float* P = args.partial + wk.split * args.partial_split_stride;
 #pragma unroll 1
-                for (int c = 0; c < bn; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + c, v);
-                    tmem_ld_wait();
+                    for (int c = 0; c < bn; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tbase + c, v);
+                        tmem_ld_wait();
+                        if (live) {
+                            float4* dst = reinterpret_cast<float4*>(P + orow * bn + c);
+                            const int nv = min(32, bn - c) / 4;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
-                    const int n = min(32, E - c);
-#pragma unroll 1
-                    for (int i = 0; i < n; ++i) {
-                        const int e = c + i;
-                        float l = mine[i];
-                        if (args.bias) l += args.bias[e];
-                        unsigned long long kk =
-                            ((unsigned long long)logit_order_key(l) << 32) | (uint32_t)(~(uint32_t)e);
-                        float vv = l;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            if (kk > key[j]) {
-                                const unsigned long long tk = key[j];
-                                const float tv = val[j];
-                                key[j] = kk, val[j] = vv;
-                                kk = tk, vv = tv;
-                            }
+                            for (int i = 0; i < 8; ++i)
+                                if (i < nv)
+                                    dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                         __uint_as_float(v[4 * i + 2]),
+                                                         __uint_as_float(v[4 * i + 3]));
                         }
                     }
-                }
-                if (live) {
-                    const int k = args.top_k;
-                    const size_t t = orow;
-                    float sum = 0.f;
+                } else {
+                    RouterTopk top;
+#pragma unroll 1
+                    for (int c = 0; c < bn; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tbase + c, v);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (j < k) sum += expf(val[j] - val[0]);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (j < k) {
-                            args.topk_idx[t * k + j] = (int)(~(uint32_t)(key[j] & 0xffffffffull));
-                            args.topk_w[t * k + j] = expf(val[j] - val[0]) / sum;
-                        }
+                        for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
+                        top.insert(mine, c, min(32, args.n_experts - c), args.bias);
                     }
+                    if (live) top.write(args, orow);
                 }
             } else if constexpr (kMode == kGateUp) {
               if (args.k_splits > 1) {
@@ -484,6 +568,10 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             if constexpr (kMode == kGateUp) {
                 if (args.k_splits > 1) gate_up_split_fixup<kI8>(args, wk, lane);
+            }
+            if constexpr (kMode == kRouter) {
+                if (args.k_splits > 1)
+                    router_split_fixup(args, wk, q, lane, stg + lane * 33);
             }
             if (++acc == 2) acc = 0, acc_phase ^= 1;
         }
@@ -664,8 +752,9 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcG
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b) {
     if (grid <= 0) return cudaSuccess;
-    // the split gate/up fixup counts the four epilogue warps of one CTA per slice
-    if (mode == kGateUp && args.k_splits > 1 && (pair || !args.partial || !args.tile_counter))
+    // the split gate/up and router fixups count epilogue warps of single CTAs
+    if ((mode == kGateUp || mode == kRouter) && args.k_splits > 1 &&
+        (pair || !args.partial || !args.tile_counter))
         return cudaErrorInvalidValue;
     cudaError_t e;
     if (int8_b) {

@@ -134,6 +134,8 @@ constexpr int kMultiDispatchPairs = 12288;
 // Batches from this many tokens route on the tensor cores.
 constexpr int kTcRouterMinTokens = 512;
 constexpr int kMaxKSplit = 16;
+// K slices of the tensor-core router at most (the last slice routes the rows).
+constexpr int kMaxRouterSplit = 8;
 // Batches averaging at most this many (token, slot) pairs per expert run the
 // decode GEMMs (weights as the MMA's M operand, 32-token tiles).
 constexpr int kDecMaxPairsPerExpert = 16;
@@ -350,7 +352,20 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.status = h->status;
         a.wait_limit_ns = h->wait_limit_ns;
         a.stall_producer = h->stall_tma ? 1 : 0;
-        const int grid = std::min((T + tc_gemm_block_m() - 1) / tc_gemm_block_m(), h->num_sms);
+        // At most a quarter as many 128-token tiles as SMs: split K (float32
+        // partial logits in Y, one arrival counter per tile and lane quarter
+        // in gu_counter).  With fewer slices the fixup's latency (fence,
+        // counter, reloading the partials) costs more than the shorter K loop
+        // saves (measured: E = 64, 2 slices, 28 -> 35 us).
+        const int tiles = (T + tc_gemm_block_m() - 1) / tc_gemm_block_m();
+        if (4 * tiles <= h->num_sms) {
+            const int fit = (int)std::min<size_t>(kMaxRouterSplit, h->y_floats / ((size_t)T * h->e_pad));
+            a.k_splits = choose_k_splits(tiles, a.k_blocks, h->num_sms, fit);
+            a.partial = h->Y;
+            a.partial_split_stride = (size_t)T * h->e_pad;
+            a.tile_counter = h->gu_counter;
+        }
+        const int grid = std::min(tiles * a.k_splits, h->num_sms);
         Stage g(h, COLIBRI_STAGE_ROUTER, s);
         st = g.done(launch_tc_gemm(kRouter, false, tm_x, h->tm_wr, a, grid, s), 1);
         if (st != COLIBRI_OK) return st;

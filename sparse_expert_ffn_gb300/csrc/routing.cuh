@@ -66,22 +66,36 @@ __host__ __device__ constexpr size_t dispatch_smem_bytes(int E) {
 // 引擎解析" section 3.3 stage 3: the input slices of one expert packed into one
 // mini-batch).  A warp walks a contiguous range [lo, hi) of r, 32 at a time.
 
+// Both passes read the warp's expert ids kWalkBatch * 32 at a time, the
+// loads of a batch issued before any is used, so that a pass waits for one
+// memory latency per batch instead of one per 32 pairs.
+constexpr int kWalkBatch = 8;
+
 // Pass 1: add the warp's per-expert counts into my[E]: lanes holding the
 // same expert are found with __match_any_sync and the group leader adds the
 // group size (no atomics, so the counts never depend on timing).
 __device__ __forceinline__ void warp_count_pass(const int32_t* __restrict__ topk_idx, int lo,
                                                 int hi, int E, int32_t* my, int* status) {
     const int lane = threadIdx.x & 31;
-    for (int base = lo; base < hi; base += 32) {
-        const int r = base + lane;
-        int e = r < hi ? topk_idx[r] : -1;
-        if (e >= E || (e < 0 && r < hi)) {
-            atomicExch(status, DEV_BAD_INDEX);
-            e = -1;
+    for (int b0 = lo; b0 < hi; b0 += kWalkBatch * 32) {
+        int ev[kWalkBatch];
+#pragma unroll
+        for (int i = 0; i < kWalkBatch; ++i) {
+            const int r = b0 + i * 32 + lane;
+            ev[i] = r < hi ? topk_idx[r] : -1;
         }
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(m) - 1) my[e] += __popc(m);
-        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kWalkBatch; ++i) {
+            const int r = b0 + i * 32 + lane;
+            int e = ev[i];
+            if (e >= E || (e < 0 && r < hi)) {
+                atomicExch(status, DEV_BAD_INDEX);
+                e = -1;
+            }
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && lane == __ffs(m) - 1) my[e] += __popc(m);
+            __syncwarp();
+        }
     }
 }
 
@@ -96,21 +110,30 @@ __device__ __forceinline__ void warp_scatter_pass(const int32_t* __restrict__ to
                                                   int32_t* __restrict__ inv) {
     const int lane = threadIdx.x & 31;
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base = lo; base < hi; base += 32) {
-        const int r = base + lane;
-        int e = r < hi ? topk_idx[r] : -1;
-        if (e >= E) e = -1;
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        int32_t start = 0;
-        if (e >= 0) start = my[e];
-        __syncwarp();
-        if (e >= 0) {
-            const int p = start + __popc(m & lt_mask);
-            perm[p] = r;
-            inv[r] = p - seg_start[e] < cap ? p : -1;
-            if (lane == __ffs(m) - 1) my[e] = start + __popc(m);
+    for (int b0 = lo; b0 < hi; b0 += kWalkBatch * 32) {
+        int ev[kWalkBatch];
+#pragma unroll
+        for (int i = 0; i < kWalkBatch; ++i) {
+            const int r = b0 + i * 32 + lane;
+            ev[i] = r < hi ? topk_idx[r] : -1;
         }
-        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kWalkBatch; ++i) {
+            const int r = b0 + i * 32 + lane;
+            int e = ev[i];
+            if (e >= E) e = -1;
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            int32_t start = 0;
+            if (e >= 0) start = my[e];
+            __syncwarp();
+            if (e >= 0) {
+                const int p = start + __popc(m & lt_mask);
+                perm[p] = r;
+                inv[r] = p - seg_start[e] < cap ? p : -1;
+                if (lane == __ffs(m) - 1) my[e] = start + __popc(m);
+            }
+            __syncwarp();
+        }
     }
 }
 

@@ -358,21 +358,23 @@ __device__ __forceinline__ Work decode_work(int w, int n_blocks, int k_splits,
     return r;
 }
 
-// Router mode: dense m-tiles of 128 consecutive tokens, one n-block.
-__device__ __forceinline__ Work dense_work(int w, int rows_total) {
+// Router mode: dense m-tiles of 128 consecutive tokens, one n-block, K
+// slices fastest.
+__device__ __forceinline__ Work dense_work(int w, int rows_total, int k_splits) {
     Work r;
+    const int t = w / k_splits;
     r.expert = 0;
-    r.row0 = w * kBM;
+    r.row0 = t * kBM;
     r.rows = min(kBM, rows_total - r.row0);
     r.nblk = 0;
-    r.split = 0;
-    r.tile = w;
+    r.split = w - t * k_splits;
+    r.tile = t;
     return r;
 }
 
 template <int kMode>
 __device__ __forceinline__ Work get_work(int w, const TcGemmArgs& a) {
-    if constexpr (kMode == kRouter) return dense_work(w, a.dense_rows);
+    if constexpr (kMode == kRouter) return dense_work(w, a.dense_rows, a.k_splits);
     else return decode_work(w, a.n_blocks, a.k_splits, a.tile_expert, a.tile_row, a.tile_info);
 }
 
