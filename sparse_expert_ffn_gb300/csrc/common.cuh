@@ -131,7 +131,9 @@ __device__ __forceinline__ void load8_cg(const float* p, float (&v)[8]) {
 template <typename T>
 __device__ __forceinline__ void rmsnorm_row_warp(const T* __restrict__ hr, const T* __restrict__ gamma,
                                                  int d, float eps, T* __restrict__ ur, int lane) {
+    // (loops unrolled by 4: four rows' worth of loads in flight per lane)
     float ss = 0.f;
+#pragma unroll 4
     for (int i = lane * 8; i < d; i += 256) {
         float v[8];
         load8(hr + i, v);
@@ -140,6 +142,7 @@ __device__ __forceinline__ void rmsnorm_row_warp(const T* __restrict__ hr, const
     }
     ss = warp_sum(ss);
     const float inv_rms = 1.0f / sqrtf(ss / (float)d + eps);
+#pragma unroll 4
     for (int i = lane * 8; i < d; i += 256) {
         float v[8], g[8];
         load8(hr + i, v);

@@ -46,6 +46,7 @@ __device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<f
 // adds them, so that enough bytes are in flight.
 constexpr int kCombineVec = 4;
 constexpr int kCombineThreads = 128;
+constexpr int kCombineSlices = 4;   // split-K slices loaded together
 
 template <typename T>
 __global__ void combine_kernel(const float* __restrict__ Y, const float* __restrict__ topk_w,
@@ -70,17 +71,28 @@ __global__ void combine_kernel(const float* __restrict__ Y, const float* __restr
             const int g = g0 + u * kCombineThreads;
             v[u] = g < d4 ? row[g] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        for (int sp = 1; sp < nsplit; ++sp) {
-            const float4* prow = row + sp * (split_stride / 4);
+        // split-K slices, added in slice order; the loads of four slices are
+        // issued before any is added
+        for (int sp0 = 1; sp0 < nsplit; sp0 += kCombineSlices) {
+            float4 p[kCombineSlices][kCombineVec];
 #pragma unroll
-            for (int u = 0; u < kCombineVec; ++u) {
-                const int g = g0 + u * kCombineThreads;
-                if (g < d4) {
-                    const float4 p = prow[g];
-                    v[u].x += p.x;
-                    v[u].y += p.y;
-                    v[u].z += p.z;
-                    v[u].w += p.w;
+            for (int i = 0; i < kCombineSlices; ++i) {
+                const float4* prow = row + (size_t)(sp0 + i) * (split_stride / 4);
+#pragma unroll
+                for (int u = 0; u < kCombineVec; ++u) {
+                    const int g = g0 + u * kCombineThreads;
+                    p[i][u] = (sp0 + i < nsplit && g < d4) ? prow[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kCombineSlices; ++i) {
+                if (sp0 + i >= nsplit) break;
+#pragma unroll
+                for (int u = 0; u < kCombineVec; ++u) {
+                    v[u].x += p[i][u].x;
+                    v[u].y += p[i][u].y;
+                    v[u].z += p[i][u].z;
+                    v[u].w += p[i][u].w;
                 }
             }
         }

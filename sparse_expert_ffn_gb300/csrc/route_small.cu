@@ -60,6 +60,7 @@ route_small_kernel(const T* __restrict__ x, const T* __restrict__ wr,
         const T* xr = src + (size_t)t * d + q * seg;
         const T* w = wr + (size_t)e * d + q * seg;
         float s = 0.f;
+#pragma unroll 4
         for (int i = lane * 8; i < seg; i += 256) {
             float xv[8], wv[8];
             load8_cg(xr + i, xv);
