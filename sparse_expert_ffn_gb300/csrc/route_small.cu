@@ -41,12 +41,55 @@ route_small_kernel(const T* __restrict__ x, const T* __restrict__ wr,
     int32_t* dsh = reinterpret_cast<int32_t*>(part + ((ntok * E * nq + 63) & ~63));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // 0. (pre-norm layer) u = RMSNorm(x) * gamma, one warp per token; the
-    // rest of the kernel routes and gathers u, read back through L2.
+    // 0. (pre-norm layer) u = RMSNorm(x) * gamma; the rest of the kernel
+    // routes and gathers u, read back through L2.  With fewer tokens than
+    // warps each row is cut into wpt slices of whole 256-element steps (a
+    // warp each): the slices' sums of squares go through shared memory and
+    // are added in slice order.  Otherwise one warp per token.
     const T* src = x;
     if (gamma) {
-        for (int t = warp; t < ntok; t += kDispatchWarps)
-            rmsnorm_row_warp(x + (size_t)t * d, gamma, d, eps, u + (size_t)t * d, lane);
+        int wpt = 1;
+        while (ntok * wpt * 2 <= kDispatchWarps && d % (256 * wpt * 2) == 0) wpt *= 2;
+        if (wpt == 1) {
+            for (int t = warp; t < ntok; t += kDispatchWarps)
+                rmsnorm_row_warp(x + (size_t)t * d, gamma, d, eps, u + (size_t)t * d, lane);
+        } else {
+            float* ssp = part;                    // [ntok * wpt] <= kDispatchWarps
+            const int seg = d / wpt;
+            const int unit = ntok * wpt;
+            if (warp < unit) {
+                const int t = warp / wpt, sl = warp - t * wpt;
+                const T* hr = x + (size_t)t * d + sl * seg;
+                float ss = 0.f;
+#pragma unroll 4
+                for (int i = lane * 8; i < seg; i += 256) {
+                    float v[8];
+                    load8(hr + i, v);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) ss = fmaf(v[c], v[c], ss);
+                }
+                ss = warp_sum(ss);
+                if (lane == 0) ssp[warp] = ss;
+            }
+            __syncthreads();
+            if (warp < unit) {
+                const int t = warp / wpt, sl = warp - t * wpt;
+                float tot = 0.f;
+                for (int i = 0; i < wpt; ++i) tot += ssp[t * wpt + i];
+                const float inv_rms = 1.0f / sqrtf(tot / (float)d + eps);
+                const T* hr = x + (size_t)t * d + sl * seg;
+                T* ur = u + (size_t)t * d + sl * seg;
+                const T* gr = gamma + sl * seg;
+#pragma unroll 4
+                for (int i = lane * 8; i < seg; i += 256) {
+                    float v[8], g[8];
+                    load8(hr + i, v);
+                    load8(gr + i, g);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) ur[i + c] = from_f32<T>(v[c] * inv_rms * g[c]);
+                }
+            }
+        }
         __syncthreads();
         src = u;
     }
