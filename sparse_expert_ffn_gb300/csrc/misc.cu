@@ -1,4 +1,5 @@
 // Gather, combine, RMSNorm and the init-time weight repack.
+#include <algorithm>
 #include <mutex>
 #include <unordered_map>
 
@@ -10,19 +11,37 @@ namespace colibri {
 namespace {
 
 // Xp[p, :] = x[perm[p] / k, :] — the tokens of every expert as consecutive
-// rows (the A operand of the grouped GEMM).  One CTA per pair row, 16-byte
-// vectors; with kToF16, bf16 rows are converted to f16 (the A type of the
+// rows (the A operand of the grouped GEMM), in 16-byte vectors; with
+// kToF16, bf16 rows are converted to f16 (the A type of the
 // int8-weight GEMMs).
+// A warp copies whole rows, walking p = warp, warp + (warps in the grid), ...
+// with the next row's source index loaded ahead and eight 16-byte loads per
+// lane in flight, so that the copy runs at memory bandwidth instead of one
+// row's latency chain per CTA.
+constexpr int kGatherThreads = 256;
+constexpr int kGatherCtasPerSm = 8;
+
 template <bool kToF16>
-__global__ void gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k,
-                            int row_vecs, uint4* __restrict__ xp) {
+__global__ void __launch_bounds__(kGatherThreads)
+gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k, int row_vecs,
+            int npairs, uint4* __restrict__ xp) {
     pdl_enter();
-    const int p = blockIdx.x;
-    const int t = perm[p] / k;
-    const uint4* src = x + (size_t)t * row_vecs;
-    uint4* dst = xp + (size_t)p * row_vecs;
-    for (int i = threadIdx.x; i < row_vecs; i += blockDim.x)
-        dst[i] = kToF16 ? bf16x8_to_f16x8(src[i]) : src[i];
+    const int lane = threadIdx.x & 31;
+    const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+    int p = gw;
+    int t_next = p < npairs ? perm[p] / k : 0;
+    for (; p < npairs; p += nw) {
+        const int t = t_next;
+        if (p + nw < npairs) t_next = perm[p + nw] / k;
+        const uint4* src = x + (size_t)t * row_vecs;
+        uint4* dst = xp + (size_t)p * row_vecs;
+#pragma unroll 8
+        for (int i = lane; i < row_vecs; i += 32) {
+            const uint4 v = __ldg(src + i);
+            dst[i] = kToF16 ? bf16x8_to_f16x8(v) : v;
+        }
+    }
 }
 
 // Combine: y[t, c] = sum_j w[t, j] * Y[inv[t*k + j], c], j in order, float32;
@@ -48,7 +67,10 @@ constexpr int kCombineVec = 4;
 constexpr int kCombineThreads = 128;
 constexpr int kCombineSlices = 4;   // split-K slices loaded together
 
-template <typename T>
+// kSplit: Y holds more than one K slice (decode-sized batches); without it
+// the kernel keeps no slice buffers (half the registers, twice the resident
+// warps for the bandwidth-bound prefill combine).
+template <typename T, bool kSplit>
 __global__ void combine_kernel(const float* __restrict__ Y, const float* __restrict__ topk_w,
                                const int32_t* __restrict__ inv, int k, int d, int nsplit,
                                size_t split_stride,
@@ -73,6 +95,7 @@ __global__ void combine_kernel(const float* __restrict__ Y, const float* __restr
         }
         // split-K slices, added in slice order; the loads of four slices are
         // issued before any is added
+        if constexpr (kSplit) {
         for (int sp0 = 1; sp0 < nsplit; sp0 += kCombineSlices) {
             float4 p[kCombineSlices][kCombineVec];
 #pragma unroll
@@ -95,6 +118,7 @@ __global__ void combine_kernel(const float* __restrict__ Y, const float* __restr
                     v[u].w += p[i][u].w;
                 }
             }
+        }
         }
 #pragma unroll
         for (int u = 0; u < kCombineVec; ++u) {
@@ -163,11 +187,21 @@ cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, in
                           int npairs, void* xp, cudaStream_t s, bool to_f16) {
     if (npairs <= 0) return cudaSuccess;
     const int row_vecs = d * elem_bytes / 16;
+    static int sms = 0;
+    if (sms <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            sms = 1;
+    }
+    const int warps_per_cta = kGatherThreads / 32;
+    const int grid = std::max(1, std::min((npairs + warps_per_cta - 1) / warps_per_cta,
+                                          sms * kGatherCtasPerSm));
     const cudaError_t e =
-        to_f16 ? launch_pdl(gather_rows<true>, npairs, 128, 0, s, (const uint4*)x, perm, k, row_vecs,
-                            (uint4*)xp)
-               : launch_pdl(gather_rows<false>, npairs, 128, 0, s, (const uint4*)x, perm, k,
-                            row_vecs, (uint4*)xp);
+        to_f16 ? launch_pdl(gather_rows<true>, grid, kGatherThreads, 0, s, (const uint4*)x, perm, k,
+                            row_vecs, npairs, (uint4*)xp)
+               : launch_pdl(gather_rows<false>, grid, kGatherThreads, 0, s, (const uint4*)x, perm, k,
+                            row_vecs, npairs, (uint4*)xp);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -195,12 +229,22 @@ cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const 
     const int per_block = kCombineThreads * kCombineVec;   // float4 groups per block
     const dim3 block(kCombineThreads), grid((d / 4 + per_block - 1) / per_block, T);
     cudaError_t e;
-    if (dt == DType::BF16)
-        e = launch_pdl(combine_kernel<__nv_bfloat16>, grid, block, 0, s, Y, topk_w, inv, k, d,
-                       nsplit, split_stride, (const __nv_bfloat16*)resid, (__nv_bfloat16*)y);
-    else
-        e = launch_pdl(combine_kernel<float>, grid, block, 0, s, Y, topk_w, inv, k, d, nsplit,
-                       split_stride, (const float*)resid, (float*)y);
+    const bool split = nsplit > 1;
+    if (dt == DType::BF16) {
+        const auto* r = (const __nv_bfloat16*)resid;
+        auto* o = (__nv_bfloat16*)y;
+        e = split ? launch_pdl(combine_kernel<__nv_bfloat16, true>, grid, block, 0, s, Y, topk_w, inv,
+                               k, d, nsplit, split_stride, r, o)
+                  : launch_pdl(combine_kernel<__nv_bfloat16, false>, grid, block, 0, s, Y, topk_w, inv,
+                               k, d, nsplit, split_stride, r, o);
+    } else {
+        const auto* r = (const float*)resid;
+        auto* o = (float*)y;
+        e = split ? launch_pdl(combine_kernel<float, true>, grid, block, 0, s, Y, topk_w, inv, k, d,
+                               nsplit, split_stride, r, o)
+                  : launch_pdl(combine_kernel<float, false>, grid, block, 0, s, Y, topk_w, inv, k, d,
+                               nsplit, split_stride, r, o);
+    }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
