@@ -50,10 +50,12 @@ dispatch_count_kernel(const int32_t* __restrict__ topk_idx, int n, int E,
     }
 }
 
+constexpr size_t kScanSmemMax = 160 * 1024;   // block counts staged in shared memory up to this
+
 // 2. one CTA: expert counts, offsets, every CTA's base in every expert
 //    segment (CTAs in order), and the tile list
 __global__ void __launch_bounds__(kDispatchWarps * 32)
-dispatch_scan_kernel(int32_t* __restrict__ block_counts, int nb, int E,
+dispatch_scan_kernel(int32_t* block_counts, int nb, int E, int staged,
                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int bm,
                      int32_t* __restrict__ tile_expert, int32_t* __restrict__ tile_row,
                      int32_t* __restrict__ tile_info, int32_t* __restrict__ num_tiles, int cap,
@@ -61,9 +63,30 @@ dispatch_scan_kernel(int32_t* __restrict__ block_counts, int nb, int E,
     pdl_enter();
     __shared__ int32_t ecount[256], eoff[257], tbase[257];
     const int e = threadIdx.x;
+    // every (block, expert) count is read once into shared memory, eight
+    // loads in flight per thread, then walked from there (batches whose
+    // counts do not fit walk them in global memory)
+    extern __shared__ int32_t bc_sh[];   // [nb][E] when staged
+    const int32_t* bc = staged ? bc_sh : block_counts;
+    if (staged) {
+        for (int i = threadIdx.x; i < nb * E; i += blockDim.x * 8) {
+            int32_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = i + u * blockDim.x;
+                v[u] = j < nb * E ? block_counts[j] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = i + u * blockDim.x;
+                if (j < nb * E) bc_sh[j] = v[u];
+            }
+        }
+    }
+    __syncthreads();
     if (e < E) {
         int32_t c = 0;
-        for (int b = 0; b < nb; ++b) c += block_counts[b * E + e];
+        for (int b = 0; b < nb; ++b) c += bc[b * E + e];
         ecount[e] = c;
     }
     __syncthreads();
@@ -82,8 +105,8 @@ dispatch_scan_kernel(int32_t* __restrict__ block_counts, int nb, int E,
     __syncthreads();
     if (e < E) {
         int32_t run = eoff[e];
-        for (int b = 0; b < nb; ++b) {     // counts -> bases, in place
-            const int32_t c = block_counts[b * E + e];
+        for (int b = 0; b < nb; ++b) {     // counts -> bases
+            const int32_t c = bc[b * E + e];
             block_counts[b * E + e] = run;
             run += c;
         }
@@ -140,9 +163,14 @@ cudaError_t launch_dispatch_multi(const int32_t* topk_idx, int n, int E, int32_t
     const dim3 block(kDispatchWarps * 32);
     cudaError_t e = launch_pdl(dispatch_count_kernel, nb, block, smem, s, topk_idx, n, E,
                                block_counts, status);
-    if (e == cudaSuccess)
-        e = launch_pdl(dispatch_scan_kernel, 1, block, 0, s, block_counts, nb, E, counts, offsets,
-                       bm, tile_expert, tile_row, tile_info, num_tiles, cap, kept);
+    if (e == cudaSuccess) {
+        const size_t need = (size_t)nb * E * sizeof(int32_t);
+        const int staged = need <= kScanSmemMax ? 1 : 0;
+        const size_t scan_smem = staged ? need : 0;
+        if (staged) smem_attr((const void*)dispatch_scan_kernel, (int)scan_smem);
+        e = launch_pdl(dispatch_scan_kernel, 1, block, scan_smem, s, block_counts, nb, E, staged,
+                       counts, offsets, bm, tile_expert, tile_row, tile_info, num_tiles, cap, kept);
+    }
     if (e == cudaSuccess)
         e = launch_pdl(dispatch_scatter_kernel, nb, block, smem, s, topk_idx, n, E, block_counts,
                        offsets, cap, perm, inv, status);
