@@ -103,7 +103,7 @@ def algorithmic(shape, T, counts, weights="bf16"):
         # per kernel
         "up_flops": 4 * T * k * d * f, "down_flops": 2 * T * k * d * f,
         "up_bytes": int(active * 2 * w + T * d * s + T * k * f * s),
-        "down_bytes": int(active * w + T * k * f * s + T * k * d * 4),
+        "down_bytes": int(active * w + T * k * f * s + T * k * d * s),
     }
 
 

@@ -81,6 +81,10 @@ constexpr uint32_t kRingBytes = 192 * 1024;   // shared-memory ring of every ins
 constexpr uint32_t kStagingOffset = kRingBytes + 512;   // after the ring and the barriers
 constexpr int kStgStride = 36;                           // floats per staged row
 constexpr uint32_t kStgWarpBytes = 32 * kStgStride * 4;  // 4608
+// Router: each epilogue warp's copy of the logit offset (E <= 256 floats),
+// so that the top-k insertion loop reads it from shared memory
+constexpr uint32_t kBiasOffset = kStagingOffset + 4 * kStgWarpBytes;
+constexpr uint32_t kBiasWarpBytes = 256 * 4;
 constexpr int kMaxRouterStages = 12;
 constexpr int kAccCols = 256;     // TMEM columns per accumulator
 constexpr int kTmemCols = 512;    // two accumulators
@@ -166,7 +170,7 @@ struct RouterTopk {
 // 32 rows in slice order (so the sum does not depend on arrival order), routes
 // them and rearms the counter.  Nothing waits on another CTA.
 __device__ __noinline__ void router_split_fixup(const TcGemmArgs& args, const Work& wk, int q,
-                                                int lane, float* mine) {
+                                                int lane, float* mine, const float* bias) {
     __threadfence();
     __syncwarp();
     int* ctr = args.tile_counter + (size_t)wk.tile * 4 + q;
@@ -204,7 +208,7 @@ __device__ __noinline__ void router_split_fixup(const TcGemmArgs& args, const Wo
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) mine[i] = acc[i];
-            top.insert(mine, c, n, args.bias);
+            top.insert(mine, c, n, bias);
         }
         top.write(args, t);
     }
@@ -428,6 +432,16 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;       // row of this CTA's 128-row half
+        // router: this warp's copy of the logit offset
+        const float* bias_sh = nullptr;
+        if constexpr (kMode == kRouter) {
+            if (args.bias) {
+                float* b = reinterpret_cast<float*>(smem + kBiasOffset) + (warp - 2) * (kBiasWarpBytes / 4);
+                for (int e = lane; e < args.n_experts; e += 32) b[e] = args.bias[e];
+                __syncwarp();
+                bias_sh = b;
+            }
+        }
         const uint32_t acc_empty_leader0 =
             kPair ? map_to_rank(smem_u32(&acc_empty[0]), 0) : smem_u32(&acc_empty[0]);
         int acc = 0;
@@ -477,7 +491,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
-                        top.insert(mine, c, min(32, args.n_experts - c), args.bias);
+                        top.insert(mine, c, min(32, args.n_experts - c), bias_sh);
                     }
                     if (live) top.write(args, orow);
                 }
@@ -531,10 +545,12 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
               }
             } else {
-                // Y (float32) for this thread's row, 32 columns per chunk,
-                // staged and stored as 128-byte row segments, 4 rows per warp
-                // instruction.
+                // Y for this thread's row, 32 columns per chunk, staged and
+                // stored as row segments, 4 rows per warp instruction: float32
+                // (128 bytes a row), or bf16 (64 bytes) when the GEMM has no K
+                // slices and args.y_bf16 is set.
                 float* Y = reinterpret_cast<float*>(args.out) + wk.split * args.out_split_stride;
+                __nv_bfloat16* Yb = reinterpret_cast<__nv_bfloat16*>(args.out);
                 const int row_base = (int)rank * kBM + q * 32;
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
@@ -552,8 +568,16 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         const int rr = it * 4 + (lane >> 3), c4 = lane & 7;
                         if (row_base + rr < wk.rows) {
                             const float4 val = reinterpret_cast<const float4*>(stg + rr * kStgStride)[c4];
-                            reinterpret_cast<float4*>(Y + (size_t)(wk.row0 + row_base + rr) * args.out_ld +
-                                                      wk.nblk * kBN + c * 32)[c4] = val;
+                            const size_t o = (size_t)(wk.row0 + row_base + rr) * args.out_ld + wk.nblk * kBN +
+                                             c * 32 + c4 * 4;
+                            if (args.y_bf16) {
+                                uint2 pk;
+                                pk.x = pack_h2<false>(val.x, val.y);
+                                pk.y = pack_h2<false>(val.z, val.w);
+                                *reinterpret_cast<uint2*>(Yb + o) = pk;
+                            } else {
+                                *reinterpret_cast<float4*>(Y + o) = val;
+                            }
                         }
                     }
                     __syncwarp();
@@ -571,7 +595,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             }
             if constexpr (kMode == kRouter) {
                 if (args.k_splits > 1)
-                    router_split_fixup(args, wk, q, lane, stg + lane * 33);
+                    router_split_fixup(args, wk, q, lane, stg + lane * 33, bias_sh);
             }
             if (++acc == 2) acc = 0, acc_phase ^= 1;
         }
@@ -704,7 +728,7 @@ EncodeTiledFn encode_fn() {
 
 size_t tc_gemm_smem_bytes() {
     // ring + barriers (512 B) + 4 epilogue staging tiles + 1024-byte alignment slack
-    return (size_t)kStagingOffset + 4 * kStgWarpBytes + 1024;
+    return (size_t)kBiasOffset + 1024;
 }
 int tc_gemm_block_m() { return kBM; }
 int tc_gemm_pair_rows() { return 2 * kBM; }
@@ -729,7 +753,8 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 template <int kMode, bool kPair, bool kI8 = false>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcGemmArgs& args,
                        int grid, cudaStream_t s) {
-    const size_t smem = tc_gemm_smem_bytes();
+    // the router's epilogue warps also keep the logit offset in shared memory
+    const size_t smem = tc_gemm_smem_bytes() + (kMode == kRouter ? 4 * kBiasWarpBytes : 0);
     auto k = grouped_gemm_tc<kMode, kPair, kI8>;
     smem_attr((const void*)k, (int)smem);
     cudaLaunchConfig_t cfg = {};
@@ -752,6 +777,8 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcG
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b) {
     if (grid <= 0) return cudaSuccess;
+    // bf16 Y: the down projection's rows, not K slices
+    if (args.y_bf16 && (mode != kDown || args.k_splits > 1)) return cudaErrorInvalidValue;
     // the split gate/up and router fixups count epilogue warps of single CTAs
     if ((mode == kGateUp || mode == kRouter) && args.k_splits > 1 &&
         (pair || !args.partial || !args.tile_counter))

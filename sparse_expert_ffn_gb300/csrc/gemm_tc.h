@@ -20,6 +20,7 @@ struct TcGemmArgs {
                                  // non-empty; kDown: slice s writes out + s * out_split_stride
     int b_rows_per_expert;       // rows of the packed B operand per expert
     void* out;                   // H (bf16, kGateUp) or Y (float32, kDown)
+    int y_bf16;                  // kDown without K slices: Y stored as bf16 (one rounding)
     int out_ld;                  // row stride of `out` in elements
     size_t out_split_stride;     // elements between the outputs of two K slices
     // kGateUp with k_splits > 1 (single CTAs only): float32 G|U partials

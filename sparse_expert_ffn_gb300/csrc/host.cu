@@ -393,6 +393,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     }
     int nsplit = 1;
     size_t split_stride = 0;
+    bool y_bf16 = false;     // Y rows stored as bf16 by the down GEMM
     if (ex == COLIBRI_EXEC_STREAM) {
         {
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
@@ -490,6 +491,10 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             a.k_splits = choose_k_splits(tiles_est * a.n_blocks, a.k_blocks, units, fit);
         }
         a.out_split_stride = (size_t)npairs * d;
+        // Without K slices the token-on-M GEMM stores Y as bf16 (one
+        // rounding, as H): the combine, bound by reading Y, reads half.
+        a.y_bf16 = (!dec && a.k_splits == 1) ? 1 : 0;
+        y_bf16 = a.y_bf16 != 0;
         {
             const int grid = cta_per_unit * (int)std::min<int64_t>(
                                                     (int64_t)tiles_ub * a.n_blocks * a.k_splits, units);
@@ -506,8 +511,8 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     }
     {
         Stage g(h, COLIBRI_STAGE_COMBINE, s);
-        st = g.done(launch_combine(h->dt, h->Y, h->topk_w, h->inv, T, k, d, nsplit, split_stride,
-                                   resid, y, s), 1);
+        st = g.done(launch_combine(h->dt, h->Y, y_bf16, h->topk_w, h->inv, T, k, d, nsplit,
+                                   split_stride, resid, y, s), 1);
         if (st != COLIBRI_OK) return st;
     }
     h->last_T = T;

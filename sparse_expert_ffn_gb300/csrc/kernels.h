@@ -65,8 +65,9 @@ cudaError_t launch_ffn_down_stream_i8(DType dt, const void* H, const int8_t* wq,
 
 cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,
                           int npairs, void* xp, cudaStream_t s, bool to_f16 = false);
-cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const int32_t* inv,
-                           int T, int k, int d, int nsplit, size_t split_stride,
+// y_bf16: Y holds the down projection's rows as bf16 (no K slices).
+cudaError_t launch_combine(DType dt, const float* Y, bool y_bf16, const float* topk_w,
+                           const int32_t* inv, int T, int k, int d, int nsplit, size_t split_stride,
                            const void* resid, void* y, cudaStream_t s);
 cudaError_t launch_rmsnorm(DType dt, const void* h, const void* gamma, int T, int d, float eps,
                            void* u, cudaStream_t s);

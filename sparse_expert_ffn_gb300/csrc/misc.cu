@@ -67,11 +67,23 @@ constexpr int kCombineVec = 4;
 constexpr int kCombineThreads = 128;
 constexpr int kCombineSlices = 4;   // split-K slices loaded together
 
-// kSplit: Y holds more than one K slice (decode-sized batches); without it
-// the kernel keeps no slice buffers (half the registers, twice the resident
-// warps for the bandwidth-bound prefill combine).
-template <typename T, bool kSplit>
-__global__ void combine_kernel(const float* __restrict__ Y, const float* __restrict__ topk_w,
+// Four consecutive Y values as float4: float32 rows, or bf16 rows (8 bytes).
+__device__ __forceinline__ float4 load_y4(const float* row, int g) {
+    return reinterpret_cast<const float4*>(row)[g];
+}
+__device__ __forceinline__ float4 load_y4(const __nv_bfloat16* row, int g) {
+    const uint2 u = reinterpret_cast<const uint2*>(row)[g];
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// kSplit: Y holds more than one K slice (decode-sized batches, float32);
+// without it the kernel keeps no slice buffers (half the registers, twice
+// the resident warps for the bandwidth-bound prefill combine).  TY: the
+// type Y was stored in (bf16 for prefill on the tensor cores).
+template <typename T, bool kSplit, typename TY>
+__global__ void combine_kernel(const TY* __restrict__ Y, const float* __restrict__ topk_w,
                                const int32_t* __restrict__ inv, int k, int d, int nsplit,
                                size_t split_stride,
                                const T* resid, T* y) {  // resid may alias y (in-place residual)
@@ -86,16 +98,18 @@ __global__ void combine_kernel(const float* __restrict__ Y, const float* __restr
         const int pos = inv[(size_t)t * k + j];
         if (pos < 0) continue;                      // dropped by the expert's capacity
         const float w = topk_w[(size_t)t * k + j];
-        const float4* row = reinterpret_cast<const float4*>(Y + (size_t)pos * d);
+        const TY* yrow = Y + (size_t)pos * d;
         float4 v[kCombineVec];
 #pragma unroll
         for (int u = 0; u < kCombineVec; ++u) {
             const int g = g0 + u * kCombineThreads;
-            v[u] = g < d4 ? row[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u] = g < d4 ? load_y4(yrow, g) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         // split-K slices, added in slice order; the loads of four slices are
         // issued before any is added
         if constexpr (kSplit) {
+        static_assert(!kSplit || sizeof(TY) == 4, "K slices are float32");
+        const float4* row = reinterpret_cast<const float4*>(yrow);
         for (int sp0 = 1; sp0 < nsplit; sp0 += kCombineSlices) {
             float4 p[kCombineSlices][kCombineVec];
 #pragma unroll
@@ -222,10 +236,11 @@ cudaError_t smem_attr(const void* kernel, int bytes) {
     return e;
 }
 
-cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const int32_t* inv,
-                           int T, int k, int d, int nsplit, size_t split_stride,
+cudaError_t launch_combine(DType dt, const float* Y, bool y_bf16, const float* topk_w,
+                           const int32_t* inv, int T, int k, int d, int nsplit, size_t split_stride,
                            const void* resid, void* y, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
+    if (y_bf16 && (nsplit > 1 || dt != DType::BF16)) return cudaErrorInvalidValue;
     const int per_block = kCombineThreads * kCombineVec;   // float4 groups per block
     const dim3 block(kCombineThreads), grid((d / 4 + per_block - 1) / per_block, T);
     cudaError_t e;
@@ -233,17 +248,22 @@ cudaError_t launch_combine(DType dt, const float* Y, const float* topk_w, const 
     if (dt == DType::BF16) {
         const auto* r = (const __nv_bfloat16*)resid;
         auto* o = (__nv_bfloat16*)y;
-        e = split ? launch_pdl(combine_kernel<__nv_bfloat16, true>, grid, block, 0, s, Y, topk_w, inv,
-                               k, d, nsplit, split_stride, r, o)
-                  : launch_pdl(combine_kernel<__nv_bfloat16, false>, grid, block, 0, s, Y, topk_w, inv,
-                               k, d, nsplit, split_stride, r, o);
+        if (y_bf16)
+            e = launch_pdl(combine_kernel<__nv_bfloat16, false, __nv_bfloat16>, grid, block, 0, s,
+                           (const __nv_bfloat16*)Y, topk_w, inv, k, d, nsplit, split_stride, r, o);
+        else if (split)
+            e = launch_pdl(combine_kernel<__nv_bfloat16, true, float>, grid, block, 0, s, Y, topk_w,
+                           inv, k, d, nsplit, split_stride, r, o);
+        else
+            e = launch_pdl(combine_kernel<__nv_bfloat16, false, float>, grid, block, 0, s, Y, topk_w,
+                           inv, k, d, nsplit, split_stride, r, o);
     } else {
         const auto* r = (const float*)resid;
         auto* o = (float*)y;
-        e = split ? launch_pdl(combine_kernel<float, true>, grid, block, 0, s, Y, topk_w, inv, k, d,
-                               nsplit, split_stride, r, o)
-                  : launch_pdl(combine_kernel<float, false>, grid, block, 0, s, Y, topk_w, inv, k, d,
-                               nsplit, split_stride, r, o);
+        e = split ? launch_pdl(combine_kernel<float, true, float>, grid, block, 0, s, Y, topk_w, inv,
+                               k, d, nsplit, split_stride, r, o)
+                  : launch_pdl(combine_kernel<float, false, float>, grid, block, 0, s, Y, topk_w, inv,
+                               k, d, nsplit, split_stride, r, o);
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
