@@ -65,7 +65,7 @@ def parse_args(argv=None):
                          "selects soft routing (every expert, softmax over all logits)")
     ap.add_argument("--weights", choices=["bf16", "int8"], default="bf16",
                     help="expert weight format: bf16, or int8 64x64 blocks (converted on the host, "
-                         "streamed and dequantised on CUDA cores)")
+                         "dequantised to f16 by converter warps of the tensor-core GEMMs)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the decode-size sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
