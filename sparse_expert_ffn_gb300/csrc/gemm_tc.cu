@@ -119,13 +119,17 @@ __device__ __forceinline__ void convert_stage(const uint8_t* __restrict__ sq, ui
 // Router epilogue: top-k by insertion over a key that puts the larger logit
 // first and the lower expert id first on ties (as the CUDA-core router), then
 // the softmax over the k.  Logits arrive 32 at a time in shared memory (a
-// rolled loop over them keeps the instruction footprint small).
+// rolled loop over them keeps the instruction footprint small).  K >= k
+// slots: every logit runs a chain of K compare-and-swaps, the thread's
+// critical path when E is large, so the list is as short as the layer's k
+// allows (1, 2, 4 or 8).
+template <int K>
 struct RouterTopk {
-    unsigned long long key[8];
-    float val[8];
+    unsigned long long key[K];
+    float val[K];
     __device__ __forceinline__ RouterTopk() {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) key[j] = 0ull, val[j] = 0.f;
+        for (int j = 0; j < K; ++j) key[j] = 0ull, val[j] = 0.f;
     }
     // logits of experts c .. c + n - 1 in l[0 .. n)
     __device__ __forceinline__ void insert(const float* l, int c, int n, const float* bias) {
@@ -138,7 +142,7 @@ struct RouterTopk {
                 ((unsigned long long)logit_order_key(v) << 32) | (uint32_t)(~(uint32_t)e);
             float vv = v;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < K; ++j) {
                 if (kk > key[j]) {
                     const unsigned long long tk = key[j];
                     const float tv = val[j];
@@ -152,10 +156,10 @@ struct RouterTopk {
         const int k = args.top_k;
         float sum = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < K; ++j)
             if (j < k) sum += expf(val[j] - val[0]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < K; ++j) {
             if (j < k) {
                 args.topk_idx[t * k + j] = (int)(~(uint32_t)(key[j] & 0xffffffffull));
                 args.topk_w[t * k + j] = expf(val[j] - val[0]) / sum;
@@ -164,27 +168,16 @@ struct RouterTopk {
     }
 };
 
-// Router with K split into slices: every slice's epilogue warp counts itself
-// in on a counter per (tile, lane quarter) once its partial logits are
-// globally visible; the warp that arrives last adds the slices' logits of its
-// 32 rows in slice order (so the sum does not depend on arrival order), routes
-// them and rearms the counter.  Nothing waits on another CTA.
-__device__ __noinline__ void router_split_fixup(const TcGemmArgs& args, const Work& wk, int q,
-                                                int lane, float* mine, const float* bias) {
-    __threadfence();
-    __syncwarp();
-    int* ctr = args.tile_counter + (size_t)wk.tile * 4 + q;
-    int old = 0;
-    if (lane == 0) old = atomicAdd(ctr, 1);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old != args.k_splits - 1) return;
-    __threadfence();
+// The last slice's rows: slices' logits added in slice order, then routed.
+template <int K>
+__device__ __forceinline__ void router_fixup_rows(const TcGemmArgs& args, const Work& wk, int q,
+                                                  int lane, float* mine, const float* bias) {
     const int E = args.n_experts;
     const int ld = args.bn_rows;                  // partial row stride: E padded to 16
     const int row = q * 32 + lane;
     const size_t t = (size_t)wk.row0 + row;
     if (row < wk.rows) {
-        RouterTopk top;
+        RouterTopk<K> top;
         for (int c = 0; c < E; c += 32) {
             const int n = min(32, E - c);
             const int nv = min(32, ld - c) / 4;   // float4 groups present in the row
@@ -212,6 +205,48 @@ __device__ __noinline__ void router_split_fixup(const TcGemmArgs& args, const Wo
         }
         top.write(args, t);
     }
+}
+
+
+// Whole-K router rows: the thread's E logits from its TMEM lane, 32 at a
+// time through shared memory, then the top-k and softmax.
+template <int K>
+__device__ __forceinline__ void router_rows_tmem(uint32_t tbase, int bn, float* mine,
+                                                 const TcGemmArgs& args, const float* bias, bool live,
+                                                 size_t orow) {
+    RouterTopk<K> top;
+#pragma unroll 1
+    for (int c = 0; c < bn; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tbase + c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
+        top.insert(mine, c, min(32, args.n_experts - c), bias);
+    }
+    if (live) top.write(args, orow);
+}
+
+// Router with K split into slices: every slice's epilogue warp counts itself
+// in on a counter per (tile, lane quarter) once its partial logits are
+// globally visible; the warp that arrives last adds the slices' logits of its
+// 32 rows in slice order (so the sum does not depend on arrival order), routes
+// them and rearms the counter.  Nothing waits on another CTA.
+__device__ __noinline__ void router_split_fixup(const TcGemmArgs& args, const Work& wk, int q,
+                                                int lane, float* mine, const float* bias) {
+    __threadfence();
+    __syncwarp();
+    int* ctr = args.tile_counter + (size_t)wk.tile * 4 + q;
+    int old = 0;
+    if (lane == 0) old = atomicAdd(ctr, 1);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != args.k_splits - 1) return;
+    __threadfence();
+    const int k = args.top_k;
+    if (k <= 1) router_fixup_rows<1>(args, wk, q, lane, mine, bias);
+    else if (k <= 2) router_fixup_rows<2>(args, wk, q, lane, mine, bias);
+    else if (k <= 4) router_fixup_rows<4>(args, wk, q, lane, mine, bias);
+    else router_fixup_rows<8>(args, wk, q, lane, mine, bias);
     __syncwarp();
     if (lane == 0) *ctr = 0;
 }
@@ -483,17 +518,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         }
                     }
                 } else {
-                    RouterTopk top;
-#pragma unroll 1
-                    for (int c = 0; c < bn; c += 32) {
-                        uint32_t v[32];
-                        tmem_ld32(tbase + c, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
-                        top.insert(mine, c, min(32, args.n_experts - c), bias_sh);
-                    }
-                    if (live) top.write(args, orow);
+                    const int k = args.top_k;
+                    if (k <= 1) router_rows_tmem<1>(tbase, bn, mine, args, bias_sh, live, orow);
+                    else if (k <= 2) router_rows_tmem<2>(tbase, bn, mine, args, bias_sh, live, orow);
+                    else if (k <= 4) router_rows_tmem<4>(tbase, bn, mine, args, bias_sh, live, orow);
+                    else router_rows_tmem<8>(tbase, bn, mine, args, bias_sh, live, orow);
                 }
             } else if constexpr (kMode == kGateUp) {
               if (args.k_splits > 1) {
