@@ -162,12 +162,33 @@ colibri_status_t colibri_forward(colibri_moe_t* h, const void* x, int32_t T, voi
 
 /*
  * colibri_forward_host - the same layer on host buffers: copies x to the
- * device, runs colibri_forward, copies y back and waits for the stream.
+ * device, runs colibri_forward, copies y back and waits until y_host holds
+ * the result.
  *   x_host, y_host [T, d_model] host memory (pinned recommended), dtype.
  * Uses the workspace's own device copies of x and y (no allocation).
  */
 colibri_status_t colibri_forward_host(colibri_moe_t* h, const void* x_host, int32_t T,
                                       void* y_host, void* stream);
+
+/*
+ * colibri_forward_host_async - colibri_forward_host without the wait, for
+ * pipelining a sequence of batches: the upload of x and the download of y run
+ * on two copy streams of the handle, and successive calls alternate between
+ * two staging slots, so that one call's upload and the previous call's
+ * download overlap the layer of another.  The layer itself runs on `stream`
+ * after the upload; every call on one handle must pass the same stream.
+ * x_host must stay unchanged and y_host must not be read until
+ * colibri_host_wait returns.  With pageable host memory the copies are not
+ * asynchronous (pin both buffers).  Returns an error without waiting.
+ */
+colibri_status_t colibri_forward_host_async(colibri_moe_t* h, const void* x_host, int32_t T,
+                                            void* y_host, void* stream);
+
+/*
+ * colibri_host_wait - wait until every colibri_forward_host_async call on the
+ * handle has finished and written its y_host.
+ */
+colibri_status_t colibri_host_wait(colibri_moe_t* h);
 
 /*
  * colibri_rmsnorm_moe_residual - one layer of a pre-norm decode stack

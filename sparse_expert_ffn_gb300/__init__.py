@@ -60,6 +60,8 @@ def _load():
         "colibri_quantize_int8_block64": ([P, I32, I32, I32, P, P, P], I32),
         "colibri_forward": ([P, P, I32, P, P], I32),
         "colibri_forward_host": ([P, P, I32, P, P], I32),
+        "colibri_forward_host_async": ([P, P, I32, P, P], I32),
+        "colibri_host_wait": ([P], I32),
         "colibri_rmsnorm_moe_residual": ([P, P, I32, P, ctypes.c_float, P], I32),
         "colibri_get_routing": ([P, P, P, P, P, P], I32),
         "colibri_set_executor": ([P, I32], I32),
@@ -81,7 +83,8 @@ def _load():
 
 
 _lib = None
-_C_NAMES = ("colibri_init", "colibri_init_int8", "colibri_quantize_int8_block64", "colibri_forward", "colibri_forward_host",
+_C_NAMES = ("colibri_init", "colibri_init_int8", "colibri_quantize_int8_block64", "colibri_forward",
+            "colibri_forward_host", "colibri_forward_host_async", "colibri_host_wait",
             "colibri_rmsnorm_moe_residual", "colibri_get_routing", "colibri_set_executor",
             "colibri_set_capacity",
             "colibri_check", "colibri_launch_count", "colibri_workspace_bytes",
@@ -239,6 +242,20 @@ class MoELayer:
                                     _stream_ptr(stream)), "colibri_forward_host")
         self.last_T = x_host.shape[0]
         return y_host
+
+    def forward_host_async(self, x_host, y_host, stream=None):
+        """forward_host without the wait (pinned host tensors; successive calls
+        overlap their copies with each other's layer).  y_host holds the result
+        after host_wait(); x_host must not change before then."""
+        _check(library().colibri_forward_host_async(self._h, _ptr(x_host), x_host.shape[0],
+                                                    _ptr(y_host), _stream_ptr(stream)),
+               "colibri_forward_host_async")
+        self.last_T = x_host.shape[0]
+        return y_host
+
+    def host_wait(self):
+        """Wait for every forward_host_async call on this layer."""
+        _check(library().colibri_host_wait(self._h), "colibri_host_wait")
 
     def rmsnorm_moe_residual(self, hidden, gamma, eps: float, stream=None):
         """hidden <- hidden + MoE(RMSNorm(hidden) * gamma), in place."""

@@ -76,8 +76,16 @@ struct colibri_moe {
     void* xp = nullptr;     // [max_pairs, d] token rows in expert order
     float* Y = nullptr;     // [max_pairs, d]
     void* u = nullptr;      // [max_tokens, d]
+    // host-buffer forwards: two staging slots of x and y ([2][max_tokens, d]),
+    // an upload and a download stream, and per slot the events "x landed",
+    // "layer done" and "y downloaded"
     void* x_stage = nullptr;
     void* y_stage = nullptr;
+    size_t stage_bytes = 0;   // bytes of one slot
+    cudaStream_t cs_in = nullptr, cs_out = nullptr;
+    cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr},
+                ev_out[2] = {nullptr, nullptr};
+    int host_slot = 0;
     int max_pairs = 0;
     int max_tiles = 0;
     int max_resident_pairs = 0;  // CTA pairs of the expert GEMMs resident at once
@@ -204,6 +212,15 @@ void release(colibri_moe_t* h) {
         cudaEventDestroy(r.b);
     }
     for (auto e : h->ev_pool) cudaEventDestroy(e);
+    if (h->cs_in) cudaStreamSynchronize(h->cs_in);
+    if (h->cs_out) cudaStreamSynchronize(h->cs_out);
+    for (int i = 0; i < 2; ++i) {
+        if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+        if (h->ev_done[i]) cudaEventDestroy(h->ev_done[i]);
+        if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);
+    }
+    if (h->cs_in) cudaStreamDestroy(h->cs_in);
+    if (h->cs_out) cudaStreamDestroy(h->cs_out);
     cudaFree(h->wr);
     cudaFree(h->bias);
     cudaFree(h->wgu);
@@ -706,7 +723,7 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
                  o_xp = h->grouped_ok ? carve(P * d * h->esz) : 0, o_h = carve(P * f * h->esz),
                  o_y = carve(y_floats * 4), o_guc = carve(gu_counter_bytes),
                  o_u = carve((size_t)M * d * h->esz),
-                 o_xs = carve((size_t)M * d * h->esz), o_ys = carve((size_t)M * d * h->esz);
+                 o_xs = carve((size_t)2 * M * d * h->esz), o_ys = carve((size_t)2 * M * d * h->esz);
     h->ws_bytes = off;
     if ((st = from_cuda(ac.alloc(&h->ws, off))) != COLIBRI_OK) return fail(st);
     uint8_t* b = (uint8_t*)h->ws;
@@ -732,7 +749,17 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
     h->u = b + o_u;
     h->x_stage = b + o_xs;
     h->y_stage = b + o_ys;
+    h->stage_bytes = (size_t)M * d * h->esz;
     if ((st = from_cuda(cudaMemset(h->ws, 0, off))) != COLIBRI_OK) return fail(st);
+    // host-buffer forwards: copy streams and slot events (no timing)
+    if ((st = from_cuda(cudaStreamCreateWithFlags(&h->cs_in, cudaStreamNonBlocking))) != COLIBRI_OK ||
+        (st = from_cuda(cudaStreamCreateWithFlags(&h->cs_out, cudaStreamNonBlocking))) != COLIBRI_OK)
+        return fail(st);
+    for (int i = 0; i < 2; ++i)
+        if ((st = from_cuda(cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming))) != COLIBRI_OK ||
+            (st = from_cuda(cudaEventCreateWithFlags(&h->ev_done[i], cudaEventDisableTiming))) != COLIBRI_OK ||
+            (st = from_cuda(cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming))) != COLIBRI_OK)
+            return fail(st);
 
     if (h->grouped_ok) {
         // int8 handles: single-CTA tiles only, B maps over the int8 codes
@@ -800,21 +827,49 @@ colibri_status_t colibri_forward(colibri_moe_t* h, const void* x, int32_t T, voi
     return st;
 }
 
-colibri_status_t colibri_forward_host(colibri_moe_t* h, const void* x_host, int32_t T,
-                                      void* y_host, void* stream) {
+colibri_status_t colibri_forward_host_async(colibri_moe_t* h, const void* x_host, int32_t T,
+                                            void* y_host, void* stream) {
     if (!h || !x_host || !y_host || T < 0 || T > h->cfg.max_tokens) return COLIBRI_ERR_INVALID_ARG;
     if (T == 0) return COLIBRI_OK;
     DeviceGuard g(h->cfg.device);
     if (!g.ok) return COLIBRI_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
+    const int slot = h->host_slot;
+    h->host_slot ^= 1;
+    uint8_t* xs = static_cast<uint8_t*>(h->x_stage) + slot * h->stage_bytes;
+    uint8_t* ys = static_cast<uint8_t*>(h->y_stage) + slot * h->stage_bytes;
     const size_t bytes = (size_t)T * h->cfg.d_model * h->esz;
-    cudaError_t e = cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s);
+    // upload: the slot's x is free once the layer that read it two calls ago is done
+    cudaError_t e = cudaStreamWaitEvent(h->cs_in, h->ev_done[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, h->cs_in);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_in[slot], h->cs_in);
+    // the layer: x landed, and the slot's y downloaded by its previous call
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_in[slot], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_out[slot], 0);
     if (e != cudaSuccess) return from_cuda(e);
-    colibri_status_t st = run_layer(h, h->x_stage, T, h->y_stage, nullptr, s);
+    const colibri_status_t st = run_layer(h, xs, T, ys, nullptr, s);
     if (st != COLIBRI_OK) return st;
-    e = cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return from_cuda(e);
-    return from_cuda(cudaStreamSynchronize(s));
+    // download, after the layer
+    e = cudaEventRecord(h->ev_done[slot], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->cs_out, h->ev_done[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, h->cs_out);
+    if (e == cudaSuccess) e = cudaEventRecord(h->ev_out[slot], h->cs_out);
+    return from_cuda(e);
+}
+
+colibri_status_t colibri_host_wait(colibri_moe_t* h) {
+    if (!h) return COLIBRI_ERR_INVALID_ARG;
+    DeviceGuard g(h->cfg.device);
+    if (!g.ok) return COLIBRI_ERR_CUDA;
+    // every download is on cs_out and each follows its call's layer
+    return from_cuda(cudaStreamSynchronize(h->cs_out));
+}
+
+colibri_status_t colibri_forward_host(colibri_moe_t* h, const void* x_host, int32_t T,
+                                      void* y_host, void* stream) {
+    const colibri_status_t st = colibri_forward_host_async(h, x_host, T, y_host, stream);
+    if (st != COLIBRI_OK) return st;
+    return colibri_host_wait(h);
 }
 
 colibri_status_t colibri_rmsnorm_moe_residual(colibri_moe_t* h, void* hidden, int32_t T,

@@ -32,6 +32,7 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ("colibri_init", "colibri_forward", "colibri_forward_host", "colibri_free",
+              "colibri_forward_host_async", "colibri_host_wait",
               "colibri_get_routing", "colibri_rmsnorm_moe_residual", "colibri_status_str",
               "colibri_check", "colibri_init_int8", "colibri_quantize_int8_block64"):
         assert n in names
@@ -86,6 +87,8 @@ def test_init_rejects_null_pointers(sef):
 def test_calls_on_null_handle_are_invalid(sef):
     assert sef.colibri_forward(None, None, 1, None, None) == 1
     assert sef.colibri_forward_host(None, None, 1, None, None) == 1
+    assert sef.colibri_forward_host_async(None, None, 1, None, None) == 1
+    assert sef.colibri_host_wait(None) == 1
     assert sef.colibri_get_routing(None, None, None, None, None, None) == 1
     assert sef.colibri_set_executor(None, 0) == 1
     assert sef.colibri_check(None, None) == 1

@@ -75,6 +75,23 @@ def test_tiny_forward_host_matches_device_forward(tiny):
     assert torch.equal(yh, y_dev.cpu())
 
 
+def test_tiny_forward_host_async_pipelines_batches(tiny):
+    """Five pipelined calls (the two staging slots reused, batch sizes
+    changing) on separate pinned buffers: after host_wait every y equals the
+    device forward of its own x."""
+    x16, _ = tiny.tokens(16)
+    xs = [x16[:T] * s for T, s in ((16, 1.0), (5, -0.5), (16, 2.0), (9, 0.25), (1, 3.0))]
+    refs = [tiny.run(x.contiguous(), "auto")[0].cpu() for x in xs]
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.full_like(x, float("nan")).pin_memory() for x in xh]
+    for a, b in zip(xh, yh):
+        tiny.layer.forward_host_async(a, b)
+    tiny.layer.host_wait()
+    for b, ref in zip(yh, refs):
+        assert torch.equal(b, ref)
+    assert tiny.layer.check() == 0
+
+
 # ------------------------------------------------------------------ Mixtral-shaped
 
 
