@@ -320,6 +320,68 @@ colibri_status_t colibri_route_static(const void* x, const void* w_router,
                                       int32_t* topk_idx, float* topk_w, int32_t* counts,
                                       int32_t* perm, void* stream);
 
+/*
+ * Expert parallelism: the experts of a layer split across the GPUs of one
+ * machine, the token rows exchanged with an all-to-all (cf-1.com section 4.1:
+ * GPU-to-GPU bandwidth for the communication between experts on several
+ * cards; section 4.3: several GPUs of one machine).  The exchange itself is
+ * the caller's (a collective library); these calls are the steps on each
+ * side of it.  The source side
+ * routes its tokens (colibri_route_static), gathers the rows into expert
+ * order (colibri_gather_rows), so that the rows bound for each owner are one
+ * contiguous range, and after the exchange back combines the returned rows
+ * (colibri_combine_rows).  An owner runs its experts on the rows it received
+ * (colibri_forward_routed on a handle holding only its experts).
+ */
+
+/*
+ * colibri_forward_routed - colibri_forward with the caller's routing instead
+ * of the router: y[t] = sum_j topk_w[t, j] * FFN_{topk_idx[t, j]}(x[t]), j in
+ * order, float32, then rounded once to dtype.  Dispatch, expert GEMMs and
+ * combine are those of colibri_forward.
+ *   x, y      [T, d_model] device, dtype, 16-byte aligned, not overlapping
+ *   topk_idx  [T, k] device int32, expert ids of this handle (0 .. n_experts-1)
+ *   topk_w    [T, k] device float32
+ * T * k may not exceed max_tokens * top_k of the handle's configuration
+ * (COLIBRI_ERR_INVALID_ARG).  An id out of range is reported by colibri_check
+ * (COLIBRI_ERR_CUDA) after the stream reaches it.  Allocates nothing.
+ */
+colibri_status_t colibri_forward_routed(colibri_moe_t* h, const void* x, int32_t T, int32_t k,
+                                        const int32_t* topk_idx, const float* topk_w, void* y,
+                                        void* stream);
+
+/*
+ * colibri_gather_rows - xp[p] = x[perm[p] / k] for p < npairs: the token rows
+ * in the expert order of a dispatch permutation (perm as colibri_route_static
+ * and colibri_get_routing give it).
+ *   x [x_rows, d_model], xp [npairs, d_model] device, dtype, 16-byte aligned
+ *   perm [npairs] device int32; a value outside 0 .. x_rows*k-1 gathers a
+ *   zero row (every access stays in bounds)
+ * d_model * element size a multiple of 16 bytes.  Runs on the current
+ * device, ordered on `stream`; allocates nothing.
+ */
+colibri_status_t colibri_gather_rows(const void* x, int32_t x_rows, const int32_t* perm, int32_t k,
+                                     int32_t npairs, int32_t d_model, int32_t dtype, void* xp,
+                                     void* stream);
+
+/*
+ * colibri_combine_rows - y[t] = sum_j topk_w[t, j] * rows[p(t, j)], j in
+ * order, float32, rounded once to dtype, where p(t, j) is the position of
+ * pair t*k + j in perm (rows in expert order, one per pair).
+ *   rows        [T * k, d_model] device: float32 (rows_dtype FP32), or bf16
+ *               (rows_dtype BF16, with dtype BF16); 16-byte aligned
+ *   topk_w      [T, k] device float32
+ *   perm        [T * k] device int32, a permutation of 0 .. T*k-1 (a pair
+ *               whose position no value names adds nothing; values out of
+ *               range are skipped, so every access stays in bounds)
+ *   inv_scratch [T * k] device int32, overwritten (the inverse of perm)
+ *   y           [T, d_model] device, dtype, 16-byte aligned
+ * d_model % 8 == 0.  Runs on the current device, ordered on `stream`.
+ */
+colibri_status_t colibri_combine_rows(const void* rows, int32_t rows_dtype, const float* topk_w,
+                                      const int32_t* perm, int32_t T, int32_t k, int32_t d_model,
+                                      int32_t dtype, int32_t* inv_scratch, void* y, void* stream);
+
 /* colibri_free - release everything the handle holds; NULL is allowed.
  * Synchronises the handle's device first. */
 void colibri_free(colibri_moe_t* h);

@@ -72,6 +72,9 @@ def _load():
         "colibri_profile_enable": ([P, ctypes.c_int], I32),
         "colibri_profile_read": ([P, ctypes.POINTER(ctypes.c_double), U64P], I32),
         "colibri_route_static": ([P, P, P, I32, I32, I32, I32, I32, P, P, P, P, P], I32),
+        "colibri_forward_routed": ([P, P, I32, I32, P, P, P, P], I32),
+        "colibri_gather_rows": ([P, I32, P, I32, I32, I32, I32, P, P], I32),
+        "colibri_combine_rows": ([P, I32, P, P, I32, I32, I32, I32, P, P, P], I32),
         "colibri_free": ([P], None),
         "colibri_status_str": ([I32], ctypes.c_char_p),
     }
@@ -89,6 +92,7 @@ _C_NAMES = ("colibri_init", "colibri_init_int8", "colibri_quantize_int8_block64"
             "colibri_set_capacity",
             "colibri_check", "colibri_launch_count", "colibri_workspace_bytes",
             "colibri_profile_enable", "colibri_profile_read", "colibri_route_static",
+            "colibri_forward_routed", "colibri_gather_rows", "colibri_combine_rows",
             "colibri_free")
 
 
@@ -235,6 +239,25 @@ class MoELayer:
         return out
 
     __call__ = forward
+
+    def forward_routed(self, x, topk_idx, topk_w, out=None, stream=None):
+        """y[t] = sum_j topk_w[t, j] * FFN_{topk_idx[t, j]}(x[t]) with the caller's
+        routing (int32 ids of this handle's experts, float32 gates; [T] or [T, k])."""
+        import torch
+        if x.dtype != self.dtype or x.device != self.device or x.dim() != 2 or x.shape[1] != self.d:
+            raise ValueError("x must be [T, d_model] with the layer's dtype on its device")
+        T = x.shape[0]
+        idx = topk_idx.reshape(T, -1).to(torch.int32).contiguous()
+        w = topk_w.reshape(T, -1).to(torch.float32).contiguous()
+        if idx.shape != w.shape:
+            raise ValueError("topk_idx and topk_w must have the same shape")
+        x = x.contiguous()
+        if out is None:
+            out = torch.empty_like(x)
+        _check(library().colibri_forward_routed(self._h, _ptr(x), T, idx.shape[1], _ptr(idx), _ptr(w),
+                                                _ptr(out), _stream_ptr(stream)),
+               "colibri_forward_routed")
+        return out
 
     def forward_host(self, x_host, y_host, stream=None):
         """The layer on host tensors (copies in, runs, copies out, waits)."""

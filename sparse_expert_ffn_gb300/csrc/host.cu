@@ -316,10 +316,13 @@ struct Stage {
 // The layer on device buffers; `resid` (may equal y) adds a residual.  With
 // `gamma` the layer input is u = RMSNorm(x) * gamma (written to h->u): fused
 // into the small-batch routing kernel when that runs, else its own launch.
+// With `r_idx` the routing is the caller's (r_k experts per row, gates r_w):
+// no router runs, the rest of the layer is the same.
 colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, const void* resid,
-                           cudaStream_t s, const void* gamma = nullptr, float eps = 0.f) {
+                           cudaStream_t s, const void* gamma = nullptr, float eps = 0.f,
+                           const int32_t* r_idx = nullptr, const float* r_w = nullptr, int r_k = 0) {
     const auto& c = h->cfg;
-    const int E = c.n_experts, k = c.top_k, d = c.d_model, f = c.d_ff;
+    const int E = c.n_experts, k = r_idx ? r_k : c.top_k, d = c.d_model, f = c.d_ff;
     const int npairs = T * k;
     colibri_status_t st;
     const int ex = choose_executor(h, T);
@@ -331,8 +334,8 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     const int tile_rows = dec ? tc_gemm_dec_tile_rows() : pair ? tc_gemm_pair_rows() : tc_gemm_block_m();
     // Small batch: router, top-k, softmax, dispatch and gather in one CTA.
     // soft routing (k == E) runs on the CUDA-core router kernel
-    const bool soft = k == E;
-    const bool fused_routing = !soft && route_small_fits(T, d, E, k);
+    const bool soft = !r_idx && k == E;
+    const bool fused_routing = !r_idx && !soft && route_small_fits(T, d, E, k);
     const int cap = h->capacity < 0 ? INT_MAX : h->capacity;
     if (gamma && !fused_routing) {
         Stage g(h, COLIBRI_STAGE_RMSNORM, s);
@@ -340,7 +343,15 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         if (st != COLIBRI_OK) return st;
         x = h->u;
     }
-    if (fused_routing) {
+    if (r_idx) {
+        // the caller's routing, into the workspace the dispatch and combine read
+        Stage g(h, COLIBRI_STAGE_ROUTER, s);
+        cudaError_t e = cudaMemcpyAsync(h->topk_idx, r_idx, (size_t)npairs * 4, cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(h->topk_w, r_w, (size_t)npairs * 4, cudaMemcpyDeviceToDevice, s);
+        st = g.done(e, 0);
+        if (st != COLIBRI_OK) return st;
+    } else if (fused_routing) {
         Stage g(h, COLIBRI_STAGE_ROUTER, s);
         st = g.done(launch_route_small(h->dt, x, h->wr, h->bias, T, d, E, k, h->topk_idx,
                                        h->topk_w, h->counts, h->offsets, h->perm, h->inv,
@@ -443,7 +454,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             // boxes of 128 consecutive rows read it far faster than per-row
             // gathers inside the GEMM
             Stage g(h, COLIBRI_STAGE_GATHER, s);
-            st = g.done(launch_gather(h->esz, x, h->perm, k, d, npairs, h->xp, s, h->int8), 1);
+            st = g.done(launch_gather(h->esz, x, h->perm, k, d, npairs, npairs, h->xp, s, h->int8), 1);
             if (st != COLIBRI_OK) return st;
         }
         TcGemmArgs a{};
@@ -825,6 +836,58 @@ colibri_status_t colibri_forward(colibri_moe_t* h, const void* x, int32_t T, voi
     const colibri_status_t st = run_layer(h, x, T, y, nullptr, (cudaStream_t)stream);
     if (st != COLIBRI_OK && h->sticky == COLIBRI_OK) h->sticky = st;
     return st;
+}
+
+colibri_status_t colibri_forward_routed(colibri_moe_t* h, const void* x, int32_t T, int32_t k,
+                                        const int32_t* topk_idx, const float* topk_w, void* y,
+                                        void* stream) {
+    if (!h || !x || !y || !topk_idx || !topk_w || T < 0 || k <= 0) return COLIBRI_ERR_INVALID_ARG;
+    if ((int64_t)T * k > (int64_t)h->max_pairs) return COLIBRI_ERR_INVALID_ARG;
+    if (((uintptr_t)x & 15) || ((uintptr_t)y & 15)) return COLIBRI_ERR_INVALID_ARG;
+    const size_t bytes = (size_t)T * h->cfg.d_model * h->esz;
+    if (T > 0 && ranges_overlap(x, bytes, y, bytes)) return COLIBRI_ERR_INVALID_ARG;
+    if (T == 0) return COLIBRI_OK;
+    DeviceGuard g(h->cfg.device);
+    if (!g.ok) return COLIBRI_ERR_CUDA;
+    const colibri_status_t st =
+        run_layer(h, x, T, y, nullptr, (cudaStream_t)stream, nullptr, 0.f, topk_idx, topk_w, k);
+    if (st != COLIBRI_OK && h->sticky == COLIBRI_OK) h->sticky = st;
+    return st;
+}
+
+colibri_status_t colibri_gather_rows(const void* x, int32_t x_rows, const int32_t* perm, int32_t k,
+                                     int32_t npairs, int32_t d_model, int32_t dtype, void* xp,
+                                     void* stream) {
+    if (!x || !perm || !xp || x_rows < 0 || k <= 0 || npairs < 0 || d_model <= 0)
+        return COLIBRI_ERR_INVALID_ARG;
+    if ((int64_t)x_rows * k > INT32_MAX) return COLIBRI_ERR_INVALID_ARG;
+    if (dtype != COLIBRI_DTYPE_FP32 && dtype != COLIBRI_DTYPE_BF16) return COLIBRI_ERR_INVALID_ARG;
+    const int esz = dtype == COLIBRI_DTYPE_BF16 ? 2 : 4;
+    if (((uintptr_t)x & 15) || ((uintptr_t)xp & 15) || (d_model * esz) % 16)
+        return COLIBRI_ERR_INVALID_ARG;
+    if (npairs == 0) return COLIBRI_OK;
+    return from_cuda(
+        launch_gather(esz, x, perm, k, d_model, npairs, x_rows * k, xp, (cudaStream_t)stream));
+}
+
+colibri_status_t colibri_combine_rows(const void* rows, int32_t rows_dtype, const float* topk_w,
+                                      const int32_t* perm, int32_t T, int32_t k, int32_t d_model,
+                                      int32_t dtype, int32_t* inv_scratch, void* y, void* stream) {
+    if (!rows || !topk_w || !perm || !inv_scratch || !y || T < 0 || k <= 0 || d_model <= 0)
+        return COLIBRI_ERR_INVALID_ARG;
+    if (dtype != COLIBRI_DTYPE_FP32 && dtype != COLIBRI_DTYPE_BF16) return COLIBRI_ERR_INVALID_ARG;
+    // float32 rows, or bf16 rows for a bf16 output
+    if (rows_dtype != COLIBRI_DTYPE_FP32 && !(rows_dtype == COLIBRI_DTYPE_BF16 && dtype == COLIBRI_DTYPE_BF16))
+        return COLIBRI_ERR_INVALID_ARG;
+    if (((uintptr_t)rows & 15) || ((uintptr_t)y & 15) || d_model % 8) return COLIBRI_ERR_INVALID_ARG;
+    if (T == 0) return COLIBRI_OK;
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_invert_perm(perm, T * k, inv_scratch, s);
+    if (e == cudaSuccess)
+        e = launch_combine(dtype == COLIBRI_DTYPE_BF16 ? DType::BF16 : DType::F32,
+                           static_cast<const float*>(rows), rows_dtype == COLIBRI_DTYPE_BF16, topk_w,
+                           inv_scratch, T, k, d_model, 1, 0, nullptr, y, s);
+    return from_cuda(e);
 }
 
 colibri_status_t colibri_forward_host_async(colibri_moe_t* h, const void* x_host, int32_t T,

@@ -63,12 +63,16 @@ cudaError_t launch_ffn_down_stream_i8(DType dt, const void* H, const int8_t* wq,
                                       const int32_t* offsets, int d, int f, int E, float* Y,
                                       cudaStream_t s);
 
+// xp[p] = x[perm[p] / k] for p < npairs; a perm value outside [0, src_pairs)
+// gathers a zero row.
 cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,
-                          int npairs, void* xp, cudaStream_t s, bool to_f16 = false);
+                          int npairs, int src_pairs, void* xp, cudaStream_t s, bool to_f16 = false);
 // y_bf16: Y holds the down projection's rows as bf16 (no K slices).
 cudaError_t launch_combine(DType dt, const float* Y, bool y_bf16, const float* topk_w,
                            const int32_t* inv, int T, int k, int d, int nsplit, size_t split_stride,
                            const void* resid, void* y, cudaStream_t s);
+// inv[perm[p]] = p for p < n.
+cudaError_t launch_invert_perm(const int32_t* perm, int n, int32_t* inv, cudaStream_t s);
 cudaError_t launch_rmsnorm(DType dt, const void* h, const void* gamma, int T, int d, float eps,
                            void* u, cudaStream_t s);
 cudaError_t launch_transpose_remap(int elem_bytes, const void* in, void* out, int batch, int R,

@@ -24,18 +24,24 @@ constexpr int kGatherCtasPerSm = 8;
 template <bool kToF16>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k, int row_vecs,
-            int npairs, uint4* __restrict__ xp) {
+            int npairs, int src_pairs, uint4* __restrict__ xp) {
     pdl_enter();
     const int lane = threadIdx.x & 31;
     const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+    // pair q = t*k + j of x's src_pairs; any other value gathers a zero row
+    auto row_of = [&](int q) { return (unsigned)q < (unsigned)src_pairs ? q / k : -1; };
     int p = gw;
-    int t_next = p < npairs ? perm[p] / k : 0;
+    int t_next = p < npairs ? row_of(perm[p]) : 0;
     for (; p < npairs; p += nw) {
         const int t = t_next;
-        if (p + nw < npairs) t_next = perm[p + nw] / k;
-        const uint4* src = x + (size_t)t * row_vecs;
+        if (p + nw < npairs) t_next = row_of(perm[p + nw]);
         uint4* dst = xp + (size_t)p * row_vecs;
+        if (t < 0) {
+            for (int i = lane; i < row_vecs; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+        }
+        const uint4* src = x + (size_t)t * row_vecs;
 #pragma unroll 8
         for (int i = lane; i < row_vecs; i += 32) {
             const uint4 v = __ldg(src + i);
@@ -198,7 +204,7 @@ __global__ void transpose_remap(const E* __restrict__ in, E* __restrict__ out, i
 }  // namespace
 
 cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,
-                          int npairs, void* xp, cudaStream_t s, bool to_f16) {
+                          int npairs, int src_pairs, void* xp, cudaStream_t s, bool to_f16) {
     if (npairs <= 0) return cudaSuccess;
     const int row_vecs = d * elem_bytes / 16;
     static int sms = 0;
@@ -213,9 +219,9 @@ cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, in
                                           sms * kGatherCtasPerSm));
     const cudaError_t e =
         to_f16 ? launch_pdl(gather_rows<true>, grid, kGatherThreads, 0, s, (const uint4*)x, perm, k,
-                            row_vecs, npairs, (uint4*)xp)
+                            row_vecs, npairs, src_pairs, (uint4*)xp)
                : launch_pdl(gather_rows<false>, grid, kGatherThreads, 0, s, (const uint4*)x, perm, k,
-                            row_vecs, npairs, (uint4*)xp);
+                            row_vecs, npairs, src_pairs, (uint4*)xp);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -265,6 +271,25 @@ cudaError_t launch_combine(DType dt, const float* Y, bool y_bf16, const float* t
                   : launch_pdl(combine_kernel<float, false, float>, grid, block, 0, s, Y, topk_w, inv,
                                k, d, nsplit, split_stride, r, o);
     }
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+namespace {
+__global__ void invert_perm_kernel(const int32_t* __restrict__ perm, int n, int32_t* __restrict__ inv) {
+    pdl_enter();
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p < n) {
+        const int q = perm[p];
+        if (q >= 0 && q < n) inv[q] = p;            // a value out of range is skipped
+    }
+}
+}  // namespace
+
+cudaError_t launch_invert_perm(const int32_t* perm, int n, int32_t* inv, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    // -1 first: a position that no perm value names reads as a dropped pair
+    cudaError_t e = cudaMemsetAsync(inv, 0xff, (size_t)n * sizeof(int32_t), s);
+    if (e == cudaSuccess) e = launch_pdl(invert_perm_kernel, (n + 255) / 256, 256, 0, s, perm, n, inv);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
