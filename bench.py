@@ -536,7 +536,7 @@ def run_stack(args):
 
     def step():
         for layer in layers:
-            layer.rmsnorm_moe_residual(h, gamma, synth.STACK_EPS)
+            layer.forward_stack_layer(h, gamma, synth.STACK_EPS)
 
     for _ in range(args.warmup):
         h.copy_(h0)

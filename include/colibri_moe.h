@@ -191,7 +191,7 @@ colibri_status_t colibri_forward_host_async(colibri_moe_t* h, const void* x_host
 colibri_status_t colibri_host_wait(colibri_moe_t* h);
 
 /*
- * colibri_rmsnorm_moe_residual - one layer of a pre-norm decode stack
+ * colibri_forward_stack_layer - one layer of a pre-norm decode stack
  * (pnsm.cn section 2.2: residual around the MoE block):
  *   u = bf16(RMSNorm(hidden) * gamma),  hidden <- bf16(hidden + MoE(u))
  * RMSNorm(h) = h / sqrt(mean(h^2) + eps), in float32; the residual sum is
@@ -200,8 +200,8 @@ colibri_status_t colibri_host_wait(colibri_moe_t* h);
  *   gamma  [d_model] device, dtype
  * Requires dtype BF16 or FP32 matching the handle; allocates nothing.
  */
-colibri_status_t colibri_rmsnorm_moe_residual(colibri_moe_t* h, void* hidden, int32_t T,
-                                              const void* gamma, float eps, void* stream);
+colibri_status_t colibri_forward_stack_layer(colibri_moe_t* h, void* hidden, int32_t T,
+                                             const void* gamma, float eps, void* stream);
 
 /*
  * colibri_get_routing - copy the last forward's routing decisions out

@@ -62,7 +62,7 @@ def _load():
         "colibri_forward_host": ([P, P, I32, P, P], I32),
         "colibri_forward_host_async": ([P, P, I32, P, P], I32),
         "colibri_host_wait": ([P], I32),
-        "colibri_rmsnorm_moe_residual": ([P, P, I32, P, ctypes.c_float, P], I32),
+        "colibri_forward_stack_layer": ([P, P, I32, P, ctypes.c_float, P], I32),
         "colibri_get_routing": ([P, P, P, P, P, P], I32),
         "colibri_set_executor": ([P, I32], I32),
         "colibri_set_capacity": ([P, I32], I32),
@@ -88,7 +88,7 @@ def _load():
 _lib = None
 _C_NAMES = ("colibri_init", "colibri_init_int8", "colibri_quantize_int8_block64", "colibri_forward",
             "colibri_forward_host", "colibri_forward_host_async", "colibri_host_wait",
-            "colibri_rmsnorm_moe_residual", "colibri_get_routing", "colibri_set_executor",
+            "colibri_forward_stack_layer", "colibri_get_routing", "colibri_set_executor",
             "colibri_set_capacity",
             "colibri_check", "colibri_launch_count", "colibri_workspace_bytes",
             "colibri_profile_enable", "colibri_profile_read", "colibri_route_static",
@@ -280,13 +280,13 @@ class MoELayer:
         """Wait for every forward_host_async call on this layer."""
         _check(library().colibri_host_wait(self._h), "colibri_host_wait")
 
-    def rmsnorm_moe_residual(self, hidden, gamma, eps: float, stream=None):
+    def forward_stack_layer(self, hidden, gamma, eps: float, stream=None):
         """hidden <- hidden + MoE(RMSNorm(hidden) * gamma), in place."""
         if hidden.dtype != self.dtype or not hidden.is_contiguous():
             raise ValueError("hidden must be contiguous with the layer's dtype")
-        _check(library().colibri_rmsnorm_moe_residual(self._h, _ptr(hidden), hidden.shape[0], _ptr(gamma),
-                                            float(eps), _stream_ptr(stream)),
-               "colibri_rmsnorm_moe_residual")
+        _check(library().colibri_forward_stack_layer(self._h, _ptr(hidden), hidden.shape[0], _ptr(gamma),
+                                                     float(eps), _stream_ptr(stream)),
+               "colibri_forward_stack_layer")
         self.last_T = hidden.shape[0]
         return hidden
 

@@ -935,8 +935,8 @@ colibri_status_t colibri_forward_host(colibri_moe_t* h, const void* x_host, int3
     return colibri_host_wait(h);
 }
 
-colibri_status_t colibri_rmsnorm_moe_residual(colibri_moe_t* h, void* hidden, int32_t T,
-                                              const void* gamma, float eps, void* stream) {
+colibri_status_t colibri_forward_stack_layer(colibri_moe_t* h, void* hidden, int32_t T,
+                                             const void* gamma, float eps, void* stream) {
     if (!h || !hidden || !gamma || T < 0 || T > h->cfg.max_tokens || !(eps >= 0.0f))
         return COLIBRI_ERR_INVALID_ARG;
     if ((uintptr_t)hidden & 15) return COLIBRI_ERR_INVALID_ARG;

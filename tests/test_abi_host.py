@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ("colibri_init", "colibri_forward", "colibri_forward_host", "colibri_free",
               "colibri_forward_host_async", "colibri_host_wait",
-              "colibri_get_routing", "colibri_rmsnorm_moe_residual", "colibri_status_str",
+              "colibri_get_routing", "colibri_forward_stack_layer", "colibri_status_str",
               "colibri_check", "colibri_init_int8", "colibri_quantize_int8_block64"):
         assert n in names
 

@@ -84,7 +84,7 @@ def test_residual_layer_with_capacity_zero_is_identity(lib):
         h0 = h.clone()
         gamma = torch.ones(shape.d_model, dtype=torch.bfloat16, device=c.dev)
         c.layer.set_capacity(0)
-        c.layer.rmsnorm_moe_residual(h, gamma, 1e-5)
+        c.layer.forward_stack_layer(h, gamma, 1e-5)
         torch.cuda.synchronize()
         assert c.layer.check() == 0
         assert torch.equal(h, h0)

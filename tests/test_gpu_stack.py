@@ -49,7 +49,7 @@ def test_stack_teacher_forced_layers(stack):
         h = synth.tokens(shape, B, seed=7, device="cuda")           # bf16 N(0,1) hidden state
         for l, layer in enumerate(layers):
             h_in = h.clone()
-            layer.rmsnorm_moe_residual(h, gamma, synth.STACK_EPS)
+            layer.forward_stack_layer(h, gamma, synth.STACK_EPS)
             if l in CHECK_LAYERS:
                 torch.cuda.synchronize()
                 assert layer.check() == 0
