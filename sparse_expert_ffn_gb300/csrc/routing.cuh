@@ -174,12 +174,15 @@ __device__ __forceinline__ void dispatch_block(
     int32_t* ecount = wcnt + kDispatchWarps * E;  // [E]
     int32_t* eoff = ecount + E;                   // [E + 1]
     int32_t* tbase = eoff + E + 1;                // [E + 1]
-    const int warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) wcnt[i] = 0;
+    // Warp w walks pairs [w*chunk, (w+1)*chunk); only the first `nw` warps
+    // hold any (a small batch fills one warp), so only their counts are kept.
+    const int chunk = ((n + kDispatchWarps - 1) / kDispatchWarps + 31) & ~31;
+    const int nw = chunk > 0 ? min(kDispatchWarps, (n + chunk - 1) / chunk) : 0;
+    for (int i = threadIdx.x; i < nw * E; i += blockDim.x) wcnt[i] = 0;
     __syncthreads();
 
-    const int chunk = ((n + kDispatchWarps - 1) / kDispatchWarps + 31) & ~31;
     const int lo = warp * chunk;
     const int hi = min(n, lo + chunk);
     int32_t* my = wcnt + warp * E;
@@ -189,27 +192,51 @@ __device__ __forceinline__ void dispatch_block(
     if (threadIdx.x < E) {
         const int e = threadIdx.x;
         int32_t c = 0;
-        for (int w = 0; w < kDispatchWarps; ++w) c += wcnt[w * E + e];
+        for (int w = 0; w < nw; ++w) c += wcnt[w * E + e];
         ecount[e] = c;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int32_t acc = 0, tacc = 0;
-        for (int e = 0; e < E; ++e) {
-            eoff[e] = acc;
-            tbase[e] = tacc;
-            acc += ecount[e];
-            tacc += (min(ecount[e], cap) + bm - 1) / bm;
+    if (warp == 0) {
+        // exclusive scans of the counts and of the tile counts: lane l sums
+        // experts [l*per, (l+1)*per), a warp scan gives each lane its base
+        const int per = (E + 31) / 32;
+        const int e0 = lane * per;
+        int32_t c_sum = 0, t_sum = 0;
+        for (int i = 0; i < per; ++i) {
+            const int e = e0 + i;
+            if (e < E) {
+                c_sum += ecount[e];
+                t_sum += (min(ecount[e], cap) + bm - 1) / bm;
+            }
         }
-        eoff[E] = acc;
-        tbase[E] = tacc;
-        *num_tiles = tacc;
+        int32_t c_inc = c_sum, t_inc = t_sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t a = __shfl_up_sync(0xffffffffu, c_inc, o);
+            const int32_t b = __shfl_up_sync(0xffffffffu, t_inc, o);
+            if (lane >= o) c_inc += a, t_inc += b;
+        }
+        int32_t acc = c_inc - c_sum, tacc = t_inc - t_sum;
+        for (int i = 0; i < per; ++i) {
+            const int e = e0 + i;
+            if (e < E) {
+                eoff[e] = acc;
+                tbase[e] = tacc;
+                acc += ecount[e];
+                tacc += (min(ecount[e], cap) + bm - 1) / bm;
+            }
+        }
+        if (lane == 31) {
+            eoff[E] = c_inc;
+            tbase[E] = t_inc;
+            *num_tiles = t_inc;
+        }
     }
     __syncthreads();
     if (threadIdx.x < E) {
         const int e = threadIdx.x;
         int32_t run = eoff[e];
-        for (int w = 0; w < kDispatchWarps; ++w) {
+        for (int w = 0; w < nw; ++w) {
             const int32_t c = wcnt[w * E + e];
             wcnt[w * E + e] = run;
             run += c;
