@@ -1,12 +1,13 @@
 """Expert parallelism's host logic (sparse_expert_ffn_gb300/ep.py) on CPU.
 
-The exchange plan is checked as plain functions; then two gloo ranks, each
-owning half of 8 experts and routing tokens of its own, run the whole
-expert-parallel forward with the oracle standing in for the library's
-kernels (route, gather, experts, combine), and each rank's output must equal
-the oracle's layer over all experts for its tokens.  The collective calls are
-the ones the GPU path makes (all_to_all_single of the count table and of the
-row blocks, there over NCCL)."""
+The exchange plan is checked as plain functions. Then two or three gloo
+ranks run the whole expert-parallel forward. Each rank owns an equal share
+of the experts and routes tokens of its own (some ranks have none). The
+oracle stands in for the library's kernels (route, gather, experts,
+combine). Each rank's output must equal the oracle's layer over all experts
+for its tokens. The collective calls are the ones the GPU path makes:
+all_to_all_single of the count table and of the row blocks (over NCCL
+there)."""
 
 import os
 import socket
@@ -51,13 +52,13 @@ def _layer(seed, E=8, d=32, f=48):
     return wr, wg, wu, wd
 
 
-def _rank_main(rank, world, port, T, k, out):
+def _rank_main(rank, world, port, T, k, E, out):
     import torch.distributed as dist
     import oracle
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        wr, wg, wu, wd = _layer(5)
+        wr, wg, wu, wd = _layer(5, E=E)
         E = wr.shape[1]
         El = E // world
         x = np.random.default_rng(100 + rank).standard_normal((T[rank], wr.shape[0]))
@@ -103,12 +104,13 @@ def _rank_main(rank, world, port, T, k, out):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("T", [(7, 11), (5, 0)])
-def test_two_gloo_ranks_match_the_whole_layer(T):
-    world, port, k = 2, _free_port(), 2
+@pytest.mark.parametrize("T,k,E", [((7, 11), 2, 8), ((5, 0), 2, 8), ((9, 0, 4), 3, 6),
+                                   ((1, 6, 13), 1, 6)])
+def test_gloo_ranks_match_the_whole_layer(T, k, E):
+    world, port = len(T), _free_port()
     with mp.Manager() as m:
         out = m.dict()
-        mp.spawn(_rank_main, args=(world, port, T, k, out), nprocs=world, join=True)
+        mp.spawn(_rank_main, args=(world, port, T, k, E, out), nprocs=world, join=True)
         res = dict(out)
     for rank in range(world):
         err, scale = res[rank]
