@@ -95,3 +95,43 @@ def test_calls_on_null_handle_are_invalid(sef):
     n = ctypes.c_uint64()
     assert sef.colibri_launch_count(None, ctypes.byref(n)) == 1
     sef.colibri_free(None)   # NULL-safe
+
+
+def _aligned(buf, offset=0):
+    """An address inside `buf` on a 16-byte boundary, plus `offset` bytes."""
+    a = ctypes.addressof(buf)
+    return ctypes.c_void_p(((a + 15) & ~15) + offset)
+
+
+def test_handle_free_calls_check_arguments_before_cuda(sef):
+    buf = (ctypes.c_uint8 * 4096)()
+    p, odd = _aligned(buf), _aligned(buf, 8)
+    F32, BF16 = sef.DTYPE_FP32, sef.DTYPE_BF16
+    # gather_rows(x, x_rows, perm, k, npairs, d_model, dtype, xp, stream)
+    g = sef.colibri_gather_rows
+    assert g(None, 4, p, 2, 8, 64, F32, p, None) == 1
+    assert g(p, -1, p, 2, 8, 64, F32, p, None) == 1
+    assert g(p, 4, p, 0, 8, 64, F32, p, None) == 1
+    assert g(p, 4, p, 2, -1, 64, F32, p, None) == 1
+    assert g(p, 4, p, 2, 8, 64, 7, p, None) == 1
+    assert g(odd, 4, p, 2, 8, 64, F32, p, None) == 1
+    assert g(p, 4, p, 2, 8, 2, F32, p, None) == 1          # 8-byte rows
+    assert g(p, 1 << 30, p, 4, 8, 64, F32, p, None) == 1   # x_rows * k overflows
+    assert g(p, 4, p, 2, 0, 64, BF16, p, None) == 0        # nothing to gather
+    # combine_rows(rows, rows_dtype, topk_w, perm, T, k, d_model, dtype, inv, y, stream)
+    c = sef.colibri_combine_rows
+    assert c(None, F32, p, p, 4, 2, 64, F32, p, p, None) == 1
+    assert c(p, F32, p, p, 4, 2, 64, F32, None, p, None) == 1
+    assert c(p, F32, p, p, -1, 2, 64, F32, p, p, None) == 1
+    assert c(p, BF16, p, p, 4, 2, 64, F32, p, p, None) == 1  # bf16 rows need bf16 y
+    assert c(p, F32, p, p, 4, 2, 60, F32, p, p, None) == 1   # d_model % 8
+    assert c(p, F32, p, p, 4, 2, 64, F32, p, odd, None) == 1
+    assert c(p, BF16, p, p, 0, 2, 64, BF16, p, p, None) == 0  # no tokens
+    # forward_routed needs a handle
+    assert sef.colibri_forward_routed(None, p, 4, 2, p, p, p, None) == 1
+    # route_static: the configuration limits
+    r = sef.colibri_route_static
+    assert r(p, p, None, 4, 64, 8, 9, F32, p, p, p, p, None) == 1   # k > E
+    assert r(p, p, None, 4, 64, 300, 2, F32, p, p, p, p, None) == 4
+    assert r(p, p, None, 4, 96, 8, 2, F32, p, p, p, p, None) == 4   # d % 64
+    assert r(p, p, None, 0, 64, 8, 2, F32, p, p, p, p, None) == 0   # T = 0
