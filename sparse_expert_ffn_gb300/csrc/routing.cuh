@@ -131,6 +131,8 @@ __device__ __forceinline__ void warp_scatter_pass(const int32_t* __restrict__ to
                 perm[p] = r;
                 inv[r] = p - seg_start[e] < cap ? p : -1;
                 if (lane == __ffs(m) - 1) my[e] = start + __popc(m);
+            } else if (r < hi) {
+                inv[r] = -1;     // an expert id out of range (reported by pass 1): adds nothing
             }
             __syncwarp();
         }
