@@ -326,12 +326,12 @@ colibri_status_t colibri_route_static(const void* x, const void* w_router,
  * GPU-to-GPU bandwidth for the communication between experts on several
  * cards; section 4.3: several GPUs of one machine).  The exchange itself is
  * the caller's (a collective library); these calls are the steps on each
- * side of it.  The source side
- * routes its tokens (colibri_route_static), gathers the rows into expert
- * order (colibri_gather_rows), so that the rows bound for each owner are one
- * contiguous range, and after the exchange back combines the returned rows
- * (colibri_combine_rows).  An owner runs its experts on the rows it received
- * (colibri_forward_routed on a handle holding only its experts).
+ * side of it.  The source side routes its tokens (colibri_route_static) and
+ * gathers the rows into expert order (colibri_gather_rows), so that the rows
+ * bound for each owner are one contiguous range; after the exchange back it
+ * combines the returned rows (colibri_combine_rows).  An owner runs its
+ * experts on the rows it received (colibri_forward_routed on a handle
+ * holding only its experts).
  */
 
 /*
