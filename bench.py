@@ -67,6 +67,9 @@ def parse_args(argv=None):
                     help="expert weight format: bf16, or int8 64x64 blocks (converted on the host, "
                          "dequantised to f16 by converter warps of the tensor-core GEMMs)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the decode-size sweep")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the block of the other workloads (Qwen2- and DeepSeek-shaped "
+                         "layers, int8 weights, the decode stack) in the default run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -134,6 +137,21 @@ KERNEL_SOURCES = {
     "ffn_up_stream": ("sparse_expert_ffn_gb300/csrc/ffn_stream.cu", "sparse_expert_ffn_gb300/csrc/common.cuh"),
     "ffn_down_stream": ("sparse_expert_ffn_gb300/csrc/ffn_stream.cu", "sparse_expert_ffn_gb300/csrc/common.cuh"),
 }
+
+
+def traffic_key(workload, T, shape, weights="bf16"):
+    """The name a committed ncu summary gives a kernel's workload: the
+    workload and token count, plus the experts per token when they differ
+    from the shape's own and the weight format when it is not bf16, so that
+    one configuration's bytes are never reported for another's."""
+    import synth
+    base = getattr(synth, WORKLOADS[workload][0]) if workload in WORKLOADS else shape
+    key = f"{workload}_T{T}"
+    if shape.top_k != base.top_k:
+        key += f"_k{shape.top_k}"
+    if weights != "bf16":
+        key += f"_{weights}"
+    return key
 
 
 def measured_traffic(kernel, workload):
@@ -320,6 +338,252 @@ def time_steps_flushed(layer, x, y, steps, warmup, stream, scratch):
     return sum(a.elapsed_time(b) for a, b in ev)
 
 
+def kernel_name(stage, shape, T, weights):
+    """The library kernel behind a profiled stage of a layer call."""
+    grouped = shape.dtype == "bf16" and shape.d_model % 256 == 0
+    i8 = "_i8" if weights == "int8" else ""
+    # decode-sized batches (at most 16 pairs per expert on average) run the
+    # GEMMs with the weights as the MMA's M operand
+    gk = "grouped_gemm_dec" if T * shape.top_k <= 16 * shape.n_experts else "grouped_gemm_tc"
+    return {("expert_up", True): gk + "<kGateUp>", ("expert_down", True): gk + "<kDown>",
+            ("expert_up", False): "ffn_up_stream" + i8,
+            ("expert_down", False): "ffn_down_stream" + i8}.get((stage, grouped), stage)
+
+
+def dominant_roofline(stages, alg, kname, pk, traffic=None):
+    """Roofline of the stage with the largest share of the profiled region.
+
+    `alg` holds the algorithmic FLOPs and bytes of each GEMM summed over the
+    launches profiled (one layer call, or every layer of a stack step).  The
+    kernel is tensor-bound when its FLOPs take longer at the tensor peak than
+    its bytes at the HBM peak (prefill), HBM-bound otherwise (decode sizes)."""
+    dom = max(stages, key=lambda s: stages[s]["ms_total"])
+    per_launch_s = stages[dom]["ms_total"] / stages[dom]["launches"] / 1e3
+    launches_per_call = stages[dom]["launches"] / alg["calls"]
+    fl = {"expert_up": alg["up_flops"], "expert_down": alg["down_flops"]}.get(dom, 0) / alg["calls"] / launches_per_call
+    by = {"expert_up": alg["up_bytes"], "expert_down": alg["down_bytes"]}.get(dom, alg["bytes"]) / alg["calls"] / launches_per_call
+    tensor = fl / (pk["bf16_tflops"] * 1e12) >= by / (pk["hbm_gbs"] * 1e9) and fl > 0
+    if tensor:
+        achieved = fl / per_launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
+                "peak_kind": f"bf16 dense burst, {pk['source']}"}
+    else:
+        achieved = by / per_launch_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": f"HBM copy, {pk['source']}"}
+    roof["kernel"] = kname(dom)
+    roof["share_of_step"] = round(stages[dom]["ms_total"] / sum(v["ms_total"] for v in stages.values()), 4)
+    roof["traffic"] = traffic(roof["kernel"]) if traffic else None
+    roof["algorithmic_per_launch"] = int(fl if tensor else by)
+    return roof
+
+
+def layer_roofline(alg, step_s, pk):
+    """The whole layer's roofline: max(bytes / HBM, FLOPs / tensor peak) over the step time."""
+    t_hbm = alg["bytes"] / (pk["hbm_gbs"] * 1e9)
+    t_tc = alg["flops"] / (pk["bf16_tflops"] * 1e12)
+    return {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+            "roofline_time_us": round(1e6 * max(t_hbm, t_tc), 1),
+            "step_us": round(step_s * 1e6, 1),
+            "frac": round(max(t_hbm, t_tc) / step_s, 4)}
+
+
+def profile_stages(lib, handles):
+    """Per-stage totals of the library's event profiling, summed over handles."""
+    import ctypes
+    stages = {}
+    for hdl in handles:
+        tot = (ctypes.c_double * 7)()
+        cnt = (ctypes.c_uint64 * 7)()
+        lib.colibri_profile_read(hdl, tot, cnt)
+        lib.colibri_profile_enable(hdl, 0)
+        for i in range(7):
+            if cnt[i]:
+                st = stages.setdefault(STAGES[i], {"ms_total": 0.0, "launches": 0})
+                st["ms_total"] += tot[i]
+                st["launches"] += int(cnt[i])
+    return stages
+
+
+def steps_for(t_step_s, floor, target_s=0.08, cap=4000):
+    """Enough steps for a timed region of about target_s (so that the clock
+    sampler, every 100 ms, sees it), at least `floor`."""
+    return int(min(cap, max(floor, math.ceil(target_s / max(t_step_s, 1e-7)))))
+
+
+def measure_layer(sef, shape, T, weights, seed, dev, stream, pk, steps, warmup, clocks, tag,
+                  world=1, name=None, scratch=None):
+    """One layer workload: time K steps (L2 flushed before every step when
+    the active weights would fit twice in L2), profile the stages, and return
+    the entry of the bench line's `workloads` block (and the flush buffer)."""
+    import torch
+
+    import synth
+    wr = synth.router_weight(shape, seed, 0, dev)
+    wg, wu, wd = synth.expert_weights(shape, seed, 0, dev)
+    layer = make_layer(sef, shape, wr, wg, wu, wd, weights,
+                       router_bias=synth.router_offset(shape), max_tokens=max(T, 128))
+    del wr, wg, wu, wd
+    torch.cuda.empty_cache()
+    try:
+        x = synth.tokens(shape, T, seed, 0, dev)
+        y = torch.empty_like(x)
+        layer.forward(x, y, stream=stream)
+        counts = layer.routing()["counts"].cpu().numpy()
+        alg = algorithmic(shape, T, counts, weights)
+        flush = world == 1 and alg["bytes"] < 2 * L2_BYTES
+        if flush and scratch is None:
+            scratch = torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=dev)
+        # calibrate the step count
+        t_cal = (time_steps_flushed(layer, x, y, 3, 1, stream, scratch) if flush else
+                 time_steps(layer, x, y, 3, 1, world, stream)[0]) / 3 / 1e3
+        k = steps_for(t_cal, steps)
+        if clocks:
+            clocks.mark(tag + "_start")
+        if flush:
+            ms = time_steps_flushed(layer, x, y, k, warmup, stream, scratch)
+        else:
+            ms, _, _ = time_steps(layer, x, y, k, warmup, world, stream)
+        if clocks:
+            clocks.mark(tag + "_end")
+        ms = max_over_ranks(ms, world)
+        _, _, stages = time_steps(layer, x, y, min(k, 200), 1, world, stream, profile=True)
+        t_step = ms / k / 1e3
+        alg["calls"] = min(k, 200)
+        for key_ in ("up_flops", "down_flops", "up_bytes", "down_bytes", "bytes", "flops"):
+            alg[key_] = alg[key_] * alg["calls"]
+        roof = dominant_roofline(stages, alg, lambda st_: kernel_name(st_, shape, T, weights), pk,
+                                 lambda kn: measured_traffic(kn, traffic_key(name or shape.name, T, shape, weights)))
+        for key_ in ("up_flops", "down_flops", "up_bytes", "down_bytes", "bytes", "flops"):
+            alg[key_] = alg[key_] // alg["calls"]
+        entry = {"tokens_per_s": round(world * T / t_step, 1),
+                 "us_per_step": round(t_step * 1e6, 2),
+                 "steps": k,
+                 "layer_roofline": layer_roofline(alg, t_step, pk),
+                 "roofline": roof,
+                 "active_experts": alg["active_experts"],
+                 "stages_us": {s_: round(v["ms_total"] * 1e3 / alg["calls"], 1) for s_, v in stages.items()},
+                 "clocks": clocks.summary(tag + "_start", tag + "_end") if clocks else None}
+        if flush:
+            entry["l2"] = "flushed before every step (512 MB write, untimed); steps timed one by one"
+        else:
+            entry["l2"] = "inputs larger than L2"
+        return entry, scratch
+    finally:
+        layer.close()
+
+
+def build_stack(sef, B, seed, dev, weights="bf16"):
+    import torch
+
+    import synth
+    shape = synth.MIXTRAL
+    layers = []
+    for l in range(synth.STACK_LAYERS):
+        wr = synth.router_weight(shape, seed, l, dev)
+        wg, wu, wd = synth.expert_weights(shape, seed, l, dev)
+        layers.append(make_layer(sef, shape, wr, wg, wu, wd, weights, max_tokens=max(B, 1)))
+        del wr, wg, wu, wd
+    torch.cuda.empty_cache()
+    return layers
+
+
+def measure_stack(sef, layers, B, seed, dev, stream, pk, steps, warmup, clocks, tag, world=1,
+                  weights="bf16", exact=False):
+    """One decode-stack step = h reset to the batch's input, then the 32
+    layers (RMSNorm -> MoE -> residual), over B single-token sequences.
+    Times exactly `steps` steps when `exact`, else enough steps for ~0.15 s
+    (at least `steps`).  Returns (entry, launches in the timed region, steps
+    timed, the batch's input)."""
+    import torch
+
+    import synth
+    shape = synth.MIXTRAL
+    lib = sef.library()
+    gamma = torch.ones(shape.d_model, dtype=torch.bfloat16, device=dev)
+    h0 = synth.tokens(shape, B, seed, 0, dev)
+    h = h0.clone()
+
+    def step():
+        h.copy_(h0)       # every step starts from the same hidden state
+        for layer in layers:
+            layer.forward_stack_layer(h, gamma, synth.STACK_EPS, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def timed(k, profile):
+        for layer in layers:
+            lib.colibri_profile_enable(layer.handle, 1 if profile else 0)
+        n0 = sum(l.launch_count for l in layers)
+        barrier(world)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return max_over_ranks(a.elapsed_time(b), world), sum(l.launch_count for l in layers) - n0
+
+    if exact:
+        k = steps
+    else:
+        ms_cal, _ = timed(2, False)
+        k = steps_for(ms_cal / 2 / 1e3, steps, target_s=0.15, cap=200)
+    if clocks:
+        clocks.mark(tag + "_start")
+    ms, launches = timed(k, False)
+    if clocks:
+        clocks.mark(tag + "_end")
+    time.sleep(0.5)
+    kp = min(k, 10)
+    ms_prof, _ = timed(kp, True)
+    stages = profile_stages(lib, [l.handle for l in layers])
+    # per-layer algorithmic work of one step (every step routes alike: h is reset)
+    alg = {"calls": kp, "up_flops": 0, "down_flops": 0, "up_bytes": 0, "down_bytes": 0,
+           "bytes": 0, "flops": 0}
+    active = 0
+    for layer in layers:
+        a_l = algorithmic(shape, B, layer.routing()["counts"].cpu().numpy(), weights)
+        active += a_l["active_experts"]
+        for key_ in ("up_flops", "down_flops", "up_bytes", "down_bytes", "bytes", "flops"):
+            alg[key_] += a_l[key_]
+        assert layer.check() == 0
+    # RMSNorm reads and writes the hidden state once more per layer
+    alg["bytes"] += synth.STACK_LAYERS * (2 * B * shape.d_model * 2 + shape.d_model * 2)
+    step_s = ms / k / 1e3
+    per_step = dict(alg)
+    for key_ in ("up_flops", "down_flops", "up_bytes", "down_bytes", "bytes", "flops"):
+        alg[key_] *= kp
+    roof = dominant_roofline(stages, alg, lambda st_: kernel_name(st_, shape, B, weights), pk,
+                             lambda kn: measured_traffic(kn, traffic_key("stack", B, shape, weights)))
+    entry = {"tokens_per_s": round(world * B / step_s, 1),
+             "ms_per_step": round(step_s * 1e3, 4),
+             "steps": k,
+             "stack_roofline": {"bound": "hbm", "bytes_per_step": int(per_step["bytes"]),
+                                "achieved_gbs": round(per_step["bytes"] / step_s / 1e9, 1),
+                                "peak": pk["hbm_gbs"],
+                                "frac": round(per_step["bytes"] / step_s / 1e9 / pk["hbm_gbs"], 4),
+                                "active_experts_per_step": active},
+             "roofline": roof,
+             "stages_us_per_step": {s_: round(v["ms_total"] * 1e3 / kp, 1) for s_, v in stages.items()},
+             "ms_per_step_profiled": round(ms_prof / kp, 4),
+             "clocks": clocks.summary(tag + "_start", tag + "_end") if clocks else None,
+             "l2": "inputs larger than L2 (90 GB of weights)"}
+    return entry, int(launches), k, h0
+
+
+def gpu_id_of(dev):
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    uid = str(getattr(props, "uuid", "") or "")
+    return (uid if uid.startswith("GPU-") else "GPU-" + uid) if uid else str(dev.index or 0)
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -338,10 +602,7 @@ def run_ours(args):
         label += ", soft routing" if args.top_k == shape.n_experts else f", top-{args.top_k}"
     T = args.tokens or T_default
     pk = peaks()
-    props = torch.cuda.get_device_properties(dev)
-    uid = str(getattr(props, "uuid", "") or "")
-    gpu_id = (uid if uid.startswith("GPU-") else "GPU-" + uid) if uid else str(local)
-    clocks = ClockSampler(gpu_id) if rank == 0 else None
+    clocks = ClockSampler(gpu_id_of(dev)) if rank == 0 else None
 
     # weights: layer seed per rank (replicas over independent synthetic layers)
     seed = rank_seed(args.seed, rank)
@@ -379,45 +640,14 @@ def run_ours(args):
     step_ms = ms / args.steps
     value = job_throughput(world, T, args.steps, ms)
 
-    # roofline of the dominant kernel (largest share of the timed region)
-    dom = max(stages, key=lambda s: stages[s]["ms_total"])
-    per_launch_s = stages[dom]["ms_total"] / stages[dom]["launches"] / 1e3
-    # the library runs bf16 layers on the tcgen05 GEMMs (executor auto); a
-    # small batch routes and gathers in one kernel, so look at the dtype
-    grouped = shape.dtype == "bf16"
-    i8 = "_i8" if args.weights == "int8" else ""
-    # decode-sized batches (at most 16 pairs per expert on average) run the
-    # GEMMs with the weights as the MMA's M operand
-    gk = "grouped_gemm_dec" if T * shape.top_k <= 16 * shape.n_experts else "grouped_gemm_tc"
-    kname = {("expert_up", True): gk + "<kGateUp>", ("expert_down", True): gk + "<kDown>",
-             ("expert_up", False): "ffn_up_stream" + i8, ("expert_down", False): "ffn_down_stream" + i8}.get(
-        (dom, grouped), dom)
-    workload = f"{args.workload}_T{T}"
-    # the kernel's bound: tensor when its FLOPs take longer at the tensor peak
-    # than its bytes at the HBM peak (prefill), HBM otherwise (decode sizes)
-    fl_dom = alg["up_flops"] if dom == "expert_up" else alg["down_flops"]
-    by_dom = {"expert_up": alg["up_bytes"], "expert_down": alg["down_bytes"]}.get(dom, alg["bytes"])
-    tensor_bound = fl_dom / (pk["bf16_tflops"] * 1e12) >= by_dom / (pk["hbm_gbs"] * 1e9)
-    if grouped and dom in ("expert_up", "expert_down") and tensor_bound:
-        fl = fl_dom
-        achieved = fl / per_launch_s / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
-                "peak_kind": f"bf16 dense burst, {pk['source']}"}
-    else:
-        by = {"expert_up": alg["up_bytes"], "expert_down": alg["down_bytes"]}.get(dom, alg["bytes"])
-        achieved = by / per_launch_s / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / pk["hbm_gbs"], 4), "peak_kind": f"HBM copy, {pk['source']}"}
-    roof["kernel"] = kname
-    roof["share_of_step"] = round(stages[dom]["ms_total"] / sum(v["ms_total"] for v in stages.values()), 4)
-    roof["traffic"] = measured_traffic(kname, workload)
-    roof["algorithmic_per_launch"] = fl_dom if roof["bound"] == "tensor" else by_dom
-
-    whole = {"roofline_time_us": round(1e6 * max(alg["bytes"] / (pk["hbm_gbs"] * 1e9),
-                                                 alg["flops"] / (pk["bf16_tflops"] * 1e12)), 1),
-             "step_us": round(step_ms * 1e3, 1)}
-    whole["frac"] = round(whole["roofline_time_us"] / whole["step_us"], 4)
+    # roofline of the dominant kernel (largest share of the profiled region)
+    alg_run = dict(alg, calls=args.steps)
+    for key_ in ("up_flops", "down_flops", "up_bytes", "down_bytes", "bytes", "flops"):
+        alg_run[key_] = alg[key_] * args.steps
+    wkey = traffic_key(args.workload, T, shape, args.weights)
+    roof = dominant_roofline(stages, alg_run, lambda st_: kernel_name(st_, shape, T, args.weights), pk,
+                             lambda kn: measured_traffic(kn, wkey))
+    whole = layer_roofline(alg, step_ms / 1e3, pk)
 
     # end to end through the public C API on pinned host buffers: every step
     # uploads x and downloads y; the pipelined calls overlap one step's copies
@@ -441,8 +671,7 @@ def run_ours(args):
     sweep = {}
     scratch = None
     if not args.no_sweep:
-        for Ts, ex in [(t, "auto") for t in sweep_T if t <= max_t]:
-            layer.set_executor(ex)
+        for Ts in [t for t in sweep_T if t <= max_t]:
             xs = synth.tokens(shape, Ts, seed, 0, dev)
             ys = torch.empty_like(xs)
             layer.forward(xs, ys, stream=stream)
@@ -458,7 +687,6 @@ def run_ours(args):
             else:
                 ms_s, _, _ = time_steps(layer, xs, ys, args.steps, args.warmup, world, stream)
             _, _, st_s = time_steps(layer, xs, ys, args.steps, 1, world, stream, profile=True)
-            layer.set_executor("auto")
             ms_s = max_over_ranks(ms_s, world)
             t_step = ms_s / args.steps / 1e3
             entry = {"tokens_per_s": round(world * Ts / t_step, 1),
@@ -469,13 +697,48 @@ def run_ours(args):
                                    for k, v in st_s.items()}}
             if flush:
                 entry["l2"] = "flushed before every step (512 MB write, untimed); steps timed one by one"
-            sweep[f"T{Ts}" + ("" if ex == "auto" else "_" + ex)] = entry
+            sweep[f"T{Ts}"] = entry
+    layer.close()
+    del x, y
+    torch.cuda.empty_cache()
+
+    # the other workloads, each timed and clock-sampled on its own (default run only)
+    workloads = None
+    if (not args.no_workloads and args.workload == "mixtral" and args.tokens is None
+            and not args.top_k and args.weights == "bf16"):
+        workloads = {}
+        wsteps, wwarm = max(3, min(args.steps, 10)), max(3, min(args.warmup, 5))
+        plan = [("qwen2_moe", synth.QWEN2, 1, "bf16"), ("qwen2_moe", synth.QWEN2, 64, "bf16"),
+                ("qwen2_moe", synth.QWEN2, 8192, "bf16"),
+                ("deepseek_moe", synth.DEEPSEEK, 16384, "bf16"),
+                ("deepseek_moe_masked", synth.DEEPSEEK_MASKED, 16384, "bf16"),
+                ("mixtral", synth.MIXTRAL, 1, "int8"), ("mixtral", synth.MIXTRAL, 4096, "int8")]
+        for wl, shp, Tw, wt in plan:
+            tag = f"{wl}_T{Tw}" + ("" if wt == "bf16" else f"_{wt}")
+            entry, scratch = measure_layer(sef, shp, Tw, wt, seed, dev, stream, pk, wsteps, wwarm,
+                                           clocks, tag, world, name=wl, scratch=scratch)
+            entry["workload"] = f"{WORKLOADS[wl][2]}, T={Tw} tokens" + \
+                ("" if wt == "bf16" else f", {wt} expert weights")
+            workloads[tag] = entry
+        scratch = None
+        torch.cuda.empty_cache()
+        layers = build_stack(sef, max(synth.STACK_BATCHES), seed, dev)
+        try:
+            for B in synth.STACK_BATCHES:
+                entry, _, _, _ = measure_stack(sef, layers, B, seed, dev, stream, pk, wsteps, wwarm,
+                                               clocks, f"stack_B{B}", world)
+                entry["workload"] = f"{WORKLOADS['stack'][2]}, batch {B}"
+                workloads[f"stack_B{B}"] = entry
+        finally:
+            for l_ in layers:
+                l_.close()
+            torch.cuda.empty_cache()
     if clocks:
         clocks.stop()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(shape, x, seed=seed, target_s=args.cpu_seconds)
+        cpu = cpu_baseline(shape, T, seed=seed, target_s=args.cpu_seconds)
 
     out = {
         "metric": "MoE-layer tokens/s at 1 GB300; % of HBM (decode) / bf16 TC (prefill) roofline",
@@ -498,9 +761,10 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "sweep": sweep,
     }
+    if workloads is not None:
+        out["workloads"] = workloads
     if rank == 0:
         print(json.dumps(out), flush=True)
-    layer.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -509,8 +773,6 @@ def run_ours(args):
 def run_stack(args):
     """One step = 32 Mixtral-shaped layers, each RMSNorm -> MoE -> residual,
     over a batch of B single-token sequences; weight-streaming bound."""
-    import ctypes
-
     import torch
 
     import sparse_expert_ffn_gb300 as sef
@@ -522,87 +784,71 @@ def run_stack(args):
     shape, B = synth.MIXTRAL, args.tokens or 64
     pk = peaks()
     seed = rank_seed(args.seed, rank)
-    layers = []
-    for l in range(synth.STACK_LAYERS):
-        wr = synth.router_weight(shape, seed, l, dev)
-        wg, wu, wd = synth.expert_weights(shape, seed, l, dev)
-        layers.append(make_layer(sef, shape, wr, wg, wu, wd, args.weights, max_tokens=max(B, 1)))
-        del wr, wg, wu, wd
-    torch.cuda.empty_cache()
-    gamma = torch.ones(shape.d_model, dtype=torch.bfloat16, device=dev)
-    h0 = synth.tokens(shape, B, seed, 0, dev)
-    h = h0.clone()
-    lib = sef.library()
-
-    def step():
-        for layer in layers:
-            layer.forward_stack_layer(h, gamma, synth.STACK_EPS)
-
-    for _ in range(args.warmup):
-        h.copy_(h0)
-        step()
-    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_id_of(dev)) if rank == 0 else None
     stream = torch.cuda.current_stream()
+    layers = build_stack(sef, B, seed, dev, args.weights)
+    entry, launches, k, h0 = measure_stack(sef, layers, B, seed, dev, stream, pk, args.steps,
+                                           args.warmup, clocks, "timed", world, args.weights,
+                                           exact=True)
+    step_ms = entry["ms_per_step"]
 
-    def timed(profile):
+    # end to end through the public API on pinned host buffers: every step
+    # uploads the batch's hidden state, runs the 32 layers in place and
+    # downloads the result
+    gamma = torch.ones(shape.d_model, dtype=torch.bfloat16, device=dev)
+    hh = h0.cpu().pin_memory()
+    oh = torch.empty_like(hh).pin_memory()
+    h = torch.empty_like(h0)
+    e2e_steps = max(3, min(k, 20))
+
+    def host_step():
+        h.copy_(hh, non_blocking=True)
         for layer in layers:
-            lib.colibri_profile_enable(layer.handle, 1 if profile else 0)
-        n0 = sum(l.launch_count for l in layers)
-        barrier(world)
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        return max_over_ranks(a.elapsed_time(b), world), sum(l.launch_count for l in layers) - n0
+            layer.forward_stack_layer(h, gamma, synth.STACK_EPS, stream=stream)
+        oh.copy_(h, non_blocking=True)
 
-    ms, launches = timed(False)
-    # per-stage kernel times from a second pass with an event pair per launch
-    time.sleep(1.0)
-    ms_prof, _ = timed(True)
-    stages = {}
-    active = 0
+    host_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        host_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": round(world * B * e2e_steps / e2e_s, 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(hh.numel() * hh.element_size()),
+           "d2h_bytes_per_step": int(oh.numel() * oh.element_size())}
+    if clocks:
+        clocks.stop()
     for layer in layers:
-        tot = (ctypes.c_double * 7)()
-        cnt = (ctypes.c_uint64 * 7)()
-        lib.colibri_profile_read(layer.handle, tot, cnt)
-        for i in range(7):
-            if cnt[i]:
-                st = stages.setdefault(STAGES[i], {"ms_total": 0.0, "launches": 0})
-                st["ms_total"] += tot[i]
-                st["launches"] += int(cnt[i])
-        active += int((layer.routing()["counts"] > 0).sum().item())
-        assert layer.check() == 0
-    step_s = ms / args.steps / 1e3
-    d, f, E = shape.d_model, shape.d_ff, shape.n_experts
-    wbytes = d * f * (1.0 + 8.0 / 4096) if args.weights == "int8" else d * f * 2
-    step_bytes = int(active * 3 * wbytes + synth.STACK_LAYERS * (d * E * 2 + 4 * B * d * 2 + d * 2))
+        layer.close()
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = stack_cpu_baseline(B, seed, target_s=args.cpu_seconds)
+
     out = {
         "metric": "MoE-layer tokens/s at 1 GB300; % of HBM (decode) / bf16 TC (prefill) roofline",
-        "value": round(job_throughput(world, B, args.steps, ms), 1), "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "value": entry["tokens_per_s"], "unit": "tokens/s",
+        "n_gpus": world, "steps": k, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{WORKLOADS['stack'][2]}, batch {B}" + (", int8 expert weights" if args.weights == "int8" else ""),
                    "weights": args.weights, "layers": synth.STACK_LAYERS,
                    "batch": B, "parallelism": f"token-parallel x{world}",
-                   "l2": "inputs larger than L2 (90 GB of weights)"},
-        "stack_roofline": {"bound": "hbm", "bytes_per_step": step_bytes,
-                           "achieved_gbs": round(step_bytes / step_s / 1e9, 1),
-                           "peak": pk["hbm_gbs"],
-                           "frac": round(step_bytes / step_s / 1e9 / pk["hbm_gbs"], 4),
-                           "active_experts_per_step": active},
-        "stages_us_per_step": {k: round(v["ms_total"] * 1e3 / args.steps, 1) for k, v in stages.items()},
-        "ms_per_step_profiled": round(ms_prof / args.steps, 4),
-        "gpu_launches": int(launches),
+                   "l2": entry["l2"]},
+        "roofline": entry["roofline"],
+        "stack_roofline": entry["stack_roofline"],
+        "stages_us_per_step": entry["stages_us_per_step"],
+        "ms_per_step_profiled": entry["ms_per_step_profiled"],
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "clocks": entry["clocks"],
+        "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
-    for layer in layers:
-        layer.close()
 
 
 # ----------------------------------------------------------------------------- oracle (CPU)
@@ -627,13 +873,11 @@ def _oracle_weights(wr, wg, wu, wd):
     return (oracle.to_f64(wr), oracle.to_f64(wg), oracle.to_f64(wu), oracle.to_f64(wd))
 
 
-def cpu_baseline(shape, x, seed=0, target_s=15.0):
+def cpu_baseline(shape, T, seed=0, target_s=15.0):
     """The oracle, as it stands, on a bounded sample of the workload's tokens."""
-    import numpy as np
-
     import oracle
     import synth
-    xh, wr, wg, wu, wd = _host_inputs(shape, x.shape[0], seed)
+    xh, wr, wg, wu, wd = _host_inputs(shape, T, seed)
     W = _oracle_weights(wr, wg, wu, wd)
     del wg, wu, wd
     x64 = oracle.to_f64(xh)
@@ -651,6 +895,40 @@ def cpu_baseline(shape, x, seed=0, target_s=15.0):
     return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"first {n} of the {x64.shape[0]} tokens, whole layer (float64 numpy, BLAS "
                       f"threads = all {cores} cores), {dt:.1f} s"}
+
+
+def stack_cpu_baseline(B, seed=0, target_s=15.0):
+    """The oracle's stack layer (RMSNorm, MoE, residual), as it stands, on
+    the batch's hidden state, for as many of the 32 layers as fit in about
+    target_s (at least one), scaled to a 32-layer step.  Converting a layer's
+    weights to float64 for the oracle is not timed."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth
+    shape = synth.MIXTRAL
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    h = oracle.to_f64(synth.tokens(shape, B, seed, 0, dev).cpu())
+    g = np.ones(shape.d_model)
+    spent, done = 0.0, 0
+    for l in range(synth.STACK_LAYERS):
+        wr = synth.router_weight(shape, seed, l, dev).cpu()
+        wg, wu, wd = synth.expert_weights(shape, seed, l, dev)
+        W = _oracle_weights(wr, wg.cpu(), wu.cpu(), wd.cpu())
+        del wg, wu, wd
+        t0 = time.perf_counter()
+        h = oracle.stack_layer(h, g, synth.STACK_EPS, *W, shape.top_k)["h_out"]
+        spent += time.perf_counter() - t0
+        done += 1
+        del W
+        if spent * (done + 1) / done > target_s:
+            break
+    step_s = spent / done * synth.STACK_LAYERS
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(B / step_s, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"the first {done} of the 32 layers at batch {B} ({spent:.1f} s, float64 "
+                      f"numpy, BLAS threads = all {cores} cores), scaled to a 32-layer step"}
 
 
 def run_reference(args):

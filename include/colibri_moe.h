@@ -54,7 +54,8 @@ typedef enum {
     COLIBRI_EXEC_GROUPED = 2      /* tcgen05 grouped GEMM expert FFN (bf16 only) */
 } colibri_executor_t;
 
-/* Layer shape.  d_model % 64 == 0 and d_ff % 128 == 0 are required
+/* Layer shape.  d_model % 64 == 0, d_model <= 57856 (one token row of the
+ * CUDA-core router in shared memory) and d_ff % 128 == 0 are required
  * (UNSUPPORTED otherwise); 1 <= top_k <= n_experts <= 256; top_k <= 8, or
  * top_k == n_experts.
  * top_k == n_experts selects soft routing (m.nxbn.cn section 2.2: a Soft MoE
@@ -290,7 +291,7 @@ colibri_status_t colibri_profile_read(colibri_moe_t* h, double* total_ms, uint64
  * the device memory, or in a loop that cannot take the device-wide
  * synchronisation an allocation may cause.  Nothing is allocated: the call's
  * intermediate data lives in one fixed file-scope device array inside the
- * library (about 4.7 MiB, held by every GPU that loads the library until the
+ * library (about 4.6 MiB, held by every GPU that loads the library until the
  * process exits).
  *
  *   x           [T, d_model] device, dtype
@@ -302,17 +303,31 @@ colibri_status_t colibri_profile_read(colibri_moe_t* h, double* total_ms, uint64
  *   perm        [T * top_k] device int32, written
  * Limits of the fixed array: d_model * n_experts <= 1048576 and
  * T * top_k <= 131072; larger sizes return COLIBRI_ERR_INVALID_ARG before any
- * CUDA call.  Shape rules as colibri_init (d_model % 64 == 0, n_experts <= 256,
- * top_k <= 8 or top_k == n_experts (soft routing, as in colibri_moe_config_t):
- * COLIBRI_ERR_UNSUPPORTED otherwise).
+ * CUDA call.  Shape rules as colibri_init (d_model % 64 == 0, d_model <=
+ * 57856, n_experts <= 256, top_k <= 8 or top_k == n_experts (soft routing, as
+ * in colibri_moe_config_t): COLIBRI_ERR_UNSUPPORTED otherwise, before any
+ * CUDA call).
  *
  * Runs on the current device, ordered on `stream`, without waiting for it.
  * The first call on a device looks up the array's device address and checks
- * the architecture; make that first call before any stream capture.  All
- * calls on a device share the array and it keeps the last call's contents:
- * calls that overlap on the GPU (different streams, or unordered graph nodes)
- * race and give wrong results.  Results equal those of colibri_forward +
- * colibri_get_routing on a handle with the same weights.
+ * the architecture; make that first call before any stream capture.  The
+ * address is kept for the life of the process: after cudaDeviceReset the
+ * library's module is reloaded and the kept address is stale, so
+ * cudaDeviceReset is not supported in a process that calls this entry point.
+ * All calls on a device share the array and it keeps the last call's
+ * contents: calls that overlap on the GPU (different streams, or unordered
+ * graph nodes) race and give wrong results.
+ *
+ * The logits are computed by the CUDA-core router, in the same order as
+ * colibri_forward on a handle for float32 layers and for bf16 batches below
+ * 512 tokens, so those results equal colibri_get_routing's bit for bit.
+ * bf16 handles route batches of 512 tokens and more on the tensor cores,
+ * which add the products in another order: the gates may then differ in the
+ * last bits, and top-k may differ on tokens whose deciding logits lie within
+ * float32 rounding of each other.  Counts and perm are always the dispatch
+ * of the returned topk_idx.  A failure the dispatch detects on the device
+ * (an expert id out of range, which the router never writes) sets every
+ * counts[e] to -1.
  */
 colibri_status_t colibri_route_static(const void* x, const void* w_router,
                                       const float* router_bias, int32_t T, int32_t d_model,
@@ -376,7 +391,8 @@ colibri_status_t colibri_gather_rows(const void* x, int32_t x_rows, const int32_
  *               range are skipped, so every access stays in bounds)
  *   inv_scratch [T * k] device int32, overwritten (the inverse of perm)
  *   y           [T, d_model] device, dtype, 16-byte aligned
- * d_model % 8 == 0.  Runs on the current device, ordered on `stream`.
+ * d_model % 8 == 0 and T * k <= INT32_MAX (COLIBRI_ERR_INVALID_ARG
+ * otherwise).  Runs on the current device, ordered on `stream`.
  */
 colibri_status_t colibri_combine_rows(const void* rows, int32_t rows_dtype, const float* topk_w,
                                       const int32_t* perm, int32_t T, int32_t k, int32_t d_model,

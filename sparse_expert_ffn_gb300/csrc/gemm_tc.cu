@@ -10,8 +10,11 @@
 //            one tile = 128 rows x (128 gate + 128 up) columns; the epilogue
 //            reads both halves from TMEM and writes H = silu(G) * U (bf16).
 //   kDown    A = H [pairs, f], B = W_down^T [d, f] per expert, K = f
-//            one tile = 128 rows x 256 output features, written as float32
-//            (optionally one K slice of it: split-K for small batches).
+//            one tile = 128 rows x 256 output features.  Without K slices
+//            the rows Y are stored as bf16 (one rounding of each element, as
+//            for H; the combine then adds the k rows in float32 and rounds y
+//            once more); with K slices (small batches) each slice is stored
+//            as float32 and the combine adds the slices first.
 //   kRouter  A = x [T, d] (the caller's tokens), B = packed router [E_pad, d]:
 //            the router logits of 128 tokens per tile (N = E rounded up to 16),
 //            top-k and softmax in the epilogue (p1 section 3.3 stage 2).

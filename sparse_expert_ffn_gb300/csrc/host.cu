@@ -196,6 +196,7 @@ colibri_status_t validate_config(const colibri_moe_config_t* c) {
     if (c->n_experts > 256 || (c->top_k > 8 && c->top_k != c->n_experts))
         return COLIBRI_ERR_UNSUPPORTED;
     if (c->d_model % 64 != 0 || c->d_ff % 128 != 0) return COLIBRI_ERR_UNSUPPORTED;
+    if (!router_simt_fits(c->d_model)) return COLIBRI_ERR_UNSUPPORTED;
     if (c->executor == COLIBRI_EXEC_GROUPED && c->dtype != COLIBRI_DTYPE_BF16)
         return COLIBRI_ERR_UNSUPPORTED;
     return COLIBRI_OK;
@@ -880,6 +881,7 @@ colibri_status_t colibri_combine_rows(const void* rows, int32_t rows_dtype, cons
     if (rows_dtype != COLIBRI_DTYPE_FP32 && !(rows_dtype == COLIBRI_DTYPE_BF16 && dtype == COLIBRI_DTYPE_BF16))
         return COLIBRI_ERR_INVALID_ARG;
     if (((uintptr_t)rows & 15) || ((uintptr_t)y & 15) || d_model % 8) return COLIBRI_ERR_INVALID_ARG;
+    if ((int64_t)T * k > INT32_MAX) return COLIBRI_ERR_INVALID_ARG;   // pair indices are int32
     if (T == 0) return COLIBRI_OK;
     const cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_invert_perm(perm, T * k, inv_scratch, s);

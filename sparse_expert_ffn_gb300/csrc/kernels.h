@@ -14,6 +14,9 @@ enum class DType : int;
 // a host-side cache keeps it off the per-launch path.
 cudaError_t smem_attr(const void* kernel, int bytes);
 
+// The CUDA-core router keeps one token row of d floats (+256 logits) in
+// shared memory: d_model beyond that limit (about 57 000) is not supported.
+bool router_simt_fits(int d);
 cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const float* bias,
                                int ntok, int d, int E, int k, int32_t* idx, float* w,
                                cudaStream_t s, bool soft = false);

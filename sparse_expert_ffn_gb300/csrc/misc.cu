@@ -90,11 +90,12 @@ __device__ __forceinline__ float4 load_y4(const __nv_bfloat16* row, int g) {
 // type Y was stored in (bf16 for prefill on the tensor cores).
 template <typename T, bool kSplit, typename TY>
 __global__ void combine_kernel(const TY* __restrict__ Y, const float* __restrict__ topk_w,
-                               const int32_t* __restrict__ inv, int k, int d, int nsplit,
+                               const int32_t* __restrict__ inv, int T_, int k, int d, int nsplit,
                                size_t split_stride,
                                const T* resid, T* y) {  // resid may alias y (in-place residual)
     pdl_enter();
-    const int t = blockIdx.y;
+    // tokens on grid.y, strided: gridDim.y is capped at 65535, T is not
+    for (int t = blockIdx.y; t < T_; t += gridDim.y) {
     const int d4 = d / 4;
     const int g0 = blockIdx.x * kCombineThreads * kCombineVec + threadIdx.x;   // float4 index
     float4 acc[kCombineVec];
@@ -160,6 +161,7 @@ __global__ void combine_kernel(const TY* __restrict__ Y, const float* __restrict
             acc[u].w += to_f32(resid[o + 3]);
         }
         store4(y + o, acc[u]);
+    }
     }
 }
 
@@ -248,7 +250,9 @@ cudaError_t launch_combine(DType dt, const float* Y, bool y_bf16, const float* t
     if (T <= 0) return cudaSuccess;
     if (y_bf16 && (nsplit > 1 || dt != DType::BF16)) return cudaErrorInvalidValue;
     const int per_block = kCombineThreads * kCombineVec;   // float4 groups per block
-    const dim3 block(kCombineThreads), grid((d / 4 + per_block - 1) / per_block, T);
+    constexpr int kMaxGridY = 65535;
+    const dim3 block(kCombineThreads),
+        grid((d / 4 + per_block - 1) / per_block, std::min(T, kMaxGridY));
     cudaError_t e;
     const bool split = nsplit > 1;
     if (dt == DType::BF16) {
@@ -256,20 +260,20 @@ cudaError_t launch_combine(DType dt, const float* Y, bool y_bf16, const float* t
         auto* o = (__nv_bfloat16*)y;
         if (y_bf16)
             e = launch_pdl(combine_kernel<__nv_bfloat16, false, __nv_bfloat16>, grid, block, 0, s,
-                           (const __nv_bfloat16*)Y, topk_w, inv, k, d, nsplit, split_stride, r, o);
+                           (const __nv_bfloat16*)Y, topk_w, inv, T, k, d, nsplit, split_stride, r, o);
         else if (split)
             e = launch_pdl(combine_kernel<__nv_bfloat16, true, float>, grid, block, 0, s, Y, topk_w,
-                           inv, k, d, nsplit, split_stride, r, o);
+                           inv, T, k, d, nsplit, split_stride, r, o);
         else
             e = launch_pdl(combine_kernel<__nv_bfloat16, false, float>, grid, block, 0, s, Y, topk_w,
-                           inv, k, d, nsplit, split_stride, r, o);
+                           inv, T, k, d, nsplit, split_stride, r, o);
     } else {
         const auto* r = (const float*)resid;
         auto* o = (float*)y;
         e = split ? launch_pdl(combine_kernel<float, true, float>, grid, block, 0, s, Y, topk_w, inv,
-                               k, d, nsplit, split_stride, r, o)
+                               T, k, d, nsplit, split_stride, r, o)
                   : launch_pdl(combine_kernel<float, false, float>, grid, block, 0, s, Y, topk_w, inv,
-                               k, d, nsplit, split_stride, r, o);
+                               T, k, d, nsplit, split_stride, r, o);
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }

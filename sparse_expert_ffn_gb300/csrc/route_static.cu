@@ -13,12 +13,17 @@
 // grouped-GEMM tile list) in one file-scope device array of fixed size.
 //
 // The array is static device memory: every GPU that loads this library holds
-// it (kStaticScratchBytes, about 4.7 MiB) until the process exits.  All calls
+// it (kStaticScratchBytes, about 4.6 MiB) until the process exits.  All calls
 // on one device share it and it keeps the last call's contents, so two calls
 // that overlap on the GPU (on different streams, or in one graph without an
 // ordering edge) race on it.  Each call clears the one word that must start at
 // zero (the device status word); everything else it reads is written earlier
 // in the same call.
+//
+// A failure the dispatch detects on the device (an expert id outside
+// 0 .. n_experts-1, which the router itself never writes) cannot be returned
+// by the call, which comes back before the GPU runs; it is reported through
+// the outputs instead: every counts[e] is set to -1.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -47,7 +52,13 @@ constexpr size_t kOffTileInfo = kOffTileRow + round256((size_t)kStaticMaxTiles *
 constexpr size_t kOffNumTiles = kOffTileInfo + round256((size_t)kStaticMaxTiles * 4);
 constexpr size_t kOffKept = kOffNumTiles + 256;
 constexpr size_t kOffStatus = kOffKept + round256(256 * 4);
-constexpr size_t kStaticScratchBytes = kOffStatus + 256;
+// per-CTA counts of the multi-CTA dispatch: at most 64 CTAs x 256 experts
+constexpr size_t kOffBlockCounts = kOffStatus + 256;
+constexpr int kStaticMaxDispatchBlocks = kStaticMaxPairs / 2048;
+constexpr size_t kStaticScratchBytes = kOffBlockCounts + round256((size_t)kStaticMaxDispatchBlocks * 256 * 4);
+// Above this many pairs the dispatch runs over many CTAs (three launches),
+// as on a handle.
+constexpr int kStaticMultiDispatchPairs = 12288;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
 
@@ -82,6 +93,15 @@ colibri_status_t scratch_for_current_device(void** out) {
     return g_setup_status[dev];
 }
 
+// The dispatch's device status word, read back into the outputs: after a
+// failure every count is -1 (a valid count is never negative).
+__global__ void report_dispatch_status(const int* __restrict__ status, int32_t* __restrict__ counts,
+                                       int E) {
+    pdl_enter();
+    if (*status != 0)
+        for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = -1;
+}
+
 }  // namespace
 
 extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_router,
@@ -94,7 +114,8 @@ extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_ro
     if (dtype != COLIBRI_DTYPE_FP32 && dtype != COLIBRI_DTYPE_BF16) return COLIBRI_ERR_INVALID_ARG;
     if (T < 0 || d_model <= 0 || n_experts <= 0 || top_k <= 0 || top_k > n_experts)
         return COLIBRI_ERR_INVALID_ARG;
-    if (n_experts > 256 || (top_k > 8 && top_k != n_experts) || d_model % 64 != 0)
+    if (n_experts > 256 || (top_k > 8 && top_k != n_experts) || d_model % 64 != 0 ||
+        !router_simt_fits(d_model))
         return COLIBRI_ERR_UNSUPPORTED;
     // Sizes beyond the fixed scratch array.
     if ((int64_t)d_model * n_experts > kStaticMaxRouterElems ||
@@ -117,6 +138,7 @@ extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_ro
     int32_t* num_tiles = reinterpret_cast<int32_t*>(s + kOffNumTiles);
     int32_t* kept = reinterpret_cast<int32_t*>(s + kOffKept);
     int* status = reinterpret_cast<int*>(s + kOffStatus);
+    int32_t* block_counts = reinterpret_cast<int32_t*>(s + kOffBlockCounts);
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const DType dt = dtype == COLIBRI_DTYPE_BF16 ? DType::BF16 : DType::F32;
@@ -129,9 +151,17 @@ extern "C" colibri_status_t colibri_route_static(const void* x, const void* w_ro
     if (e == cudaSuccess)
         e = launch_router_simt(dt, x, wr_packed, router_bias, T, d, E, k, topk_idx, topk_w, cs,
                                k == E);   // top_k == n_experts: soft routing
-    if (e == cudaSuccess)
-        e = launch_dispatch(topk_idx, T * k, E, counts, offsets, perm, inv, kStaticTileRows,
+    const int n = T * k;
+    if (dispatch_blocks(n) > kStaticMaxDispatchBlocks) return COLIBRI_ERR_INVALID_ARG;  // not reached
+    if (e == cudaSuccess && n > kStaticMultiDispatchPairs)
+        e = launch_dispatch_multi(topk_idx, n, E, block_counts, counts, offsets, perm, inv,
+                                  kStaticTileRows, tile_expert, tile_row, tile_info, num_tiles,
+                                  status, INT_MAX, kept, cs);
+    else if (e == cudaSuccess)
+        e = launch_dispatch(topk_idx, n, E, counts, offsets, perm, inv, kStaticTileRows,
                             tile_expert, tile_row, tile_info, num_tiles, status, INT_MAX, kept,
                             cs);
+    if (e == cudaSuccess) e = launch_pdl(report_dispatch_status, 1, 256, 0, cs, status, counts, E);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? COLIBRI_OK : COLIBRI_ERR_CUDA;
 }

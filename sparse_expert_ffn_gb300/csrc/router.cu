@@ -20,6 +20,8 @@ namespace colibri {
 namespace {
 
 constexpr int kRouterWarps = 8;
+// Opt-in shared memory per CTA on sm_103 (227 KB).
+constexpr size_t kRouterSmemMax = 227 * 1024;
 
 // One CTA of kRouterWarps warps routes kRouterWarps / kWarpsPerToken tokens;
 // the kWarpsPerToken warps of a token split its experts (e = sub, sub + W, ...).
@@ -106,13 +108,17 @@ cudaError_t launch_router_t(const void* x, const void* wr, const float* bias, in
 
 }  // namespace
 
+bool router_simt_fits(int d) { return d > 0 && (size_t)(d + 256) * 4 <= kRouterSmemMax; }
+
 cudaError_t launch_router_simt(DType dt, const void* x, const void* wr, const float* bias,
                                int ntok, int d, int E, int k, int32_t* idx, float* w,
                                cudaStream_t s, bool soft) {
     if (ntok <= 0) return cudaSuccess;
+    if (!router_simt_fits(d)) return cudaErrorInvalidValue;
     // Few tokens: spread every token over a whole CTA; many: two warps per
-    // token, four tokens per CTA (70 KB of shared memory at d = 4096).
-    const bool small = ntok <= 256;
+    // token, four tokens per CTA (70 KB of shared memory at d = 4096), unless
+    // four token rows do not fit in shared memory.
+    const bool small = ntok <= 256 || kRouterSmemMax < (size_t)(kRouterWarps / 2) * (d + 256) * 4;
     const int sf = soft ? 1 : 0;
     if (dt == DType::BF16)
         return small ? launch_router_t<__nv_bfloat16, kRouterWarps>(x, wr, bias, ntok, d, E, k, idx, w, s, sf)

@@ -60,3 +60,28 @@ def test_inactive_experts_cost_no_weight_bytes():
     a0 = bench.algorithmic(synth.QWEN2, 64, _counts(64, 0))
     a1 = bench.algorithmic(synth.QWEN2, 64, _counts(64, 1))
     assert a1["bytes"] - a0["bytes"] == 3 * 2048 * 1408 * 2
+
+
+def test_traffic_key_names_top_k_and_weight_format():
+    from dataclasses import replace
+    assert bench.traffic_key("mixtral", 4096, synth.MIXTRAL) == "mixtral_T4096"
+    assert bench.traffic_key("mixtral", 4096, replace(synth.MIXTRAL, top_k=1)) == "mixtral_T4096_k1"
+    assert bench.traffic_key("mixtral", 1, synth.MIXTRAL, "int8") == "mixtral_T1_int8"
+    # a summary for another configuration is never matched
+    assert bench.measured_traffic("grouped_gemm_tc<kGateUp>", "mixtral_T4096_k1") is None
+
+
+def test_dominant_roofline_divides_per_launch():
+    """Two calls of a layer, one gate/up launch each: the per-launch FLOPs are
+    the per-call FLOPs, and the achieved rate is those over one launch's time."""
+    a = bench.algorithmic(synth.MIXTRAL, 4096, _counts(8, 8))
+    alg = dict(a, calls=2)
+    for k in ("up_flops", "down_flops", "up_bytes", "down_bytes", "bytes", "flops"):
+        alg[k] = a[k] * 2
+    stages = {"expert_up": {"ms_total": 2.0, "launches": 2},     # 1 ms per launch
+              "expert_down": {"ms_total": 1.2, "launches": 2}}
+    pk = {"hbm_gbs": 6769.4, "bf16_tflops": 1858.5, "source": "measured"}
+    roof = bench.dominant_roofline(stages, alg, lambda s: s, pk)
+    assert roof["bound"] == "tensor" and roof["kernel"] == "expert_up"
+    assert roof["algorithmic_per_launch"] == 4 * 4096 * 2 * 4096 * 14336
+    assert roof["achieved"] == pytest.approx(4 * 4096 * 2 * 4096 * 14336 / 1e-3 / 1e12, rel=1e-3)

@@ -13,14 +13,6 @@ from parity import Int8Case, check_output, check_routing
 pytestmark = pytest.mark.gpu
 
 
-def _sample(T, n, seed=0):
-    if T <= n:
-        return np.arange(T)
-    rng = np.random.default_rng(seed)
-    mid = rng.choice(np.arange(1, T - 1), size=n - 2, replace=False)
-    return np.sort(np.concatenate([[0, T - 1], mid]))
-
-
 def test_tiny_fp32_int8_ragged():
     c = Int8Case(synth.TINY, seed=0, max_tokens=64)
     try:
@@ -48,7 +40,7 @@ def test_mixtral_int8_decode(mixtral8, T, executor):
     x, x64 = mixtral8.tokens(T)
     y, r = mixtral8.run(x, executor)
     l, _ = check_routing(mixtral8, x64, r)
-    check_output(mixtral8, x64, y, r, l, _sample(T, 24))
+    check_output(mixtral8, x64, y, r, l)
     y2, _ = mixtral8.run(x, executor)
     assert torch.equal(y, y2)
 
@@ -57,7 +49,7 @@ def test_mixtral_int8_prefill_1024(mixtral8):
     x, x64 = mixtral8.tokens(1024)
     y, r = mixtral8.run(x, "grouped")
     l, _ = check_routing(mixtral8, x64, r)
-    check_output(mixtral8, x64, y, r, l, _sample(1024, 32))
+    check_output(mixtral8, x64, y, r, l)
 
 
 def test_tiny_fp32_int8_has_no_grouped_executor():
@@ -76,9 +68,9 @@ def test_qwen_int8_zipf_with_capacity():
         x, x64 = c.tokens(64)
         y, r = c.run(x)
         l, _ = check_routing(c, x64, r)
-        check_output(c, x64, y, r, l, _sample(64, 32))
+        check_output(c, x64, y, r, l)
         c.layer.set_capacity(3)
         y, r = c.run(x)
-        check_output(c, x64, y, r, l, _sample(64, 32), capacity=3)
+        check_output(c, x64, y, r, l, capacity=3)
     finally:
         c.close()

@@ -11,14 +11,19 @@ against the oracle.
 * One expert with k = 1 (k equal to the expert count: the soft-routing
   path): every gate is exactly 1 and the layer is a dense SwiGLU FFN.
 * Two experts with k = 1 at 700 tokens: the tensor-core router's 16-column
-  logit tile holds two live columns."""
+  logit tile holds two live columns.
+* 65 536 tokens on the tiny fp32 shape (more token rows than a grid's y
+  dimension holds: the combine strides over tokens), through colibri_forward
+  and through colibri_combine_rows."""
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import sparse_expert_ffn_gb300 as sef
 import synth
-from parity import Case, check_output, check_routing
+from parity import Y_RTOL, Case, check_output, check_routing
 
 pytestmark = pytest.mark.gpu
 
@@ -74,5 +79,36 @@ def test_two_experts_top1_on_the_tensor_core_router(lib):
     c = Case(shape, seed=14, max_tokens=700)
     try:
         _check_all(c, (700,))
+    finally:
+        c.close()
+
+
+def test_65536_tokens_forward_and_combine_rows(lib):
+    T = 65536
+    c = Case(synth.TINY, seed=15, max_tokens=T)
+    try:
+        x, x64 = c.tokens(T)
+        y, r = c.run(x, "auto")
+        l, near = check_routing(c, x64, r)
+        assert near.sum() <= 4
+        check_output(c, x64, y, r, l)
+
+        # colibri_combine_rows on rows in the expert order of the GPU's perm
+        k, d = c.shape.top_k, c.shape.d_model
+        dev = x.device
+        rows = synth.normal((T * k, d), 3, 0, 99, device=dev).float()
+        perm = torch.as_tensor(r["perm"].astype(np.int32), device=dev)
+        gates = torch.as_tensor(r["topk_w"], device=dev)
+        inv = torch.empty(T * k, dtype=torch.int32, device=dev)
+        out = torch.empty(T, d, dtype=torch.float32, device=dev)
+        st = sef.colibri_combine_rows(rows.data_ptr(), sef.DTYPE_FP32, gates.data_ptr(),
+                                      perm.data_ptr(), T, k, d, sef.DTYPE_FP32, inv.data_ptr(),
+                                      out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert st == sef.OK
+        torch.cuda.synchronize()
+        _, _, _, inv_ref = oracle.dispatch(r["topk_idx"], c.shape.n_experts)
+        ref = oracle.combine(rows.cpu().double().numpy(), r["topk_w"].astype(np.float64), inv_ref)
+        err = np.abs(out.cpu().double().numpy() - ref).max() / np.abs(ref).max()
+        assert err <= Y_RTOL["fp32"], err
     finally:
         c.close()

@@ -14,15 +14,6 @@ from parity import Case, check_output, check_routing
 pytestmark = pytest.mark.gpu
 
 
-def _sample(T, n, seed=0):
-    """n token indices spread over [0, T) including the first and last rows."""
-    if T <= n:
-        return np.arange(T)
-    rng = np.random.default_rng(seed)
-    mid = rng.choice(np.arange(1, T - 1), size=n - 2, replace=False)
-    return np.sort(np.concatenate([[0, T - 1], mid]))
-
-
 # ------------------------------------------------------------------ tiny fp32
 
 
@@ -108,7 +99,7 @@ def test_mixtral_decode_sizes(mixtral, T, executor):
     x, x64 = mixtral.tokens(T)
     y, r = mixtral.run(x, executor)
     l, _ = check_routing(mixtral, x64, r)
-    check_output(mixtral, x64, y, r, l, _sample(T, 32))
+    check_output(mixtral, x64, y, r, l)
 
 
 def test_mixtral_prefill_1024_pairs_and_split_k(mixtral):
@@ -117,7 +108,7 @@ def test_mixtral_prefill_1024_pairs_and_split_k(mixtral):
     x, x64 = mixtral.tokens(1024)
     y, r = mixtral.run(x, "grouped")
     l, _ = check_routing(mixtral, x64, r)
-    check_output(mixtral, x64, y, r, l, _sample(1024, 48))
+    check_output(mixtral, x64, y, r, l)
     y2, _ = mixtral.run(x, "grouped")
     assert torch.equal(y, y2)
 
@@ -127,7 +118,7 @@ def test_mixtral_prefill_4096(mixtral):
     y, r = mixtral.run(x, "grouped")
     l, near = check_routing(mixtral, x64, r)
     assert near.sum() < 20
-    check_output(mixtral, x64, y, r, l, _sample(4096, 48))
+    check_output(mixtral, x64, y, r, l)
     y2, _ = mixtral.run(x, "grouped")
     assert torch.equal(y, y2)
 
@@ -148,7 +139,7 @@ def test_qwen_zipf(qwen, T, executor):
     x, x64 = qwen.tokens(T)
     y, r = qwen.run(x, executor)
     l, _ = check_routing(qwen, x64, r)
-    check_output(qwen, x64, y, r, l, _sample(T, 96))
+    check_output(qwen, x64, y, r, l)
     if T >= 2048:   # Zipf skew: expert 0 is the busiest
         assert r["counts"][0] == r["counts"].max()
 
@@ -161,7 +152,7 @@ def test_qwen_decode_split_k_is_repeatable(qwen, T):
     x, x64 = qwen.tokens(T)
     y, r = qwen.run(x, "grouped")
     l, _ = check_routing(qwen, x64, r)
-    check_output(qwen, x64, y, r, l, _sample(T, 32))
+    check_output(qwen, x64, y, r, l)
     for _ in range(3):
         y2, _ = qwen.run(x, "grouped")
         assert torch.equal(y, y2)
@@ -176,7 +167,7 @@ def test_qwen_all_tokens_to_one_expert(lib):
         y, r = c.run(x, "grouped")
         assert r["counts"][5] == 1000
         l, _ = check_routing(c, x64, r)
-        check_output(c, x64, y, r, l, _sample(1000, 48))
+        check_output(c, x64, y, r, l)
     finally:
         c.close()
 
@@ -191,7 +182,7 @@ def test_deepseek_prefill_16384(lib, shape):
         x, x64 = c.tokens(16384)
         y, r = c.run(x, "grouped")
         l, near = check_routing(c, x64, r)
-        check_output(c, x64, y, r, l, _sample(16384, 64))
+        check_output(c, x64, y, r, l)
         if shape.bias == "mask4":
             assert np.all(r["counts"][3::4] == 0) and np.all(r["counts"][0::4] > 0)
     finally:
@@ -205,6 +196,6 @@ def test_deepseek_ragged_grouped(lib):
             x, x64 = c.tokens(T)
             y, r = c.run(x, "grouped")
             l, _ = check_routing(c, x64, r)
-            check_output(c, x64, y, r, l, _sample(T, 24))
+            check_output(c, x64, y, r, l)
     finally:
         c.close()

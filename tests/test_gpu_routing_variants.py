@@ -14,14 +14,6 @@ from parity import Case, check_output, check_routing
 pytestmark = pytest.mark.gpu
 
 
-def _sample(T, n, seed=0):
-    if T <= n:
-        return np.arange(T)
-    rng = np.random.default_rng(seed)
-    mid = rng.choice(np.arange(1, T - 1), size=n - 2, replace=False)
-    return np.sort(np.concatenate([[0, T - 1], mid]))
-
-
 @pytest.fixture(scope="module", params=[1, 4, 8], ids=["top1", "top4", "soft"])
 def mixtral_k(lib, request):
     c = Case(replace(synth.MIXTRAL, top_k=request.param), seed=0, max_tokens=1024)
@@ -39,7 +31,7 @@ def test_mixtral_routing_variants(mixtral_k, T, executor):
     l, _ = check_routing(mixtral_k, x64, r)
     if mixtral_k.shape.top_k == 8:
         assert np.all(r["counts"] == T)
-    check_output(mixtral_k, x64, y, r, l, _sample(T, 24))
+    check_output(mixtral_k, x64, y, r, l)
     y2, _ = mixtral_k.run(x, executor)
     assert torch.equal(y, y2)
 
@@ -52,6 +44,6 @@ def test_qwen_soft_routing_64_experts(lib):
             y, r = c.run(x)
             l, _ = check_routing(c, x64, r)
             assert np.all(r["counts"] == T)
-            check_output(c, x64, y, r, l, _sample(T, 8))
+            check_output(c, x64, y, r, l)
     finally:
         c.close()

@@ -3,8 +3,19 @@ RMSNorm -> MoE -> residual, batches of 1, 8 and 64 single-token sequences.
 
 Routing decisions compound across layers, so parity is checked per layer on
 identical inputs (teacher-forced): the GPU's input to layer l is handed to the
-oracle's stack layer and both outputs are compared.  The end-to-end drift of
-the last hidden state against an oracle run of all 32 layers is not gated."""
+oracle's stack layer and both outputs are compared, at eight layers spread
+over the 32 (the first and the last included).  On a near-tie token (routing
+inside float32 noise) the oracle's layer is evaluated at the GPU's chosen
+experts, as in the single-layer parity tests, so every checked layer compares
+every token.  The end-to-end drift of the last hidden state is not gated.
+
+Tolerances.  h_out = bf16(h + y) is compared at the bf16 bound (2e-2 of
+max|h_out|).  The MoE increment (h_out - h) is compared against the oracle's
+y element by element at 2e-2 * max|y| plus the rounding of h_out to bf16,
+which is at most half a bf16 ulp of |h_out|: 2^-8 |h_out| (7 stored mantissa
+bits).  That rounding is the only difference between the increment and y
+beyond y's own bf16 error, and it matters because |h| is several times |y|.
+"""
 
 import numpy as np
 import pytest
@@ -12,12 +23,13 @@ import torch
 
 import oracle
 import synth
-from parity import Y_RTOL, stack_case_layers
+from parity import NEAR_TIE_REL, Y_RTOL, Experts, stack_case_layers
 
 pytestmark = pytest.mark.gpu
 
 N_LAYERS = synth.STACK_LAYERS
-CHECK_LAYERS = (0, N_LAYERS - 1)
+CHECK_LAYERS = (0, 4, 9, 13, 18, 22, 27, N_LAYERS - 1)
+BF16_HALF_ULP_REL = 2.0 ** -8
 
 
 @pytest.fixture(scope="module")
@@ -29,46 +41,75 @@ def stack(lib):
     torch.cuda.empty_cache()
 
 
-def _layer_weights64(l, seed=0):
+def _run_and_record(layers, gamma, B):
+    """Run the whole stack on a batch of B tokens; at the checked layers keep
+    the layer's input, output and routing (host copies)."""
     shape = synth.MIXTRAL
-    wr = synth.router_weight(shape, seed, l, "cuda")
-    wg, wu, wd = synth.expert_weights(shape, seed, l, "cuda")
-    out = tuple(oracle.to_f64(t.cpu()) for t in (wr, wg, wu, wd))
+    h = synth.tokens(shape, B, seed=7, device="cuda")           # bf16 N(0,1) hidden state
+    rec = {}
+    for l, layer in enumerate(layers):
+        h_in = h.clone() if l in CHECK_LAYERS else None
+        layer.forward_stack_layer(h, gamma, synth.STACK_EPS)
+        if l in CHECK_LAYERS:
+            torch.cuda.synchronize()
+            assert layer.check() == 0
+            r = {k: v.cpu().numpy() for k, v in layer.routing().items()}
+            rec[l] = (oracle.to_f64(h_in.cpu()), oracle.to_f64(h.cpu()), r)
+    assert torch.isfinite(h.float()).all()
+    return rec
+
+
+def _check_layer(l, records):
+    """Compare layer l's recorded runs (one per batch size) with the oracle."""
+    shape = synth.MIXTRAL
+    wr = synth.router_weight(shape, 0, l, "cuda")
+    wg, wu, wd = synth.expert_weights(shape, 0, l, "cuda")
+    wr64 = oracle.to_f64(wr.cpu())
+    experts = Experts(wg, wu, wd)            # float64 copies made one expert at a time
     del wr, wg, wu, wd
     torch.cuda.empty_cache()
-    return out
+    g64 = np.ones(shape.d_model)
+    n_near = 0
+    us, gidxs, gates = [], [], []
+    for B, (h64, got, r) in records.items():
+        u = oracle.round_to_bf16(oracle.rmsnorm(h64, g64, synth.STACK_EPS))
+        logits = oracle.router_logits(u, wr64)
+        ref_idx = oracle.topk_select(logits, shape.top_k)
+        near = oracle.near_tie_tokens(u, wr64, logits, shape.top_k, NEAR_TIE_REL)
+        n_near += int(near.sum())
+        gidx = r["topk_idx"]
+        bad = (gidx != ref_idx).any(axis=1) & ~near
+        assert not bad.any(), f"B={B} layer {l}: routing differs on {int(bad.sum())} tokens"
+        counts, _, perm, _ = oracle.dispatch(gidx, shape.n_experts)
+        assert np.array_equal(r["counts"], counts) and np.array_equal(r["perm"], perm)
+        us.append(u)
+        gidxs.append(gidx)
+        gates.append(oracle.softmax_selected(logits, gidx))
+    # the layer at the GPU's experts (identical to the plain oracle where
+    # routing agrees), every batch in one call: each expert converted once
+    y_all = oracle.token_outputs(np.concatenate(us), np.concatenate(gidxs),
+                                 np.concatenate(gates), experts)
+    row = 0
+    for B, (h64, got, r) in records.items():
+        y_ref = y_all[row:row + B]
+        row += B
+        h_ref = oracle.round_to_bf16(h64 + y_ref)
+        err = np.abs(got - h_ref).max() / np.abs(h_ref).max()
+        assert err <= Y_RTOL["bf16"], f"B={B} layer {l}: h_out error {err:.3e}"
+        # the MoE increment against the oracle's y, plus the bf16 rounding of h_out
+        bound = Y_RTOL["bf16"] * np.abs(y_ref).max() + \
+            BF16_HALF_ULP_REL * np.maximum(np.abs(h_ref), np.abs(got))
+        dy = np.abs((got - h64) - y_ref)
+        assert np.all(dy <= bound), \
+            f"B={B} layer {l}: increment error {(dy - bound).max():.3e} above its bound"
+    return n_near
 
 
 def test_stack_teacher_forced_layers(stack):
     layers, gamma = stack
-    shape = synth.MIXTRAL
-    weights = {l: _layer_weights64(l) for l in CHECK_LAYERS}
-    g64 = np.ones(shape.d_model)
-    compared = 0
-    for B in synth.STACK_BATCHES:
-        h = synth.tokens(shape, B, seed=7, device="cuda")           # bf16 N(0,1) hidden state
-        for l, layer in enumerate(layers):
-            h_in = h.clone()
-            layer.forward_stack_layer(h, gamma, synth.STACK_EPS)
-            if l in CHECK_LAYERS:
-                torch.cuda.synchronize()
-                assert layer.check() == 0
-                r = {k: v.cpu().numpy() for k, v in layer.routing().items()}
-                h64 = oracle.to_f64(h_in.cpu())
-                ref = oracle.stack_layer(h64, g64, synth.STACK_EPS, *weights[l], shape.top_k)
-                # routing on the oracle's normalised input; near-ties allowed
-                near = oracle.near_tie_tokens(ref["u"], weights[l][0], ref["logits"], shape.top_k)
-                bad = (r["topk_idx"] != ref["topk_idx"]).any(axis=1) & ~near
-                assert not bad.any(), f"B={B} layer {l}: routing differs on {int(bad.sum())} tokens"
-                if not near.any():
-                    assert np.array_equal(r["counts"], ref["counts"])
-                    got = oracle.to_f64(h.cpu())
-                    err = np.abs(got - ref["h_out"]).max() / np.abs(ref["h_out"]).max()
-                    assert err <= Y_RTOL["bf16"], f"B={B} layer {l}: {err:.3e}"
-                    # the MoE increment itself, against the oracle's y
-                    dy = np.abs((got - h64) - ref["y"]).max() / np.abs(ref["y"]).max()
-                    assert dy <= 5e-2, f"B={B} layer {l}: increment error {dy:.3e}"
-                    compared += 1
-        assert torch.isfinite(h.float()).all()
-    # near-ties can skip a layer's output check, but not most of them
-    assert compared >= len(synth.STACK_BATCHES) * len(CHECK_LAYERS) - 1
+    runs = {B: _run_and_record(layers, gamma, B) for B in synth.STACK_BATCHES}
+    n_near = 0
+    for l in CHECK_LAYERS:
+        n_near += _check_layer(l, {B: runs[B][l] for B in synth.STACK_BATCHES})
+    # a near-tie needs two logits within ~1e-5 of each other: rare
+    assert n_near <= 4, f"{n_near} near-tie tokens over the checked layers"

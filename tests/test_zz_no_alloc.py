@@ -8,17 +8,26 @@ its intermediate data in a fixed device array inside the library instead of
 allocating.  This test calls it through the C ABI twice in a row, with
 different shapes and token counts so that leftovers of the first call would
 show in the second, and checks each result against the handle-based path
-(colibri_forward + colibri_get_routing on the same weights and tokens).  The
-two paths run the same router and dispatch kernels on the same repacked
-weights, so the routing must agree bit for bit (stricter than the parity
-tolerances).  The file sorts last so that a run stopping at the first failure
-has already run every other test.
+(colibri_forward + colibri_get_routing on the same weights and tokens).  At
+these batch sizes (below 512 tokens) the two paths run the same router and
+dispatch kernels on the same repacked weights, so the routing must agree bit
+for bit (stricter than the parity tolerances).  Every result is also checked
+against the CPU oracle under the parity rules of the other tests (near-tie
+tokens excepted from the top-k comparison; counts and perm the oracle's
+dispatch of the returned ids, bit for bit), including a batch at the array's
+pair limit that takes the multi-CTA dispatch.  The file sorts last so that a
+run stopping at the first failure has already run every other test.
 """
 
+from types import SimpleNamespace
+
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
+from parity import check_routing
 
 pytestmark = pytest.mark.gpu
 
@@ -42,6 +51,16 @@ def _routing_through_static_entry(sef, x, wr, bias, shape):
     return out
 
 
+def _check_against_oracle(x, wr, bias, shape, got):
+    """The parity rules of the other GPU tests, applied to the static entry's output."""
+    case = SimpleNamespace(shape=shape, wr64=oracle.to_f64(wr.cpu()),
+                           off64=None if bias is None else bias.double().cpu().numpy())
+    r = {k: v.cpu().numpy() for k, v in got.items()}
+    assert int(r["counts"].sum()) == x.shape[0] * shape.top_k   # no failure reported (-1 counts)
+    _, near = check_routing(case, oracle.to_f64(x.cpu()), r)
+    return int(near.sum())
+
+
 def test_route_static_matches_handle_path_on_two_calls_in_a_row(lib):
     sef = lib
     dev = torch.device("cuda", 0)
@@ -63,6 +82,23 @@ def test_route_static_matches_handle_path_on_two_calls_in_a_row(lib):
         layer.close()
         for key in ("topk_idx", "topk_w", "counts", "perm"):
             assert torch.equal(got[key], want[key]), f"{shape.name} T={T}: {key} differs"
+        _check_against_oracle(x, wr, bias, shape, got)
+
+
+def test_route_static_at_its_pair_limit_matches_oracle(lib):
+    """131 072 (token, slot) pairs, the most the array holds: the router's
+    many-token variant and the multi-CTA dispatch, then a small call that
+    reuses the array."""
+    sef = lib
+    dev = torch.device("cuda", 0)
+    for shape, T, seed in [(synth.QWEN2, 65536, 5), (synth.DEEPSEEK_MASKED, 300, 6)]:
+        wr = synth.router_weight(shape, seed, 0, dev)
+        b = synth.router_offset(shape)
+        bias = None if b is None else b.to(dev)
+        x = synth.tokens(shape, T, seed, 0, dev)
+        got = _routing_through_static_entry(sef, x, wr, bias, shape)
+        n_near = _check_against_oracle(x, wr, bias, shape, got)
+        assert n_near <= max(2, T // 5000)
 
 
 def test_route_static_rejects_sizes_beyond_its_array(lib):
