@@ -318,14 +318,13 @@ colibri_status_t colibri_profile_read(colibri_moe_t* h, double* total_ms, uint64
  * contents: calls that overlap on the GPU (different streams, or unordered
  * graph nodes) race and give wrong results.
  *
- * The logits are computed by the CUDA-core router, in the same order as
- * colibri_forward on a handle for float32 layers and for bf16 batches below
- * 512 tokens, so those results equal colibri_get_routing's bit for bit.
- * bf16 handles route batches of 512 tokens and more on the tensor cores,
- * which add the products in another order: the gates may then differ in the
- * last bits, and top-k may differ on tokens whose deciding logits lie within
- * float32 rounding of each other.  Counts and perm are always the dispatch
- * of the returned topk_idx.  A failure the dispatch detects on the device
+ * The logits are computed by the CUDA-core router kernel.  A handle
+ * computes them with other kernels (a many-CTA decode router with the dot
+ * products cut into slices, or the tensor cores from 512 tokens), which add
+ * the products in other orders: the gates may differ from
+ * colibri_get_routing's in the last bits, and top-k may differ on tokens
+ * whose deciding logits lie within float32 rounding of each other.  Counts
+ * and perm are always the dispatch of the returned topk_idx.  A failure the dispatch detects on the device
  * (an expert id out of range, which the router never writes) sets every
  * counts[e] to -1.
  */

@@ -68,6 +68,8 @@ struct colibri_moe {
     int32_t* tile_info = nullptr;
     int32_t* num_tiles = nullptr;
     int32_t* block_counts = nullptr;  // multi-CTA dispatch: per-CTA counts, then bases
+    float* route_part = nullptr;      // decode routing: partial logits [T][E][slices]
+    unsigned int* route_ticket = nullptr;   // decode routing: CTA arrivals, zero at rest
     int32_t* gu_counter = nullptr;    // split gate/up: arrivals per (m-tile, n-block), zero at rest
     size_t gu_counter_bytes = 0;
     size_t y_floats = 0;              // capacity of Y (also the split gate/up partials)
@@ -141,6 +143,8 @@ constexpr int kSplitMaxPairs = 2048;
 constexpr int kMultiDispatchPairs = 12288;
 // Batches from this many tokens route on the tensor cores.
 constexpr int kTcRouterMinTokens = 512;
+// The decode routing launch gathers the token rows itself up to this many bytes.
+constexpr size_t kRouteGatherBytes = 256 * 1024;
 constexpr int kMaxKSplit = 16;
 // K slices of the tensor-core router at most (the last slice routes the rows).
 constexpr int kMaxRouterSplit = 8;
@@ -333,10 +337,14 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     const bool dec = ex == COLIBRI_EXEC_GROUPED && npairs <= kDecMaxPairsPerExpert * E;
     const bool pair = ex == COLIBRI_EXEC_GROUPED && !dec && npairs >= 128 * E && !h->int8;
     const int tile_rows = dec ? tc_gemm_dec_tile_rows() : pair ? tc_gemm_pair_rows() : tc_gemm_block_m();
-    // Small batch: router, top-k, softmax, dispatch and gather in one CTA.
-    // soft routing (k == E) runs on the CUDA-core router kernel
+    // Decode-sized batch: router, top-k, softmax, dispatch (and the gather of
+    // a small batch) in one launch.  Soft routing (k == E) runs on the
+    // CUDA-core router kernel.
     const bool soft = !r_idx && k == E;
-    const bool fused_routing = !r_idx && !soft && route_small_fits(T, d, E, k);
+    const bool fused_routing = !r_idx && !soft && route_decode_fits(T, d, E, k);
+    // the gather stays in the routing launch while its rows are few: its
+    // last CTA copies them alone
+    const bool gather_in_route = fused_routing && (size_t)npairs * d * h->esz <= kRouteGatherBytes;
     const int cap = h->capacity < 0 ? INT_MAX : h->capacity;
     if (gamma && !fused_routing) {
         Stage g(h, COLIBRI_STAGE_RMSNORM, s);
@@ -354,12 +362,14 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         if (st != COLIBRI_OK) return st;
     } else if (fused_routing) {
         Stage g(h, COLIBRI_STAGE_ROUTER, s);
-        st = g.done(launch_route_small(h->dt, x, h->wr, h->bias, T, d, E, k, h->topk_idx,
-                                       h->topk_w, h->counts, h->offsets, h->perm, h->inv,
-                                       tile_rows, h->tile_expert, h->tile_row, h->tile_info,
-                                       h->num_tiles, h->status, cap, h->kept,
-                                       ex == COLIBRI_EXEC_GROUPED ? h->xp : nullptr, gamma, eps,
-                                       h->u, s, h->int8), 1);
+        st = g.done(launch_route_decode(h->dt, x, h->wr, h->bias, T, d, E, k, h->route_part,
+                                        h->route_ticket, h->topk_idx, h->topk_w, h->counts,
+                                        h->offsets, h->perm, h->inv, tile_rows, h->tile_expert,
+                                        h->tile_row, h->tile_info, h->num_tiles, h->status, cap,
+                                        h->kept,
+                                        ex == COLIBRI_EXEC_GROUPED && gather_in_route ? h->xp
+                                                                                      : nullptr,
+                                        gamma, eps, h->u, s, h->int8), 1);
         if (st != COLIBRI_OK) return st;
         if (gamma) x = h->u;
     } else if (h->grouped_ok && T >= kTcRouterMinTokens && !soft) {
@@ -450,7 +460,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         const int units = pair ? (h->max_resident_pairs > 0 ? h->max_resident_pairs : h->num_sms / 2)
                                : h->num_sms;
         const int cta_per_unit = pair ? 2 : 1;
-        if (!fused_routing) {
+        if (!gather_in_route) {
             // token rows in expert order (the gate/up GEMM's A operand); TMA
             // boxes of 128 consecutive rows read it far faster than per-row
             // gathers inside the GEMM
@@ -731,6 +741,7 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
                  o_off = carve((size_t)(E + 1) * 4), o_perm = carve(P * 4), o_inv = carve(P * 4),
                  o_te = carve((size_t)h->max_tiles * 4), o_tr = carve((size_t)h->max_tiles * 4),
                  o_tinfo = carve((size_t)h->max_tiles * 4), o_nt = carve(4), o_st = carve(4),
+                 o_tk = carve(4), o_rp = carve(route_decode_part_floats(M, E) * 4),
                  o_bc = carve((size_t)dispatch_blocks(h->max_pairs) * E * 4),
                  o_xp = h->grouped_ok ? carve(P * d * h->esz) : 0, o_h = carve(P * f * h->esz),
                  o_y = carve(y_floats * 4), o_guc = carve(gu_counter_bytes),
@@ -751,6 +762,8 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
     h->tile_info = (int32_t*)(b + o_tinfo);
     h->num_tiles = (int32_t*)(b + o_nt);
     h->status = (int*)(b + o_st);
+    h->route_ticket = (unsigned int*)(b + o_tk);
+    h->route_part = (float*)(b + o_rp);
     h->block_counts = (int32_t*)(b + o_bc);
     h->xp = h->grouped_ok ? (void*)(b + o_xp) : nullptr;
     h->H = b + o_h;
@@ -1002,6 +1015,7 @@ colibri_status_t colibri_check(colibri_moe_t* h, void* stream) {
         cudaMemset(h->status, 0, sizeof(int));
         // a launch that gave up may have left split gate/up counters armed
         cudaMemset(h->gu_counter, 0, h->gu_counter_bytes);
+        cudaMemset(h->route_ticket, 0, sizeof(unsigned int));
         if (st == COLIBRI_OK) st = dev_status == DEV_TIMEOUT ? COLIBRI_ERR_TIMEOUT : COLIBRI_ERR_CUDA;
     }
     return st;

@@ -37,16 +37,21 @@ cudaError_t launch_dispatch_multi(const int32_t* topk_idx, int n, int E, int32_t
                                   int32_t* tile_info, int32_t* num_tiles, int* status,
                                   int cap, int32_t* kept, cudaStream_t s);
 
-// Router + top-k + softmax + dispatch (+ gather when xp != null) in one CTA,
-// for batches where route_small_fits().
-bool route_small_fits(int ntok, int d, int E, int k);
-cudaError_t launch_route_small(DType dt, const void* x, const void* wr, const float* bias,
-                               int ntok, int d, int E, int k, int32_t* topk_idx, float* topk_w,
-                               int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
-                               int bm, int32_t* tile_expert, int32_t* tile_row,
-                               int32_t* tile_info, int32_t* num_tiles, int* status, int cap,
-                               int32_t* kept, void* xp, const void* gamma, float eps, void* u,
-                               cudaStream_t s, bool xp_f16 = false);
+// Router + top-k + softmax + dispatch (+ gather when xp != null) in one
+// launch for decode-sized batches (route_decode_fits()): every warp one
+// partial logit (in `part`, route_decode_part_floats() floats), the CTA that
+// draws the last `ticket` (zero at rest) does the rest.  With gamma the
+// routed rows are u = RMSNorm(x) * gamma, written to u.
+bool route_decode_fits(int ntok, int d, int E, int k);
+size_t route_decode_part_floats(int max_tok, int E);
+cudaError_t launch_route_decode(DType dt, const void* x, const void* wr, const float* bias,
+                                int ntok, int d, int E, int k, float* part, unsigned int* ticket,
+                                int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, int32_t* inv, int bm,
+                                int32_t* tile_expert, int32_t* tile_row, int32_t* tile_info,
+                                int32_t* num_tiles, int* status, int cap, int32_t* kept, void* xp,
+                                const void* gamma, float eps, void* u, cudaStream_t s,
+                                bool xp_f16 = false);
 
 // `kept` = pairs each expert accepted (its first kept[e] segment rows).
 cudaError_t launch_ffn_up_stream(DType dt, const void* x, const void* wgu, const int32_t* kept,

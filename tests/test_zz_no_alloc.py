@@ -8,15 +8,17 @@ its intermediate data in a fixed device array inside the library instead of
 allocating.  This test calls it through the C ABI twice in a row, with
 different shapes and token counts so that leftovers of the first call would
 show in the second, and checks each result against the handle-based path
-(colibri_forward + colibri_get_routing on the same weights and tokens).  At
-these batch sizes (below 512 tokens) the two paths run the same router and
-dispatch kernels on the same repacked weights, so the routing must agree bit
-for bit (stricter than the parity tolerances).  Every result is also checked
-against the CPU oracle under the parity rules of the other tests (near-tie
-tokens excepted from the top-k comparison; counts and perm the oracle's
-dispatch of the returned ids, bit for bit), including a batch at the array's
-pair limit that takes the multi-CTA dispatch.  The file sorts last so that a
-run stopping at the first failure has already run every other test.
+(colibri_forward + colibri_get_routing on the same weights and tokens) within
+the tolerances the parity tests use: the two paths compute the logits with
+different kernels (different float32 summation orders), so expert ids must
+agree on every token that is not a near-tie, gates within twice the parity
+gate bound (each side is within one bound of the float64 softmax), and counts
+and perm must agree bit for bit whenever the ids do.  Every result is also
+checked against the CPU oracle under the parity rules of the other tests
+(near-tie tokens excepted from the top-k comparison; counts and perm the
+oracle's dispatch of the returned ids, bit for bit), including a batch at the
+array's pair limit that takes the multi-CTA dispatch.  The file sorts last so
+that a run stopping at the first failure has already run every other test.
 """
 
 from types import SimpleNamespace
@@ -27,7 +29,7 @@ import torch
 
 import oracle
 import synth
-from parity import check_routing
+from parity import GATE_ATOL, NEAR_TIE_REL, check_routing
 
 pytestmark = pytest.mark.gpu
 
@@ -57,8 +59,10 @@ def _check_against_oracle(x, wr, bias, shape, got):
                            off64=None if bias is None else bias.double().cpu().numpy())
     r = {k: v.cpu().numpy() for k, v in got.items()}
     assert int(r["counts"].sum()) == x.shape[0] * shape.top_k   # no failure reported (-1 counts)
-    _, near = check_routing(case, oracle.to_f64(x.cpu()), r)
-    return int(near.sum())
+    x64 = oracle.to_f64(x.cpu())
+    _, near = check_routing(case, x64, r)
+    tau = NEAR_TIE_REL * (np.abs(x64) @ np.abs(case.wr64))
+    return near, tau
 
 
 def test_route_static_matches_handle_path_on_two_calls_in_a_row(lib):
@@ -80,9 +84,17 @@ def test_route_static_matches_handle_path_on_two_calls_in_a_row(lib):
         torch.cuda.synchronize()
         assert layer.check() == sef.OK
         layer.close()
-        for key in ("topk_idx", "topk_w", "counts", "perm"):
-            assert torch.equal(got[key], want[key]), f"{shape.name} T={T}: {key} differs"
-        _check_against_oracle(x, wr, bias, shape, got)
+        near, tau = _check_against_oracle(x, wr, bias, shape, got)
+        g, w = ({k: v.cpu().numpy() for k, v in r.items()} for r in (got, want))
+        same = (g["topk_idx"] == w["topk_idx"]).all(axis=1)
+        assert (same | near).all(), f"{shape.name} T={T}: ids differ off near-ties"
+        tau_sel = np.take_along_axis(tau, g["topk_idx"].astype(np.int64), axis=1).max(axis=1)
+        bound = 2 * (GATE_ATOL + 0.5 * tau_sel)[:, None]
+        assert (np.abs(g["topk_w"] - w["topk_w"])[same] <= bound[same]).all(), \
+            f"{shape.name} T={T}: gates differ beyond the parity bound"
+        if same.all():
+            for key in ("counts", "perm"):
+                assert np.array_equal(g[key], w[key]), f"{shape.name} T={T}: {key} differs"
 
 
 def test_route_static_at_its_pair_limit_matches_oracle(lib):
@@ -97,8 +109,8 @@ def test_route_static_at_its_pair_limit_matches_oracle(lib):
         bias = None if b is None else b.to(dev)
         x = synth.tokens(shape, T, seed, 0, dev)
         got = _routing_through_static_entry(sef, x, wr, bias, shape)
-        n_near = _check_against_oracle(x, wr, bias, shape, got)
-        assert n_near <= max(2, T // 5000)
+        near, _ = _check_against_oracle(x, wr, bias, shape, got)
+        assert near.sum() <= max(2, T // 5000)
 
 
 def test_route_static_rejects_sizes_beyond_its_array(lib):
