@@ -88,6 +88,82 @@ __device__ __forceinline__ float row_inv_rms(const T* __restrict__ hr, int d, fl
     return 1.0f / sqrtf(ss / (float)d + eps);
 }
 
+// Dispatch of n <= 32 pairs by one warp, pair r in lane r: the same counts,
+// offsets, kept counts, stable permutation, inverse and tile list as
+// dispatch_block (whose passes, barriers and per-warp tables cost a few
+// microseconds of latency for a handful of pairs).  `ecnt` and `eoff` are
+// [E] and [E + 1] ints of shared memory; perm goes to `perm_s` (shared).
+__device__ __forceinline__ void dispatch_warp(const int32_t* __restrict__ sidx, int n, int E,
+                                              int32_t* __restrict__ counts,
+                                              int32_t* __restrict__ offsets,
+                                              int32_t* __restrict__ perm_s,
+                                              int32_t* __restrict__ inv, int bm,
+                                              int32_t* __restrict__ tile_expert,
+                                              int32_t* __restrict__ tile_row,
+                                              int32_t* __restrict__ tile_info,
+                                              int32_t* __restrict__ num_tiles,
+                                              int* __restrict__ status, int cap,
+                                              int32_t* __restrict__ kept, int32_t* ecnt,
+                                              int32_t* eoff, int lane) {
+    for (int e = lane; e < E; e += 32) ecnt[e] = 0;
+    __syncwarp();
+    int e = lane < n ? sidx[lane] : -1;
+    if (lane < n && (e < 0 || e >= E)) {
+        atomicExch(status, DEV_BAD_INDEX);
+        e = -1;
+    }
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(m & ((1u << lane) - 1u));      // earlier pairs of the same expert
+    if (e >= 0 && rank == 0) ecnt[e] = __popc(m);
+    __syncwarp();
+    // exclusive scans of the counts and of the tile counts over the experts
+    // in expert order: lane l sums experts [l*per, (l+1)*per), a warp scan
+    // gives each lane its base
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per;
+    int32_t c_sum = 0, t_sum = 0;
+    for (int i = 0; i < per; ++i) {
+        const int x = e0 + i;
+        if (x < E) {
+            c_sum += ecnt[x];
+            t_sum += (min(ecnt[x], cap) + bm - 1) / bm;
+        }
+    }
+    int32_t c_inc = c_sum, t_inc = t_sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t a = __shfl_up_sync(0xffffffffu, c_inc, o);
+        const int32_t b = __shfl_up_sync(0xffffffffu, t_inc, o);
+        if (lane >= o) c_inc += a, t_inc += b;
+    }
+    int32_t acc = c_inc - c_sum, tacc = t_inc - t_sum;
+    for (int i = 0; i < per; ++i) {
+        const int x = e0 + i;
+        if (x < E) {
+            const int c = ecnt[x];
+            eoff[x] = acc;
+            counts[x] = c;
+            kept[x] = min(c, cap);
+            offsets[x] = acc;
+            write_tiles(x, min(c, cap), acc, tacc, bm, tile_expert, tile_row, tile_info);
+            acc += c;
+            tacc += (min(c, cap) + bm - 1) / bm;
+        }
+    }
+    if (lane == 31) {
+        offsets[E] = c_inc;
+        *num_tiles = t_inc;
+    }
+    __syncwarp();
+    if (e >= 0) {
+        const int p = eoff[e] + rank;
+        perm_s[p] = lane;
+        inv[lane] = rank < cap ? p : -1;
+    } else if (lane < n) {
+        inv[lane] = -1;      // an expert id out of range (reported above): adds nothing
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kRouteThreads)
 route_decode_kernel(const T* __restrict__ x, const T* __restrict__ wr,
@@ -173,10 +249,11 @@ route_decode_kernel(const T* __restrict__ x, const T* __restrict__ wr,
         }
         s = warp_sum(s);
         if (lane == 0) part[unit] = s;
+        // the threads that wrote make their writes visible before the ticket
+        if (lane == 0 || (gamma && e == 0)) __threadfence();
     }
 
     // ---- 2. ticket: the last CTA to arrive does the rest
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) last_cta = atomicAdd(ticket, 1u) == gridDim.x - 1;
     __syncthreads();
@@ -202,8 +279,14 @@ route_decode_kernel(const T* __restrict__ x, const T* __restrict__ wr,
         warp_topk_softmax(logit + t * E, E, k, lane, sidx + t * k, topk_w + (size_t)t * k);
     __syncthreads();
     for (int i = threadIdx.x; i < npairs; i += blockDim.x) topk_idx[i] = sidx[i];
-    dispatch_block(sidx, npairs, E, counts, offsets, sperm, inv, bm, tile_expert, tile_row,
-                   tile_info, num_tiles, status, cap, kept, dsh);
+    if (npairs <= 32) {
+        if (warp == 0)
+            dispatch_warp(sidx, npairs, E, counts, offsets, sperm, inv, bm, tile_expert, tile_row,
+                          tile_info, num_tiles, status, cap, kept, dsh, dsh + E, lane);
+    } else {
+        dispatch_block(sidx, npairs, E, counts, offsets, sperm, inv, bm, tile_expert, tile_row,
+                       tile_info, num_tiles, status, cap, kept, dsh);
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < npairs; i += blockDim.x) perm[i] = sperm[i];
     if (xp) {
