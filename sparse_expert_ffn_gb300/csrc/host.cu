@@ -144,7 +144,7 @@ constexpr int kMultiDispatchPairs = 12288;
 // Batches from this many tokens route on the tensor cores.
 constexpr int kTcRouterMinTokens = 512;
 // The decode routing launch gathers the token rows itself up to this many bytes.
-constexpr size_t kRouteGatherBytes = 256 * 1024;
+constexpr size_t kRouteGatherBytes = 128 * 1024;
 constexpr int kMaxKSplit = 16;
 // K slices of the tensor-core router at most (the last slice routes the rows).
 constexpr int kMaxRouterSplit = 8;
