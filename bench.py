@@ -66,6 +66,9 @@ def parse_args(argv=None):
     ap.add_argument("--weights", choices=["bf16", "int8"], default="bf16",
                     help="expert weight format: bf16, or int8 64x64 blocks (converted on the host, "
                          "dequantised to f16 by converter warps of the tensor-core GEMMs)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="stack workload: layers per step (default 32, the decode stack; fewer "
+                         "only for small profiler captures)")
     ap.add_argument("--no-sweep", action="store_true", help="skip the decode-size sweep")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the block of the other workloads (Qwen2- and DeepSeek-shaped "
@@ -474,13 +477,13 @@ def measure_layer(sef, shape, T, weights, seed, dev, stream, pk, steps, warmup, 
         layer.close()
 
 
-def build_stack(sef, B, seed, dev, weights="bf16"):
+def build_stack(sef, B, seed, dev, weights="bf16", n_layers=None):
     import torch
 
     import synth
     shape = synth.MIXTRAL
     layers = []
-    for l in range(synth.STACK_LAYERS):
+    for l in range(n_layers or synth.STACK_LAYERS):
         wr = synth.router_weight(shape, seed, l, dev)
         wg, wu, wd = synth.expert_weights(shape, seed, l, dev)
         layers.append(make_layer(sef, shape, wr, wg, wu, wd, weights, max_tokens=max(B, 1)))
@@ -554,7 +557,7 @@ def measure_stack(sef, layers, B, seed, dev, stream, pk, steps, warmup, clocks, 
             alg[key_] += a_l[key_]
         assert layer.check() == 0
     # RMSNorm reads and writes the hidden state once more per layer
-    alg["bytes"] += synth.STACK_LAYERS * (2 * B * shape.d_model * 2 + shape.d_model * 2)
+    alg["bytes"] += len(layers) * (2 * B * shape.d_model * 2 + shape.d_model * 2)
     step_s = ms / k / 1e3
     per_step = dict(alg)
     for key_ in ("up_flops", "down_flops", "up_bytes", "down_bytes", "bytes", "flops"):
@@ -573,7 +576,7 @@ def measure_stack(sef, layers, B, seed, dev, stream, pk, steps, warmup, clocks, 
              "stages_us_per_step": {s_: round(v["ms_total"] * 1e3 / kp, 1) for s_, v in stages.items()},
              "ms_per_step_profiled": round(ms_prof / kp, 4),
              "clocks": clocks.summary(tag + "_start", tag + "_end") if clocks else None,
-             "l2": "inputs larger than L2 (90 GB of weights)"}
+             "l2": f"inputs larger than L2 ({sum(l.bytes[0] for l in layers) / 1e9:.0f} GB of weights)"}
     return entry, int(launches), k, h0
 
 
@@ -786,7 +789,7 @@ def run_stack(args):
     seed = rank_seed(args.seed, rank)
     clocks = ClockSampler(gpu_id_of(dev)) if rank == 0 else None
     stream = torch.cuda.current_stream()
-    layers = build_stack(sef, B, seed, dev, args.weights)
+    layers = build_stack(sef, B, seed, dev, args.weights, args.layers)
     entry, launches, k, h0 = measure_stack(sef, layers, B, seed, dev, stream, pk, args.steps,
                                            args.warmup, clocks, "timed", world, args.weights,
                                            exact=True)
@@ -835,7 +838,7 @@ def run_stack(args):
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{WORKLOADS['stack'][2]}, batch {B}" + (", int8 expert weights" if args.weights == "int8" else ""),
-                   "weights": args.weights, "layers": synth.STACK_LAYERS,
+                   "weights": args.weights, "layers": args.layers or synth.STACK_LAYERS,
                    "batch": B, "parallelism": f"token-parallel x{world}",
                    "l2": entry["l2"]},
         "roofline": entry["roofline"],
