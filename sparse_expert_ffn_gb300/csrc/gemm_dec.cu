@@ -201,7 +201,12 @@ grouped_gemm_dec(const __grid_constant__ CUtensorMap tmTok, const __grid_constan
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = kI8 ? idesc_f16(kDecM, kDecN) : idesc_bf16(kDecM, kDecN);
+            // N = 16 for tiles of at most 16 tokens: every MMA reads and
+            // rewrites its accumulator in tensor memory, and half the
+            // columns halve that traffic (the epilogue uses only the live
+            // token columns)
+            const uint32_t idesc32 = kI8 ? idesc_f16(kDecM, kDecN) : idesc_bf16(kDecM, kDecN);
+            const uint32_t idesc16 = kI8 ? idesc_f16(kDecM, 16) : idesc_bf16(kDecM, 16);
             int stage = 0, as = 0, acc = 0;     // int8: `stage` counts token stages
             uint32_t phase = 0, aphase = 0, acc_phase = 0;
             for (int w = unit; w < total && !*abort_flag; w += n_units) {
@@ -214,6 +219,7 @@ grouped_gemm_dec(const __grid_constant__ CUtensorMap tmTok, const __grid_constan
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kDecAccCols;
+                const uint32_t idesc = wk.rows <= 16 ? idesc16 : idesc32;
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     const bool got =
