@@ -88,11 +88,17 @@ __device__ __forceinline__ float row_inv_rms(const T* __restrict__ hr, int d, fl
     return 1.0f / sqrtf(ss / (float)d + eps);
 }
 
-// Dispatch of n <= 32 pairs by one warp, pair r in lane r: the same counts,
-// offsets, kept counts, stable permutation, inverse and tile list as
-// dispatch_block (whose passes, barriers and per-warp tables cost a few
-// microseconds of latency for a handful of pairs).  `ecnt` and `eoff` are
-// [E] and [E + 1] ints of shared memory; perm goes to `perm_s` (shared).
+// Dispatch of n <= 32 * kWarpDispatchChunks pairs by one warp, pair r in
+// lane r % 32 of chunk r / 32: the same counts, offsets, kept counts, stable
+// permutation, inverse and tile list as dispatch_block (whose passes,
+// barriers and per-warp tables cost microseconds of latency for a few
+// hundred pairs).  Chunks are walked in order twice: once counting, once
+// placing each pair after the earlier pairs of its expert (earlier chunks
+// through `run`, earlier lanes of its chunk by a warp match).  `ecnt`, `run`
+// and `eoff` are [E], [E] and [E + 1] ints of shared memory; perm goes to
+// `perm_s` (shared).
+constexpr int kWarpDispatchChunks = 8;
+
 __device__ __forceinline__ void dispatch_warp(const int32_t* __restrict__ sidx, int n, int E,
                                               int32_t* __restrict__ counts,
                                               int32_t* __restrict__ offsets,
@@ -104,18 +110,22 @@ __device__ __forceinline__ void dispatch_warp(const int32_t* __restrict__ sidx, 
                                               int32_t* __restrict__ num_tiles,
                                               int* __restrict__ status, int cap,
                                               int32_t* __restrict__ kept, int32_t* ecnt,
-                                              int32_t* eoff, int lane) {
-    for (int e = lane; e < E; e += 32) ecnt[e] = 0;
+                                              int32_t* run, int32_t* eoff, int lane) {
+    for (int e = lane; e < E; e += 32) ecnt[e] = 0, run[e] = 0;
     __syncwarp();
-    int e = lane < n ? sidx[lane] : -1;
-    if (lane < n && (e < 0 || e >= E)) {
-        atomicExch(status, DEV_BAD_INDEX);
-        e = -1;
+    const unsigned lt = (1u << lane) - 1u;
+    // pass 1: counts
+    for (int r0 = 0; r0 < n; r0 += 32) {
+        const int r = r0 + lane;
+        int e = r < n ? sidx[r] : -1;
+        if (r < n && (e < 0 || e >= E)) {
+            atomicExch(status, DEV_BAD_INDEX);
+            e = -1;
+        }
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && __popc(m & lt) == 0) ecnt[e] += __popc(m);
+        __syncwarp();
     }
-    const unsigned m = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(m & ((1u << lane) - 1u));      // earlier pairs of the same expert
-    if (e >= 0 && rank == 0) ecnt[e] = __popc(m);
-    __syncwarp();
     // exclusive scans of the counts and of the tile counts over the experts
     // in expert order: lane l sums experts [l*per, (l+1)*per), a warp scan
     // gives each lane its base
@@ -155,12 +165,25 @@ __device__ __forceinline__ void dispatch_warp(const int32_t* __restrict__ sidx, 
         *num_tiles = t_inc;
     }
     __syncwarp();
-    if (e >= 0) {
-        const int p = eoff[e] + rank;
-        perm_s[p] = lane;
-        inv[lane] = rank < cap ? p : -1;
-    } else if (lane < n) {
-        inv[lane] = -1;      // an expert id out of range (reported above): adds nothing
+    // pass 2: positions, chunk by chunk in pair order
+    for (int r0 = 0; r0 < n; r0 += 32) {
+        const int r = r0 + lane;
+        int e = r < n ? sidx[r] : -1;
+        if (e >= E) e = -1;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        const int before = __popc(m & lt);                  // earlier lanes, same expert
+        int rank = 0;
+        if (e >= 0) rank = run[e] + before;                 // within the expert's segment
+        __syncwarp();
+        if (e >= 0) {
+            const int p = eoff[e] + rank;
+            perm_s[p] = r;
+            inv[r] = rank < cap ? p : -1;
+            if (before == 0) run[e] += __popc(m);
+        } else if (r < n) {
+            inv[r] = -1;      // an expert id out of range (reported above): adds nothing
+        }
+        __syncwarp();
     }
 }
 
@@ -279,10 +302,11 @@ route_decode_kernel(const T* __restrict__ x, const T* __restrict__ wr,
         warp_topk_softmax(logit + t * E, E, k, lane, sidx + t * k, topk_w + (size_t)t * k);
     __syncthreads();
     for (int i = threadIdx.x; i < npairs; i += blockDim.x) topk_idx[i] = sidx[i];
-    if (npairs <= 32) {
+    if (npairs <= 32 * kWarpDispatchChunks) {
         if (warp == 0)
             dispatch_warp(sidx, npairs, E, counts, offsets, sperm, inv, bm, tile_expert, tile_row,
-                          tile_info, num_tiles, status, cap, kept, dsh, dsh + E, lane);
+                          tile_info, num_tiles, status, cap, kept, dsh, dsh + E, dsh + 2 * E,
+                          lane);
     } else {
         dispatch_block(sidx, npairs, E, counts, offsets, sperm, inv, bm, tile_expert, tile_row,
                        tile_info, num_tiles, status, cap, kept, dsh);
