@@ -712,7 +712,7 @@ def run_ours(args):
         workloads = {}
         wsteps, wwarm = max(3, min(args.steps, 10)), max(3, min(args.warmup, 5))
         plan = [("qwen2_moe", synth.QWEN2, 1, "bf16"), ("qwen2_moe", synth.QWEN2, 64, "bf16"),
-                ("qwen2_moe", synth.QWEN2, 8192, "bf16"),
+                ("qwen2_moe", synth.QWEN2, 2048, "bf16"), ("qwen2_moe", synth.QWEN2, 8192, "bf16"),
                 ("deepseek_moe", synth.DEEPSEEK, 16384, "bf16"),
                 ("deepseek_moe_masked", synth.DEEPSEEK_MASKED, 16384, "bf16"),
                 ("mixtral", synth.MIXTRAL, 1, "int8"), ("mixtral", synth.MIXTRAL, 4096, "int8")]

@@ -391,13 +391,18 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         a.status = h->status;
         a.wait_limit_ns = h->wait_limit_ns;
         a.stall_producer = h->stall_tma ? 1 : 0;
-        // At most a quarter as many 128-token tiles as SMs: split K (float32
-        // partial logits in Y, one arrival counter per tile and lane quarter
-        // in gu_counter).  With fewer slices the fixup's latency (fence,
-        // counter, reloading the partials) costs more than the shorter K loop
-        // saves (measured: E = 64, 2 slices, 28 -> 35 us).
+        // At most a quarter as many 128-token tiles as SMs, and logit rows of
+        // at most 16 columns: split K (float32 partial logits in Y, one
+        // arrival counter per tile and lane quarter in gu_counter).  With
+        // fewer slices the fixup's latency (fence, counter, reloading the
+        // partials) costs more than the shorter K loop saves (E = 64, 2
+        // slices: 28 -> 35 us); with wider rows the fixup reloads every
+        // slice of every 32-logit chunk (measured, 128-token tiles: 8 experts
+        // at T = 4096, 27.1 us whole, 21.4 us in 4 slices; 64 experts at
+        // T = 2048, 22.7 us whole, 42.5 us in 8 slices; 128 experts at
+        // T = 2048, 29.8 us whole, 75.8 us in 8 slices).
         const int tiles = (T + tc_gemm_block_m() - 1) / tc_gemm_block_m();
-        if (4 * tiles <= h->num_sms) {
+        if (4 * tiles <= h->num_sms && h->e_pad <= 16) {
             const int fit = (int)std::min<size_t>(kMaxRouterSplit, h->y_floats / ((size_t)T * h->e_pad));
             a.k_splits = choose_k_splits(tiles, a.k_blocks, h->num_sms, fit);
             a.partial = h->Y;
