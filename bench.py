@@ -137,6 +137,8 @@ KERNEL_SOURCES = {
     "grouped_gemm_tc<kDown>": _TC,
     "grouped_gemm_dec<kGateUp>": _DEC,
     "grouped_gemm_dec<kDown>": _DEC,
+    "ffn_gemv_i8<up>": ("sparse_expert_ffn_gb300/csrc/gemv_i8.cu", "sparse_expert_ffn_gb300/csrc/tc_common.cuh"),
+    "ffn_gemv_i8<down>": ("sparse_expert_ffn_gb300/csrc/gemv_i8.cu", "sparse_expert_ffn_gb300/csrc/tc_common.cuh"),
     "ffn_up_stream": ("sparse_expert_ffn_gb300/csrc/ffn_stream.cu", "sparse_expert_ffn_gb300/csrc/common.cuh"),
     "ffn_down_stream": ("sparse_expert_ffn_gb300/csrc/ffn_stream.cu", "sparse_expert_ffn_gb300/csrc/common.cuh"),
 }
@@ -345,6 +347,13 @@ def kernel_name(stage, shape, T, weights):
     """The library kernel behind a profiled stage of a layer call."""
     grouped = shape.dtype == "bf16" and shape.d_model % 256 == 0
     i8 = "_i8" if weights == "int8" else ""
+    # int8 codes for at most three tokens: the CUDA-core GEMV, when its
+    # gate/up stage has an item (64 hidden units of one expert) per SM
+    import torch
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    if (weights == "int8" and grouped and T <= 3 and shape.top_k * shape.d_ff // 64 >= n_sms
+            and stage in ("expert_up", "expert_down")):
+        return "ffn_gemv_i8<up>" if stage == "expert_up" else "ffn_gemv_i8<down>"
     # decode-sized batches (at most 16 pairs per expert on average) run the
     # GEMMs with the weights as the MMA's M operand
     gk = "grouped_gemm_dec" if T * shape.top_k <= 16 * shape.n_experts else "grouped_gemm_tc"

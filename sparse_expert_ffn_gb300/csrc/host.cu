@@ -153,6 +153,34 @@ constexpr int kMaxRouterSplit = 8;
 constexpr int kDecMaxPairsPerExpert = 16;
 // The gate/up GEMM splits K only for batches of at most this many pairs.
 constexpr int kGateUpSplitMaxPairs = 64;
+// Int8 weights: batches of at most this many tokens stream the codes on the
+// CUDA cores (gemv_i8.cu) when the gate/up stage has at least one 64-unit
+// item per SM; the tensor-core decode GEMMs take one MMA per 2 KB of codes
+// whatever the token count, about 0.7 of HBM at best.  Measured, Mixtral-
+// shaped layer, one forward with L2 flushed (tensor cores / CUDA cores):
+// T = 1 131 / 94 us, 2 213 / 168, 3 231 / 227, 4 299 / 327, 8 399 / 721.
+constexpr int kGemvMaxTokens = 3;
+// Resident CTAs per SM the CUDA-core int8 items are sized for.
+constexpr int kGemvCtasPerSm = 8;
+
+// K slices of the CUDA-core int8 down projection: `units` (tile, 64-row
+// group) items of nkb k-tiles; the count whose busiest SM (items spread
+// evenly, every item resident) streams the fewest k-tiles, three k-tiles of
+// fixed cost per item, and fewer than three items per SM penalised in
+// proportion (too few loads in flight to cover HBM latency).
+int choose_gemv_slices(int64_t units, int nkb, int num_sms, int max_ks) {
+    int best = 1;
+    double best_cost = 0.0;
+    for (int ks = 1; ks <= std::max(1, std::min({max_ks, nkb, 16})); ++ks) {
+        const int64_t u = units * ks;
+        if (ks > 1 && u > (int64_t)num_sms * kGemvCtasPerSm) break;
+        const int64_t per_sm = (u + num_sms - 1) / num_sms;
+        double cost = (double)per_sm * ((nkb + ks - 1) / ks + 3);
+        if (u < 3 * (int64_t)num_sms) cost *= 3.0 * num_sms / (double)u;
+        if (ks == 1 || cost < best_cost) best = ks, best_cost = cost;
+    }
+    return best;
+}
 
 // K slices of a GEMM with `items` (m-tile, n-block) work items of kb K blocks
 // each, on `units` resident work units: the count (every slice non-empty)
@@ -272,13 +300,27 @@ colibri_status_t pack(int esz, const void* src, bool src_on_device, void* dst, i
     return COLIBRI_OK;
 }
 
+// The CUDA-core int8 GEMV can run this batch: int8 codes, bf16 activations,
+// at most kGemvMaxTokens tokens, and its staging fits (Y holds at least 8 K
+// slices of a batch this small).
+bool gemv_i8_usable(const colibri_moe_t* h, int T) {
+    const auto& c = h->cfg;
+    return h->int8 && h->dt == DType::BF16 && T >= 1 && T <= kGemvMaxTokens &&
+           gemv_i8_fits(gemv_i8_slots(T), c.d_model, c.d_ff, 8);
+}
+
 int choose_executor(const colibri_moe_t* h, int T) {
     if (h->cfg.executor != COLIBRI_EXEC_AUTO) return h->cfg.executor;
     // bf16: the TMA-fed grouped GEMM streams the active experts' weights
     // faster than the CUDA-core kernels at every batch size measured (one
     // token included, with split-K on the down projection); CUDA cores run
-    // the float32 layer and shapes the tensor-core path does not take.
-    (void)T;
+    // the float32 layer, shapes the tensor-core path does not take, and
+    // int8 codes for a few tokens per expert.
+    // (with at least one gate/up item per SM even when the tokens share
+    // their experts)
+    if (gemv_i8_usable(h, T) &&
+        gemv_i8_items(true, h->cfg.top_k, h->cfg.d_model, h->cfg.d_ff, 1) >= h->num_sms)
+        return COLIBRI_EXEC_STREAM;
     return h->grouped_ok ? COLIBRI_EXEC_GROUPED : COLIBRI_EXEC_STREAM;
 }
 
@@ -438,7 +480,36 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
     int nsplit = 1;
     size_t split_stride = 0;
     bool y_bf16 = false;     // Y rows stored as bf16 by the down GEMM
-    if (ex == COLIBRI_EXEC_STREAM) {
+    if (ex == COLIBRI_EXEC_STREAM && gemv_i8_usable(h, T)) {
+        // a few tokens per expert: items of 64 weight rows, every item's
+        // codes read once per pass of S token rows
+        const int S = gemv_i8_slots(T);
+        const GemvTiles tl{h->tile_expert, h->tile_row, h->tile_info, h->num_tiles, E, h->status,
+                           h->wait_limit_ns};
+        const int tiles_est = std::min(E, npairs);
+        const int max_ks = (int)std::min<size_t>(kMaxKSplit, h->y_floats / ((size_t)npairs * d));
+        int ks = choose_gemv_slices((int64_t)tiles_est * (d / 64), f / 64, h->num_sms, max_ks);
+        while (ks < max_ks && !gemv_i8_fits(S, d, f, ks)) ++ks;   // shorter slices stage less
+        const int cap_grid = h->num_sms * kGemvCtasPerSm;
+        {
+            Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
+            const int grid = std::min(gemv_i8_items(true, tiles_est, d, f, 1), cap_grid);
+            st = g.done(launch_ffn_up_gemv_i8(S, x, h->perm, k, h->q_gu, h->sc_gu,
+                                              h->zp_gu, tl, d, f, grid, h->H, s),
+                        1);
+            if (st != COLIBRI_OK) return st;
+        }
+        {
+            Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
+            const int grid = std::min(gemv_i8_items(false, tiles_est, d, f, ks), cap_grid);
+            st = g.done(launch_ffn_down_gemv_i8(S, h->H, h->q_d, h->sc_d, h->zp_d, tl, d,
+                                                f, ks, grid, h->Y, (size_t)npairs * d, s),
+                        1);
+            if (st != COLIBRI_OK) return st;
+        }
+        nsplit = ks;
+        split_stride = (size_t)npairs * d;
+    } else if (ex == COLIBRI_EXEC_STREAM) {
         {
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
             st = g.done(h->int8 ? launch_ffn_up_stream_i8(h->dt, x, h->q_gu, h->sc_gu, h->zp_gu,

@@ -71,6 +71,34 @@ cudaError_t launch_ffn_down_stream_i8(DType dt, const void* H, const int8_t* wq,
                                       const int32_t* offsets, int d, int f, int E, float* Y,
                                       cudaStream_t s);
 
+// Int8-weight expert FFN for a few tokens per expert on CUDA cores, bf16
+// layers (gemv_i8.cu): items of 64 weight rows x one K slice per CTA over the
+// dispatch's tile list, codes streamed by bulk copies into a shared-memory
+// ring, activations as 16-bit integers per 64-wide k-tile, integer dot
+// products; S token rows per pass (1, 2 or 4; more rows take several passes).
+// gemv_i8_fits: the ring and the staging area of S rows of one item fit.
+struct GemvTiles {
+    const int32_t* tile_expert;
+    const int32_t* tile_row;
+    const int32_t* tile_info;
+    const int32_t* num_tiles;
+    int E;                    // experts: tile_expert values are checked against it
+    int* status;              // DEV_TIMEOUT when a wait gave up, DEV_BAD_INDEX on a bad expert
+    uint64_t wait_limit_ns;   // bound of every wait
+};
+int gemv_i8_slots(int max_rows_per_expert);
+bool gemv_i8_fits(int S, int d, int f, int ks);
+int gemv_i8_items(bool up, int tiles, int d, int f, int ks);
+// H[p, n] = silu(g) * u as bf16, x the bf16 token rows (pair p: row perm[p] / k).
+cudaError_t launch_ffn_up_gemv_i8(int S, const void* x, const int32_t* perm, int k,
+                                  const int8_t* wq, const float* sc, const int32_t* zp,
+                                  const GemvTiles& t, int d, int f, int grid, void* H,
+                                  cudaStream_t s);
+// Y + s * y_split_stride: the float32 partial of K slice s, [pairs][d].
+cudaError_t launch_ffn_down_gemv_i8(int S, const void* H, const int8_t* wq, const float* sc,
+                                    const int32_t* zp, const GemvTiles& t, int d, int f, int ks,
+                                    int grid, float* Y, size_t y_split_stride, cudaStream_t s);
+
 // xp[p] = x[perm[p] / k] for p < npairs; a perm value outside [0, src_pairs)
 // gathers a zero row.
 cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, int k, int d,

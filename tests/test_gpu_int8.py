@@ -32,11 +32,13 @@ def mixtral8(lib):
     c.close()
 
 
-@pytest.mark.parametrize("T", [1, 8, 16, 128])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 8, 16, 128])
 @pytest.mark.parametrize("executor", ["grouped", "stream"])
 def test_mixtral_int8_decode(mixtral8, T, executor):
     """grouped: TMA-fed int8 stages dequantised in shared memory for tcgen05
-    (split-K with the last-slice fixup at these sizes); stream: CUDA cores."""
+    (split-K with the last-slice fixup at these sizes); stream: CUDA cores
+    (up to three tokens the int8 GEMV items: one, two or four token rows per
+    pass, down projection in K slices; above, the per-row weight stream)."""
     x, x64 = mixtral8.tokens(T)
     y, r = mixtral8.run(x, executor)
     l, _ = check_routing(mixtral8, x64, r)
@@ -74,3 +76,17 @@ def test_qwen_int8_zipf_with_capacity():
         check_output(c, x64, y, r, l, capacity=3)
     finally:
         c.close()
+
+
+def test_mixtral_int8_gemv_with_capacity(mixtral8):
+    """Three tokens, every expert keeping one pair: the GEMV's tiles hold only
+    the kept rows; dropped pairs add nothing in the combine."""
+    x, x64 = mixtral8.tokens(3)
+    y, r = mixtral8.run(x, "stream")
+    l, _ = check_routing(mixtral8, x64, r)
+    try:
+        mixtral8.layer.set_capacity(1)
+        y, r = mixtral8.run(x, "stream")
+        check_output(mixtral8, x64, y, r, l, capacity=1)
+    finally:
+        mixtral8.layer.set_capacity(None)
