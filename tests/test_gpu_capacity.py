@@ -57,13 +57,16 @@ def test_qwen_zipf_capacity_drops_the_hot_experts_overflow(lib, T, C):
         c.close()
 
 
-def test_deepseek_capacity_multi_cta_dispatch_and_pairs(lib):
+@pytest.mark.parametrize("C", [400, 280])
+def test_deepseek_capacity_multi_cta_dispatch_and_pairs(lib, C):
+    """C = 400: every capped expert's kept rows end 144 rows into its second
+    256-row pair tile; C = 280: 24 rows into it (a tile almost all padding)."""
     c = Case(synth.DEEPSEEK, seed=0, max_tokens=16384)
     try:
         x, x64 = c.tokens(16384)
-        y, r, keep, _ = _run_capped(c, x, x64, 400, "grouped")
-        assert (r["counts"] > 400).any() and (~keep).any()
-        y2, _, _, _ = _run_capped(c, x, x64, 400, "grouped", [0, 1])
+        y, r, keep, _ = _run_capped(c, x, x64, C, "grouped")
+        assert (r["counts"] > C).any() and (~keep).any()
+        y2, _, _, _ = _run_capped(c, x, x64, C, "grouped", [0, 1])
         assert torch.equal(y, y2)                  # deterministic under capacity too
     finally:
         c.close()
