@@ -254,11 +254,16 @@ __device__ __noinline__ void router_split_fixup(const TcGemmArgs& args, const Wo
     if (lane == 0) *ctr = 0;
 }
 
-template <int kMode, bool kPair, bool kI8>
+// Weights as M (kWM): token columns of a tile, its valid rows rounded up to
+// 32 (each CTA of the pair holds half of them as MMA B rows).
+__device__ __forceinline__ int wm_cols(int rows) { return min(2 * kBM, max(32, (rows + 31) & ~31)); }
+
+template <int kMode, bool kPair, bool kI8, bool kWM>
 __global__ void __launch_bounds__(kI8 ? kThreadsI8 : kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 TcGemmArgs args) {
     static_assert(!kI8 || (!kPair && kMode != kRouter), "int8 B: single-CTA expert GEMMs only");
+    static_assert(!kWM || (kPair && !kI8 && kMode != kRouter), "weights as M: CTA-pair expert GEMMs");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -289,6 +294,11 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t* a_empty = bars + 2 * kStages + 12;   // [kAStagesI8] kI8: A consumed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 15);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // kWM gate/up: per pair of epilogue warps (q, q + 2), "staged" and "read"
+    // barriers of the gate/up exchange, two arrivals each
+    uint64_t* xchg = bars + 32;   // [2 pairs][staged, read]
+    static_assert(!kWM || (2 * kMaxSt + 17 <= 32 && 36 * 8 <= 512),
+                  "exchange barriers after the others, inside the 512 bytes after the ring");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // CTA pair: rank 0 (leader) owns the full / acc_empty barriers and issues
@@ -319,6 +329,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(smem_u32(&acc_empty[a]), kPair ? 8 : 4);
         }
         mbar_init(smem_u32(&mma_done[0]), 1);
+        if constexpr (kWM && kMode == kGateUp)
+            for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xchg[i]), 2);
         if constexpr (kI8) {
             for (int b = 0; b < kBStages; ++b) {
                 mbar_init(smem_u32(&bf_full[b]), kConvWarps);
@@ -371,7 +383,27 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if (leader) mbar_expect_tx(fb_local, stage_tx);
                     const uint32_t sa = smem_u32(stage_a + stage * kStageA);
                     const uint32_t sb = smem_u32(stage_b + stage * kStageB);
-                    if constexpr (kPair) {
+                    if constexpr (kWM) {
+                        // A: this CTA's 128 weight rows; B: its half of the
+                        // tile's token columns (a 128-row box, of which the
+                        // MMA reads the first wm_cols / 2)
+                        const uint32_t fb = map_to_rank(fb_local, 0);
+                        tma_load_2d_pair(sb, &tmB, kb * kBK,
+                                         wk.row0 + (int)rank * (wm_cols(wk.rows) / 2), fb);
+                        if constexpr (kMode == kGateUp) {
+                            // 64 hidden units per CTA: their gate rows (TMEM
+                            // lanes 0-63) and up rows (lanes 64-127)
+                            const int f = args.b_rows_per_expert / 2;
+                            const int base = ((wk.expert * (f / 128) + wk.nblk) * 2) * 128 + (int)rank * 64;
+                            tma_load_2d_pair(sa, &tmA, kb * kBK, base, fb);
+                            tma_load_2d_pair(sa + 64 * 128, &tmA, kb * kBK, base + 128, fb);
+                        } else {
+                            tma_load_2d_pair(sa, &tmA, kb * kBK,
+                                             wk.expert * args.b_rows_per_expert + wk.nblk * kBN +
+                                                 (int)rank * kBM,
+                                             fb);
+                        }
+                    } else if constexpr (kPair) {
                         // both halves complete on the leader's barrier
                         const uint32_t fb = map_to_rank(fb_local, 0);
                         tma_load_2d_pair(sa, &tmA, kb * kBK, a_row, fb);
@@ -423,6 +455,8 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
+                // weights as M: N is the tile's token count rounded up to 32
+                const uint32_t idesc_w = kWM ? idesc_bf16(2 * kBM, wm_cols(wk.rows)) : idesc;
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     // kI8: A from its own ring (`stage` counts A stages), B
@@ -445,7 +479,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                     for (int ks = 0; ks < kBK / 16; ++ks)
                         // +32 bytes of K per step inside the swizzle atom (encoded >> 4)
-                        mma_bf16<kPair>(d_tmem, da + 2 * ks, db + 2 * ks, idesc,
+                        mma_bf16<kPair>(d_tmem, da + 2 * ks, db + 2 * ks, idesc_w,
                                         (kb > kb0) || ks != 0);
                     if constexpr (kI8) {
                         mma_commit<kPair>(smem_u32(&a_empty[stage]));
@@ -484,6 +518,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             kPair ? map_to_rank(smem_u32(&acc_empty[0]), 0) : smem_u32(&acc_empty[0]);
         int acc = 0;
         uint32_t acc_phase = 0;
+        uint32_t xphase = 0;   // kWM gate/up: phase of the pair's exchange barriers
         for (int w = unit; w < total; w += n_units) {
             const Work wk = get_work<kMode>(w, args);
             const bool got =
@@ -496,7 +531,97 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const bool live = my_row < wk.rows;
             const size_t orow = (size_t)(wk.row0 + my_row);
             float* stg = reinterpret_cast<float*>(smem + kStagingOffset) + (warp - 2) * 32 * kStgStride;
-            if constexpr (kMode == kRouter) {
+            if constexpr (kWM) {
+                // TMEM lane = weight row of this CTA, column = token of the tile
+                const int ncol = wm_cols(wk.rows);
+                if constexpr (kMode == kGateUp) {
+                    // Warp q < 2 holds the gate rows and warp q + 2 the up
+                    // rows of the same 32 hidden units (lane = unit).  Per
+                    // 32-token chunk each stages its values in shared memory,
+                    // the pair meets at a named barrier, and the gate warp
+                    // forms H for the chunk's first 16 tokens, the up warp
+                    // for the last 16 (a store: 32 consecutive units of a token).
+                    uint16_t* H = reinterpret_cast<uint16_t*>(args.out);
+                    const int unit = wk.nblk * kBM + (int)rank * 64 + (q & 1) * 32 + lane;
+                    const bool up = q >= 2;
+                    // staging slots go by warp - 2 = q ^ 2, so the partner
+                    // (lane quarter q ^ 2) stages in slot q
+                    float* partner = reinterpret_cast<float*>(smem + kStagingOffset) + q * 32 * kStgStride;
+                    // the pair's barriers: every wait bounded, so that a warp
+                    // whose partner gave up gives up too
+                    const uint32_t x_staged = smem_u32(&xchg[2 * (q & 1)]);
+                    const uint32_t x_read = smem_u32(&xchg[2 * (q & 1) + 1]);
+                    auto pair_sync = [&](uint32_t bar) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar);
+                        const bool ok = mbar_wait(bar, xphase, abort_flag, args.status, limit);
+                        return __all_sync(0xffffffffu, ok);
+                    };
+                    bool xok = true;
+#pragma unroll 1
+                    for (int c = 0; c < ncol; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tbase + c, v);
+                        tmem_ld_wait();
+                        float4* mine = reinterpret_cast<float4*>(stg + lane * kStgStride);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            mine[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                        if (!(xok = pair_sync(x_staged))) break;
+                        const float4* other =
+                            reinterpret_cast<const float4*>(partner + lane * kStgStride) + (up ? 4 : 0);
+                        const int t0 = c + (up ? 16 : 0);
+#pragma unroll
+                        for (int i4 = 0; i4 < 4; ++i4) {
+                            const float4 o = other[i4];
+                            const float ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const int i = 4 * i4 + j;
+                                const float own = __uint_as_float(up ? v[16 + i] : v[i]);
+                                const float g = up ? ov[j] : own, u = up ? own : ov[j];
+                                if (t0 + i < wk.rows) {
+                                    // fast exp and divide (|rel err| ~1e-6, far below the
+                                    // bf16 rounding of H): this epilogue is
+                                    // instruction-bound at small K
+                                    const float sg = __fdividef(g, 1.0f + __expf(-g));
+                                    const __nv_bfloat16 hb = __float2bfloat16_rn(sg * u);
+                                    H[(size_t)(wk.row0 + t0 + i) * args.out_ld + unit] =
+                                        *reinterpret_cast<const uint16_t*>(&hb);
+                                }
+                            }
+                        }
+                        // both done reading before the next chunk is staged
+                        if (!(xok = pair_sync(x_read))) break;
+                        xphase ^= 1;
+                    }
+                    if (!xok) break;
+                } else {
+                    const int feat = wk.nblk * kBN + (int)rank * kBM + q * 32 + lane;
+                    float* Y = reinterpret_cast<float*>(args.out) + wk.split * args.out_split_stride;
+                    uint16_t* Yb = reinterpret_cast<uint16_t*>(args.out);
+#pragma unroll 1
+                    for (int c = 0; c < ncol; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tbase + c, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int t = c + i;
+                            if (t < wk.rows) {
+                                const size_t o = (size_t)(wk.row0 + t) * args.out_ld + feat;
+                                if (args.y_bf16) {
+                                    const __nv_bfloat16 yb = __float2bfloat16_rn(__uint_as_float(v[i]));
+                                    Yb[o] = *reinterpret_cast<const uint16_t*>(&yb);
+                                } else {
+                                    Y[o] = __uint_as_float(v[i]);
+                                }
+                            }
+                        }
+                    }
+                }
+            } else if constexpr (kMode == kRouter) {
                 float* mine = stg + lane * 33;     // own row, stride 33: conflict-free
                 if (args.k_splits > 1) {
                     // One K slice: the thread's float32 partial logits go to
@@ -782,12 +907,12 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kMode, bool kPair, bool kI8 = false>
+template <int kMode, bool kPair, bool kI8 = false, bool kWM = false>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcGemmArgs& args,
                        int grid, cudaStream_t s) {
     // the router's epilogue warps also keep the logit offset in shared memory
     const size_t smem = tc_gemm_smem_bytes() + (kMode == kRouter ? 4 * kBiasWarpBytes : 0);
-    auto k = grouped_gemm_tc<kMode, kPair, kI8>;
+    auto k = grouped_gemm_tc<kMode, kPair, kI8, kWM>;
     smem_attr((const void*)k, (int)smem);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -807,8 +932,21 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcG
 }
 
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b) {
+                           const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b,
+                           bool weights_m) {
     if (grid <= 0) return cudaSuccess;
+    if (weights_m) {
+        // CTA pairs, bf16, gate/up over the whole K (the down projection may
+        // be split into float32 K slices): tmA the weights (64-row boxes for
+        // gate/up, 128-row boxes for down), tmB the token rows (128-row boxes)
+        if (!pair || int8_b || mode == kRouter || (mode == kGateUp && args.k_splits != 1) ||
+            (args.y_bf16 && args.k_splits != 1))
+            return cudaErrorInvalidValue;
+        const cudaError_t e = mode == kGateUp
+                                  ? launch_one<kGateUp, true, false, true>(tmA, tmB, args, grid & ~1, s)
+                                  : launch_one<kDown, true, false, true>(tmA, tmB, args, grid & ~1, s);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     // bf16 Y: the down projection's rows, not K slices
     if (args.y_bf16 && (mode != kDown || args.k_splits > 1)) return cudaErrorInvalidValue;
     // the split gate/up and router fixups count epilogue warps of single CTAs
@@ -853,7 +991,7 @@ int tc_gemm_max_pairs() {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        auto k = grouped_gemm_tc<kGateUp, true, false>;
+        auto k = grouped_gemm_tc<kGateUp, true, false, false>;
         smem_attr((const void*)k, (int)tc_gemm_smem_bytes());
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) n = 0;

@@ -59,8 +59,15 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 // stage by bulk copies; tmB unused) dequantised to f16 in shared memory by
 // converter warps; A (Xp, H) is f16 and H is written as f16; single CTAs,
 // kGateUp / kDown only.
+// weights_m (CTA pairs, bf16, no gate/up K slices): the weights are the MMA's A (M)
+// operand and the tile's tokens its B (N) operand, N = the tile's rows
+// rounded up to 32, so an expert's last tile computes at most 31 padding
+// columns instead of up to 255 padding rows.  tmA: the packed weights (gate/up
+// with 64-row boxes: each CTA's 128 A rows are the 64 gate then the 64 up rows
+// of its 64 hidden units; down with 128-row boxes), tmB: Xp or H (128-row boxes).
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b = false);
+                           const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b = false,
+                           bool weights_m = false);
 
 // Decode-sized expert GEMMs with the weights as the MMA's M operand
 // (gemm_dec.cu): tiles of 128 weight rows x 32 tokens of one expert (the tile

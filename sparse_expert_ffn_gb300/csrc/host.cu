@@ -94,6 +94,7 @@ struct colibri_moe {
     bool grouped_ok = false;
     // B operands: 128-row boxes for CTA pairs, 256-row boxes for single CTAs
     CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT, tm_wr, tm_wgu1, tm_wdT1;
+    CUtensorMap tm_wgu64;   // packed gate/up, 64-row boxes (weights-as-M pair GEMM)
     // decode GEMM (weights as M): token rows in 32-row boxes (bf16 weights:
     // tm_wgu / tm_wdT, 128-row boxes; int8 codes: bulk copies of tiles)
     CUtensorMap tm_xp32, tm_h32;
@@ -153,6 +154,14 @@ constexpr int kMaxRouterSplit = 8;
 constexpr int kDecMaxPairsPerExpert = 16;
 // The gate/up GEMM splits K only for batches of at most this many pairs.
 constexpr int kGateUpSplitMaxPairs = 64;
+// CTA-pair GEMMs run with the weights as the MMA's M operand and each tile's
+// tokens as N (rounded up to 32), so an expert's last tile carries at most 31
+// padding columns instead of up to 255 padding rows.  The down projection
+// always; gate/up from this d_model on, where a work item's MMAs (K = d) hide
+// its transposed epilogue (measured, Mixtral-shaped T = 4096: gate/up 1191 ->
+// 1175 us, down 590 -> 572 us; DeepSeek-shaped T = 16384, K = 2048: gate/up
+// 560 -> 718 us, the epilogue exposed).
+constexpr int kWmGateUpMinK = 4096;
 // Int8 weights: batches of at most this many tokens stream the codes on the
 // CUDA cores (gemv_i8.cu) when the gate/up stage has at least one 64-unit
 // item per SM; the tensor-core decode GEMMs take one MMA per 2 KB of codes
@@ -579,10 +588,13 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             const int grid = cta_per_unit * (int)std::min<int64_t>(
                                                     (int64_t)tiles_ub * a.n_blocks * a.k_splits, units);
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
-            st = g.done(dec ? launch_tc_gemm_dec(kGateUp, h->tm_xp32, h->int8 ? h->tm_xp : h->tm_wgu,
-                                                 a, grid, s, h->int8)
-                            : launch_tc_gemm(kGateUp, pair, h->tm_xp, pair ? h->tm_wgu : h->tm_wgu1,
-                                             a, grid, s, h->int8),
+            st = g.done(dec    ? launch_tc_gemm_dec(kGateUp, h->tm_xp32, h->int8 ? h->tm_xp : h->tm_wgu,
+                                                    a, grid, s, h->int8)
+                        : pair && d >= kWmGateUpMinK
+                            ? launch_tc_gemm(kGateUp, true, h->tm_wgu64, h->tm_xp, a, grid, s, false, true)
+                        : pair ? launch_tc_gemm(kGateUp, true, h->tm_xp, h->tm_wgu, a, grid, s)
+                               : launch_tc_gemm(kGateUp, false, h->tm_xp, h->tm_wgu1, a, grid, s,
+                                                h->int8),
                         1);
             if (st != COLIBRI_OK) return st;
         }
@@ -614,10 +626,12 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             const int grid = cta_per_unit * (int)std::min<int64_t>(
                                                     (int64_t)tiles_ub * a.n_blocks * a.k_splits, units);
             Stage g(h, COLIBRI_STAGE_EXPERT_DOWN, s);
-            st = g.done(dec ? launch_tc_gemm_dec(kDown, h->tm_h32, h->int8 ? h->tm_h : h->tm_wdT, a,
-                                                 grid, s, h->int8)
-                            : launch_tc_gemm(kDown, pair, h->tm_h, pair ? h->tm_wdT : h->tm_wdT1, a,
-                                             grid, s, h->int8),
+            st = g.done(dec    ? launch_tc_gemm_dec(kDown, h->tm_h32, h->int8 ? h->tm_h : h->tm_wdT, a,
+                                                    grid, s, h->int8)
+                        : pair ? launch_tc_gemm(kDown, true, h->tm_wdT, h->tm_h, a, grid, s, false,
+                                                true)
+                               : launch_tc_gemm(kDown, false, h->tm_h, h->tm_wdT1, a, grid, s,
+                                                h->int8),
                         1);
             if (st != COLIBRI_OK) return st;
         }
@@ -878,7 +892,8 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
             ok = ok && make_tmap_bf16(&h->tm_wgu, h->wgu, (uint64_t)E * 2 * f, d, 128) &&
                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 128) &&
                  make_tmap_bf16(&h->tm_wgu1, h->wgu, (uint64_t)E * 2 * f, d, 256) &&
-                 make_tmap_bf16(&h->tm_wdT1, h->wdT, (uint64_t)E * d, f, 256);
+                 make_tmap_bf16(&h->tm_wdT1, h->wdT, (uint64_t)E * d, f, 256) &&
+                 make_tmap_bf16(&h->tm_wgu64, h->wgu, (uint64_t)E * 2 * f, d, 64);
         if (!ok) {
             if (cfg->executor == COLIBRI_EXEC_GROUPED) return fail(COLIBRI_ERR_CUDA);
             h->grouped_ok = false;
