@@ -294,11 +294,6 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t* a_empty = bars + 2 * kStages + 12;   // [kAStagesI8] kI8: A consumed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 15);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    // kWM gate/up: per pair of epilogue warps (q, q + 2), "staged" and "read"
-    // barriers of the gate/up exchange, two arrivals each
-    uint64_t* xchg = bars + 32;   // [2 pairs][staged, read]
-    static_assert(!kWM || (2 * kMaxSt + 17 <= 32 && 36 * 8 <= 512),
-                  "exchange barriers after the others, inside the 512 bytes after the ring");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // CTA pair: rank 0 (leader) owns the full / acc_empty barriers and issues
@@ -329,8 +324,6 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(smem_u32(&acc_empty[a]), kPair ? 8 : 4);
         }
         mbar_init(smem_u32(&mma_done[0]), 1);
-        if constexpr (kWM && kMode == kGateUp)
-            for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xchg[i]), 2);
         if constexpr (kI8) {
             for (int b = 0; b < kBStages; ++b) {
                 mbar_init(smem_u32(&bf_full[b]), kConvWarps);
@@ -391,12 +384,13 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         tma_load_2d_pair(sb, &tmB, kb * kBK,
                                          wk.row0 + (int)rank * (wm_cols(wk.rows) / 2), fb);
                         if constexpr (kMode == kGateUp) {
-                            // 64 hidden units per CTA: their gate rows (TMEM
-                            // lanes 0-63) and up rows (lanes 64-127)
+                            // 64 hidden units per CTA in four groups of 16:
+                            // group g's 16 gate rows (TMEM lanes 32g..32g+15)
+                            // then its 16 up rows (32g+16..32g+31), one copy
+                            // through the 5-D view of make_tmap_gate_up_wm
                             const int f = args.b_rows_per_expert / 2;
-                            const int base = ((wk.expert * (f / 128) + wk.nblk) * 2) * 128 + (int)rank * 64;
-                            tma_load_2d_pair(sa, &tmA, kb * kBK, base, fb);
-                            tma_load_2d_pair(sa + 64 * 128, &tmA, kb * kBK, base + 128, fb);
+                            tma_load_5d_pair(sa, &tmA, kb * kBK, 0, 0, 0,
+                                             4 * (wk.expert * (f / 128) + wk.nblk) + (int)rank, fb);
                         } else {
                             tma_load_2d_pair(sa, &tmA, kb * kBK,
                                              wk.expert * args.b_rows_per_expert + wk.nblk * kBN +
@@ -518,7 +512,6 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             kPair ? map_to_rank(smem_u32(&acc_empty[0]), 0) : smem_u32(&acc_empty[0]);
         int acc = 0;
         uint32_t acc_phase = 0;
-        uint32_t xphase = 0;   // kWM gate/up: phase of the pair's exchange barriers
         for (int w = unit; w < total; w += n_units) {
             const Work wk = get_work<kMode>(w, args);
             const bool got =
@@ -535,68 +528,37 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // TMEM lane = weight row of this CTA, column = token of the tile
                 const int ncol = wm_cols(wk.rows);
                 if constexpr (kMode == kGateUp) {
-                    // Warp q < 2 holds the gate rows and warp q + 2 the up
-                    // rows of the same 32 hidden units (lane = unit).  Per
-                    // 32-token chunk each stages its values in shared memory,
-                    // the pair meets at a named barrier, and the gate warp
-                    // forms H for the chunk's first 16 tokens, the up warp
-                    // for the last 16 (a store: 32 consecutive units of a token).
+                    // lanes 0-15 hold the gate and lanes 16-31 the up rows of
+                    // 16 hidden units; one shuffle per token pairs them, and
+                    // lanes 0-15 form and store the chunk's first 16 tokens,
+                    // lanes 16-31 the last 16 (a store: 16 consecutive units)
                     uint16_t* H = reinterpret_cast<uint16_t*>(args.out);
-                    const int unit = wk.nblk * kBM + (int)rank * 64 + (q & 1) * 32 + lane;
-                    const bool up = q >= 2;
-                    // staging slots go by warp - 2 = q ^ 2, so the partner
-                    // (lane quarter q ^ 2) stages in slot q
-                    float* partner = reinterpret_cast<float*>(smem + kStagingOffset) + q * 32 * kStgStride;
-                    // the pair's barriers: every wait bounded, so that a warp
-                    // whose partner gave up gives up too
-                    const uint32_t x_staged = smem_u32(&xchg[2 * (q & 1)]);
-                    const uint32_t x_read = smem_u32(&xchg[2 * (q & 1) + 1]);
-                    auto pair_sync = [&](uint32_t bar) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar);
-                        const bool ok = mbar_wait(bar, xphase, abort_flag, args.status, limit);
-                        return __all_sync(0xffffffffu, ok);
-                    };
-                    bool xok = true;
+                    const int unit = wk.nblk * kBM + (int)rank * 64 + q * 16 + (lane & 15);
+                    const int hi = lane >> 4;
 #pragma unroll 1
                     for (int c = 0; c < ncol; c += 32) {
                         uint32_t v[32];
                         tmem_ld32(tbase + c, v);
                         tmem_ld_wait();
-                        float4* mine = reinterpret_cast<float4*>(stg + lane * kStgStride);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            mine[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-                        if (!(xok = pair_sync(x_staged))) break;
-                        const float4* other =
-                            reinterpret_cast<const float4*>(partner + lane * kStgStride) + (up ? 4 : 0);
-                        const int t0 = c + (up ? 16 : 0);
-#pragma unroll
-                        for (int i4 = 0; i4 < 4; ++i4) {
-                            const float4 o = other[i4];
-                            const float ov[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const int i = 4 * i4 + j;
-                                const float own = __uint_as_float(up ? v[16 + i] : v[i]);
-                                const float g = up ? ov[j] : own, u = up ? own : ov[j];
-                                if (t0 + i < wk.rows) {
-                                    // fast exp and divide (|rel err| ~1e-6, far below the
-                                    // bf16 rounding of H): this epilogue is
-                                    // instruction-bound at small K
-                                    const float sg = __fdividef(g, 1.0f + __expf(-g));
-                                    const __nv_bfloat16 hb = __float2bfloat16_rn(sg * u);
-                                    H[(size_t)(wk.row0 + t0 + i) * args.out_ld + unit] =
-                                        *reinterpret_cast<const uint16_t*>(&hb);
-                                }
+                        for (int i = 0; i < 16; ++i) {
+                            // lane < 16 sends its gate of token 16 + i and gets
+                            // the up of token i; lane >= 16 the other way round
+                            const float mine = __uint_as_float(hi ? v[16 + i] : v[i]);
+                            const float other = __shfl_xor_sync(
+                                0xffffffffu, __uint_as_float(hi ? v[i] : v[16 + i]), 16);
+                            const float g = hi ? other : mine, u = hi ? mine : other;
+                            const int t = c + 16 * hi + i;
+                            if (t < wk.rows) {
+                                // fast exp and divide (|rel err| ~1e-6, far
+                                // below the bf16 rounding of H)
+                                const float sg = __fdividef(g, 1.0f + __expf(-g));
+                                const __nv_bfloat16 hb = __float2bfloat16_rn(sg * u);
+                                H[(size_t)(wk.row0 + t) * args.out_ld + unit] =
+                                    *reinterpret_cast<const uint16_t*>(&hb);
                             }
                         }
-                        // both done reading before the next chunk is staged
-                        if (!(xok = pair_sync(x_read))) break;
-                        xphase ^= 1;
                     }
-                    if (!xok) break;
                 } else {
                     const int feat = wk.nblk * kBN + (int)rank * kBM + q * 32 + lane;
                     float* Y = reinterpret_cast<float*>(args.out) + wk.split * args.out_split_stride;
@@ -883,6 +845,24 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+bool make_tmap_gate_up_wm(CUtensorMap* map, const void* wgu, uint64_t rows, uint64_t d) {
+    // The packed gate/up rows [E][f/128][2][128][d] seen as 5-D:
+    //   (k, i, which, g, j) -> row j*64 + which*128 + g*16 + i, column k,
+    // j = 4 * (128-unit block) + half; a box {64, 16, 2, 4, 1} is, in order,
+    // group g's 16 gate rows then its 16 up rows for g = 0..3: the 64 hidden
+    // units of one half-block with gate and up interleaved per 16 units.
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows % 256 || d % 64) return false;
+    const cuuint64_t D = d * 2;
+    const cuuint64_t dims[5] = {d, 16, 2, 4, rows / 64};
+    const cuuint64_t strides[4] = {D, 128 * D, 16 * D, 64 * D};
+    const cuuint32_t box[5] = {(cuuint32_t)kBK, 16, 2, 4, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(wgu), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t tc_gemm_smem_bytes() {
     // ring + barriers (512 B) + 4 epilogue staging tiles + 1024-byte alignment slack
     return (size_t)kBiasOffset + 1024;
@@ -937,8 +917,8 @@ cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CU
     if (grid <= 0) return cudaSuccess;
     if (weights_m) {
         // CTA pairs, bf16, gate/up over the whole K (the down projection may
-        // be split into float32 K slices): tmA the weights (64-row boxes for
-        // gate/up, 128-row boxes for down), tmB the token rows (128-row boxes)
+        // be split into float32 K slices): tmA the weights (make_tmap_gate_up_wm
+        // for gate/up, 128-row boxes for down), tmB the token rows (128-row boxes)
         if (!pair || int8_b || mode == kRouter || (mode == kGateUp && args.k_splits != 1) ||
             (args.y_bf16 && args.k_splits != 1))
             return cudaErrorInvalidValue;

@@ -53,6 +53,9 @@ int tc_gemm_pair_rows();     // rows of one expert tile of a CTA pair (256)
 int tc_gemm_max_pairs();     // CTA pairs resident at once (0 if unknown)
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows, bool f16 = false);
+// The packed bf16 gate/up weights (rows = E * 2 * d_ff, d columns) as the
+// 5-D view the weights-as-M gate/up GEMM loads one CTA's A stage through.
+bool make_tmap_gate_up_wm(CUtensorMap* map, const void* wgu, uint64_t rows, uint64_t d);
 // pair: run the expert GEMMs on CTA pairs (256-row tiles, B tensor map with
 // 128-row boxes) instead of single CTAs (128-row tiles, 256-row B boxes).
 // int8_b: B is int8 codes (args.q_codes, tile-major, two 128-row tiles per
@@ -63,8 +66,9 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 // operand and the tile's tokens its B (N) operand, N = the tile's rows
 // rounded up to 32, so an expert's last tile computes at most 31 padding
 // columns instead of up to 255 padding rows.  tmA: the packed weights (gate/up
-// with 64-row boxes: each CTA's 128 A rows are the 64 gate then the 64 up rows
-// of its 64 hidden units; down with 128-row boxes), tmB: Xp or H (128-row boxes).
+// through make_tmap_gate_up_wm: each CTA's 128 A rows are 4 x (16 gate, 16 up)
+// rows of its 64 hidden units; down with 128-row boxes), tmB: Xp or H
+// (128-row boxes).
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b = false,
                            bool weights_m = false);

@@ -94,7 +94,8 @@ struct colibri_moe {
     bool grouped_ok = false;
     // B operands: 128-row boxes for CTA pairs, 256-row boxes for single CTAs
     CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT, tm_wr, tm_wgu1, tm_wdT1;
-    CUtensorMap tm_wgu64;   // packed gate/up, 64-row boxes (weights-as-M pair GEMM)
+    CUtensorMap tm_wgu_wm;  // packed gate/up, 5-D view (weights-as-M pair GEMM)
+    bool wm_gate_up = false;   // the view encoded
     // decode GEMM (weights as M): token rows in 32-row boxes (bf16 weights:
     // tm_wgu / tm_wdT, 128-row boxes; int8 codes: bulk copies of tiles)
     CUtensorMap tm_xp32, tm_h32;
@@ -590,8 +591,8 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             Stage g(h, COLIBRI_STAGE_EXPERT_UP, s);
             st = g.done(dec    ? launch_tc_gemm_dec(kGateUp, h->tm_xp32, h->int8 ? h->tm_xp : h->tm_wgu,
                                                     a, grid, s, h->int8)
-                        : pair && d >= kWmGateUpMinK
-                            ? launch_tc_gemm(kGateUp, true, h->tm_wgu64, h->tm_xp, a, grid, s, false, true)
+                        : pair && h->wm_gate_up && d >= kWmGateUpMinK
+                            ? launch_tc_gemm(kGateUp, true, h->tm_wgu_wm, h->tm_xp, a, grid, s, false, true)
                         : pair ? launch_tc_gemm(kGateUp, true, h->tm_xp, h->tm_wgu, a, grid, s)
                                : launch_tc_gemm(kGateUp, false, h->tm_xp, h->tm_wgu1, a, grid, s,
                                                 h->int8),
@@ -893,7 +894,9 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 128) &&
                  make_tmap_bf16(&h->tm_wgu1, h->wgu, (uint64_t)E * 2 * f, d, 256) &&
                  make_tmap_bf16(&h->tm_wdT1, h->wdT, (uint64_t)E * d, f, 256) &&
-                 make_tmap_bf16(&h->tm_wgu64, h->wgu, (uint64_t)E * 2 * f, d, 64);
+                 true;
+        // the 5-D view is optional: without it gate/up stays token-on-M
+        if (ok && !int8) h->wm_gate_up = make_tmap_gate_up_wm(&h->tm_wgu_wm, h->wgu, (uint64_t)E * 2 * f, d);
         if (!ok) {
             if (cfg->executor == COLIBRI_EXEC_GROUPED) return fail(COLIBRI_ERR_CUDA);
             h->grouped_ok = false;
