@@ -206,7 +206,7 @@ ffn_gemv_i8(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ per
             const int32_t* __restrict__ tile_row, const int32_t* __restrict__ tile_info,
             const int32_t* __restrict__ num_tiles, int E, int d, int f, int ks,
             __nv_bfloat16* __restrict__ H, float* __restrict__ Y, size_t y_split_stride,
-            int* status, uint64_t limit) {
+            int* status, uint64_t limit, int stall) {
     using namespace tc;
     constexpr int kStages = gv_stages<kUp>();
     constexpr int kStageBytes = gv_stage_bytes<kUp>();
@@ -248,7 +248,7 @@ ffn_gemv_i8(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ per
             uint32_t issued_phase[kStages];
             for (int i = 0; i < kStages; ++i) issued[i] = false, issued_phase[i] = 0;
             bool ok = true;
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            for (int it = blockIdx.x; it < n_items && ok && !stall; it += gridDim.x) {
                 const int sl = it % ks;
                 const int g = (it / ks) % groups;
                 const int tile = it / (ks * groups);
@@ -458,7 +458,8 @@ cudaError_t launch_one(const void* x, const int32_t* perm, int k, const int8_t* 
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3(grid), dim3(kGvThreads), (size_t)bytes, s, (const __nv_bfloat16*)x,
                    perm, k, wq, sc, zp, t.tile_expert, t.tile_row, t.tile_info, t.num_tiles, t.E, d,
-                   f, ks, (__nv_bfloat16*)H, Y, y_split_stride, t.status, t.wait_limit_ns);
+                   f, ks, (__nv_bfloat16*)H, Y, y_split_stride, t.status, t.wait_limit_ns,
+                   t.stall_producer);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

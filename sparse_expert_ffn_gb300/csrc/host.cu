@@ -495,7 +495,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
         // codes read once per pass of S token rows
         const int S = gemv_i8_slots(T);
         const GemvTiles tl{h->tile_expert, h->tile_row, h->tile_info, h->num_tiles, E, h->status,
-                           h->wait_limit_ns};
+                           h->wait_limit_ns, h->stall_tma ? 1 : 0};
         const int tiles_est = std::min(E, npairs);
         const int max_ks = (int)std::min<size_t>(kMaxKSplit, h->y_floats / ((size_t)npairs * d));
         int ks = choose_gemv_slices((int64_t)tiles_est * (d / 64), f / 64, h->num_sms, max_ks);

@@ -85,6 +85,8 @@ struct GemvTiles {
     int E;                    // experts: tile_expert values are checked against it
     int* status;              // DEV_TIMEOUT when a wait gave up, DEV_BAD_INDEX on a bad expert
     uint64_t wait_limit_ns;   // bound of every wait
+    int stall_producer;       // failure-detection tests only: issue no copy, so the
+                              // consumers' first wait runs out its bound
 };
 int gemv_i8_slots(int max_rows_per_expert);
 bool gemv_i8_fits(int S, int d, int f, int ks);

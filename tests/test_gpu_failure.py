@@ -53,23 +53,31 @@ def test_injected_allocation_failure_rolls_back(lib, monkeypatch):
     layer.close()
 
 
+# A d_model of 4096 puts gate/up on the weights-as-M pair kernel too (the
+# narrower shape runs only its down projection that way).
+WIDE = synth.LayerShape("failure_probe_wide", 4096, 1024, 8, 2, "bf16")
+
+
 # 2 tokens split the gate/up GEMM over K (last-slice fixup), 256 tokens run
 # the expert GEMMs on single CTAs, 1024 on CTA pairs (at least 128
-# (token, slot) pairs per expert on average).
-@pytest.mark.parametrize("T", [2, 256, 1024], ids=["split_k", "single_cta", "cta_pairs"])
-def test_bounded_wait_times_out_and_context_survives(lib, monkeypatch, T):
+# (token, slot) pairs per expert on average), with the weights as the MMA's
+# M operand for the down projection, and for gate/up as well on WIDE.
+@pytest.mark.parametrize("shape,T", [(SHAPE, 2), (SHAPE, 256), (SHAPE, 1024), (WIDE, 1024)],
+                         ids=["split_k", "single_cta", "cta_pairs", "cta_pairs_wide"])
+def test_bounded_wait_times_out_and_context_survives(lib, monkeypatch, shape, T):
     sef = lib
     dev = torch.device("cuda", 0)
-    ws = _weights(dev)
-    x = synth.tokens(SHAPE, T, 3, 0, dev)
+    wr = synth.router_weight(shape, 3, 0, dev)
+    ws = (wr, *synth.expert_weights(shape, 3, 0, dev))
+    x = synth.tokens(shape, T, 3, 0, dev)
 
-    ref_layer = sef.MoELayer(*ws, SHAPE.top_k, max_tokens=T, executor="grouped")
+    ref_layer = sef.MoELayer(*ws, shape.top_k, max_tokens=T, executor="grouped")
     y_ref = ref_layer.forward(x)
     assert ref_layer.check() == sef.OK
 
     monkeypatch.setenv("COLIBRI_WAIT_LIMIT_NS", "20000000")
     monkeypatch.setenv("COLIBRI_TEST_STALL_TMA", "1")
-    short = sef.MoELayer(*ws, SHAPE.top_k, max_tokens=T, executor="grouped")
+    short = sef.MoELayer(*ws, shape.top_k, max_tokens=T, executor="grouped")
     monkeypatch.delenv("COLIBRI_WAIT_LIMIT_NS")
     monkeypatch.delenv("COLIBRI_TEST_STALL_TMA")
     short.forward(x)
@@ -100,6 +108,37 @@ def test_bounded_wait_times_out_on_the_int8_gemm(lib, monkeypatch):
     monkeypatch.setenv("COLIBRI_WAIT_LIMIT_NS", "20000000")
     monkeypatch.setenv("COLIBRI_TEST_STALL_TMA", "1")
     short = sef.MoELayer(wr, None, None, None, SHAPE.top_k, max_tokens=8, int8=parts)
+    monkeypatch.delenv("COLIBRI_WAIT_LIMIT_NS")
+    monkeypatch.delenv("COLIBRI_TEST_STALL_TMA")
+    short.forward(x)
+    assert short.check() == sef.ERR_TIMEOUT
+    assert short.check() == sef.OK
+    short.close()
+
+    y2 = ref_layer.forward(x)
+    assert ref_layer.check() == sef.OK
+    assert torch.equal(y_ref, y2)
+    ref_layer.close()
+
+
+def test_bounded_wait_times_out_on_the_int8_gemv(lib, monkeypatch):
+    """The CUDA-core int8 GEMV (one token, streaming executor): its consumer
+    warps give up on a ring stage that never lands, the CTA winds down, and
+    the status word reports the timeout."""
+    sef = lib
+    dev = torch.device("cuda", 0)
+    wr, wg, wu, wd = _weights(dev)
+    parts = [tuple(t.to(dev) for t in sef.quantize_int8_block64(w)) for w in (wg, wu, wd)]
+    x = synth.tokens(SHAPE, 1, 3, 0, dev)
+    ref_layer = sef.MoELayer(wr, None, None, None, SHAPE.top_k, max_tokens=1, int8=parts,
+                             executor="stream")
+    y_ref = ref_layer.forward(x)
+    assert ref_layer.check() == sef.OK
+
+    monkeypatch.setenv("COLIBRI_WAIT_LIMIT_NS", "20000000")
+    monkeypatch.setenv("COLIBRI_TEST_STALL_TMA", "1")
+    short = sef.MoELayer(wr, None, None, None, SHAPE.top_k, max_tokens=1, int8=parts,
+                         executor="stream")
     monkeypatch.delenv("COLIBRI_WAIT_LIMIT_NS")
     monkeypatch.delenv("COLIBRI_TEST_STALL_TMA")
     short.forward(x)
