@@ -72,6 +72,19 @@ def test_deepseek_capacity_multi_cta_dispatch_and_pairs(lib, C):
         c.close()
 
 
+def test_mixtral_capacity_weights_as_m_pairs(lib):
+    """Mixtral-shaped T = 4096 (about 1024 pairs per expert) capped at 1000:
+    the CTA-pair GEMMs with the weights as the MMA's M operand (gate/up too,
+    at d_model 4096) see every capped expert's last tile end 232 rows in."""
+    c = Case(synth.MIXTRAL, seed=0, max_tokens=4096)
+    try:
+        x, x64 = c.tokens(4096)
+        y, r, keep, _ = _run_capped(c, x, x64, 1000, "grouped")
+        assert (r["counts"] > 1000).any() and (~keep).any()
+    finally:
+        c.close()
+
+
 def test_residual_layer_with_capacity_zero_is_identity(lib):
     shape = synth.LayerShape("cap_stack", 512, 1024, 8, 2, "bf16")
     c = Case(shape, seed=4, max_tokens=64)
