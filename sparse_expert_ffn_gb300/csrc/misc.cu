@@ -20,8 +20,12 @@ namespace {
 // row's latency chain per CTA.
 constexpr int kGatherThreads = 256;
 constexpr int kGatherCtasPerSm = 8;
+constexpr size_t kGatherStreamBytes = (size_t)64 << 20;
 
-template <bool kToF16>
+// kStream: rows stored with the streaming hint (st.global.cs), for an Xp
+// too large for L2: written normally it evicts the token rows x, which every
+// token's k pairs read again at k different times of the gather.
+template <bool kToF16, bool kStream>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k, int row_vecs,
             int npairs, int src_pairs, uint4* __restrict__ xp) {
@@ -45,7 +49,9 @@ gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ perm, int k
 #pragma unroll 8
         for (int i = lane; i < row_vecs; i += 32) {
             const uint4 v = __ldg(src + i);
-            dst[i] = kToF16 ? bf16x8_to_f16x8(v) : v;
+            const uint4 w = kToF16 ? bf16x8_to_f16x8(v) : v;
+            if (kStream) __stcs(dst + i, w);
+            else dst[i] = w;
         }
     }
 }
@@ -219,11 +225,13 @@ cudaError_t launch_gather(int elem_bytes, const void* x, const int32_t* perm, in
     const int warps_per_cta = kGatherThreads / 32;
     const int grid = std::max(1, std::min((npairs + warps_per_cta - 1) / warps_per_cta,
                                           sms * kGatherCtasPerSm));
-    const cudaError_t e =
-        to_f16 ? launch_pdl(gather_rows<true>, grid, kGatherThreads, 0, s, (const uint4*)x, perm, k,
-                            row_vecs, npairs, src_pairs, (uint4*)xp)
-               : launch_pdl(gather_rows<false>, grid, kGatherThreads, 0, s, (const uint4*)x, perm, k,
-                            row_vecs, npairs, src_pairs, (uint4*)xp);
+    // Xp above half of L2 streams past it (kStream); a smaller one stays for
+    // the GEMM that reads it next
+    const bool stream = (size_t)npairs * row_vecs * 16 > kGatherStreamBytes;
+    auto kern = to_f16 ? (stream ? gather_rows<true, true> : gather_rows<true, false>)
+                       : (stream ? gather_rows<false, true> : gather_rows<false, false>);
+    const cudaError_t e = launch_pdl(kern, grid, kGatherThreads, 0, s, (const uint4*)x, perm, k,
+                                     row_vecs, npairs, src_pairs, (uint4*)xp);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
