@@ -90,3 +90,25 @@ def test_mixtral_int8_gemv_with_capacity(mixtral8):
         check_output(mixtral8, x64, y, r, l, capacity=1)
     finally:
         mixtral8.layer.set_capacity(None)
+
+
+def test_mixtral_int8_gemv_shared_experts_routed(mixtral8):
+    """The caller's routing sends the three tokens to experts 3 and 5 only
+    (the last token twice to 3): expert 3 gets four rows and expert 5 two,
+    so the GEMV's four-row passes run with every row live and as a two-row
+    pass; the output is the oracle's layer at that routing."""
+    import oracle
+    from parity import Y_RTOL
+    x, x64 = mixtral8.tokens(3)
+    idx = torch.tensor([[3, 5], [5, 3], [3, 3]], dtype=torch.int32, device=x.device)
+    w = torch.tensor([[0.7, 0.3], [0.6, 0.4], [0.5, 0.5]], dtype=torch.float32, device=x.device)
+    mixtral8.layer.set_executor("stream")
+    y = mixtral8.layer.forward_routed(x, idx, w)
+    torch.cuda.synchronize()
+    assert mixtral8.layer.check() == 0
+    y_ref = oracle.token_outputs(x64, idx.cpu().numpy(), w.double().cpu().numpy(), mixtral8.experts)
+    y_gpu = oracle.to_f64(y.cpu())
+    err = np.abs(y_gpu - y_ref).max() / np.abs(y_ref).max()
+    assert err <= Y_RTOL["bf16"], f"max|err|/max|ref| = {err:.3e}"
+    y2 = mixtral8.layer.forward_routed(x, idx, w)
+    assert torch.equal(y, y2)
