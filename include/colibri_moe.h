@@ -50,7 +50,7 @@ typedef enum {
 
 typedef enum {
     COLIBRI_EXEC_AUTO = 0,        /* choose from T and the shapes */
-    COLIBRI_EXEC_STREAM = 1,      /* weight-streaming expert FFN on CUDA cores (decode sizes, fp32) */
+    COLIBRI_EXEC_STREAM = 1,      /* weight-streaming expert FFN on CUDA cores (decode sizes, fp32, int8) */
     COLIBRI_EXEC_GROUPED = 2      /* tcgen05 grouped GEMM expert FFN (bf16 only) */
 } colibri_executor_t;
 
@@ -136,11 +136,17 @@ colibri_status_t colibri_quantize_int8_block64(const void* w, int32_t dtype, int
  *   w_gate, w_up  R = d_model, C = d_ff   (as colibri_init's [E, d_model, d_ff])
  *   w_down        R = d_ff,    C = d_model
  * w_router / router_bias / cfg as in colibri_init (cfg->dtype is the
- * activation and router type).  Executors: GROUPED (bf16 activations; the
- * default) streams the int8 codes into shared memory with TMA, converter
- * warps dequantise each 256x64 stage to bf16 and the tcgen05 MMAs read it;
- * STREAM dequantises in registers on CUDA cores (the only executor for fp32
- * activations).  weights_on_device applies to every array.
+ * activation and router type).  Executors: GROUPED (bf16 activations)
+ * streams the int8 codes into shared memory with TMA, converter warps
+ * dequantise them (to f16) and the tcgen05 MMAs read them; STREAM runs on
+ * CUDA cores: for bf16 batches of at most three tokens the codes stream
+ * through shared memory by bulk copies and multiply 16-bit integer
+ * activations (one per 64-wide block, scaled by a power of two) with integer
+ * dot products, otherwise each row's codes are dequantised in registers (the
+ * only executor for fp32 activations).  AUTO picks STREAM for bf16 batches
+ * of at most three tokens whose gate/up stage has at least one 64-unit item
+ * per SM (top_k * d_ff / 64 >= SMs), GROUPED otherwise.  weights_on_device
+ * applies to every array.
  */
 colibri_status_t colibri_init_int8(const colibri_moe_config_t* cfg,
                                    const void* w_router, const float* router_bias,
