@@ -254,6 +254,29 @@ __device__ __noinline__ void router_split_fixup(const TcGemmArgs& args, const Wo
     if (lane == 0) *ctr = 0;
 }
 
+// Order in which the CTAs of the expert GEMMs take the work list when the
+// expert sizes are skewed: even positions walk it from the front, odd ones
+// from the back.  The list is in expert order, so the units of the large
+// experts (many m-tiles per weight block: bound by the tensor pipe) then run
+// beside those of the small ones (one m-tile per weight block: bound by the
+// weight stream from HBM) instead of in separate waves.  A bijection of
+// [0, total): front positions j < ceil(total / 2), back ones the rest.
+__device__ __forceinline__ int both_ends(int w, int total) {
+    const int j = w >> 1;
+    return (w & 1) ? total - 1 - j : j;
+}
+
+// Skewed: the first expert's raster band is at least four times as long as
+// the last one's (a Zipf-like load puts the large experts first).  Under
+// even loads a second stream costs L2 locality, so the list is walked in
+// order.
+__device__ __forceinline__ bool work_skewed(const int32_t* tile_info, int num_tiles) {
+    if (num_tiles < 2) return false;
+    const int first = (tile_info[0] >> 18) & 0xFF;
+    const int last = (tile_info[num_tiles - 1] >> 18) & 0xFF;
+    return first >= 4 * last;
+}
+
 // Weights as M (kWM): token columns of a tile, its valid rows rounded up to
 // 32 (each CTA of the pair holds half of them as MMA B rows).
 __device__ __forceinline__ int wm_cols(int rows) { return min(2 * kBM, max(32, (rows + 31) & ~31)); }
@@ -261,7 +284,7 @@ __device__ __forceinline__ int wm_cols(int rows) { return min(2 * kBM, max(32, (
 template <int kMode, bool kPair, bool kI8, bool kWM>
 __global__ void __launch_bounds__(kI8 ? kThreadsI8 : kThreads, 1)
 grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                TcGemmArgs args) {
+                const __grid_constant__ TokenRowMaps tmBr, TcGemmArgs args) {
     static_assert(!kI8 || (!kPair && kMode != kRouter), "int8 B: single-CTA expert GEMMs only");
     static_assert(!kWM || (kPair && !kI8 && kMode != kRouter), "weights as M: CTA-pair expert GEMMs");
     extern __shared__ uint8_t smem_raw[];
@@ -349,6 +372,10 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int num_tiles =
         kMode == kRouter ? (args.dense_rows + kBM - 1) / kBM : *args.num_tiles;
     const int total = num_tiles * args.n_blocks * args.k_splits;
+    const bool skewed = kMode != kRouter && work_skewed(args.tile_info, num_tiles);
+    // every role (producer, MMA, epilogue, both CTAs of a pair) takes the
+    // same order
+    auto work_at = [&](int w) { return get_work<kMode>(skewed ? both_ends(w, total) : w, args); };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -359,12 +386,17 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t issued_phase[kMaxSt];
             for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
             for (int w = unit; w < total && !*abort_flag && !args.stall_producer; w += n_units) {
-                const Work wk = get_work<kMode>(w, args);
+                const Work wk = work_at(w);
                 const int a_row = wk.row0 + (int)rank * kBM;
                 const int b_row = wk.expert * args.b_rows_per_expert + wk.nblk * kBN +
                                   (int)rank * b_rows_cta;
                 const int kb0 = wk.split * kb_per_split;
                 const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
+                // kWM: each CTA loads the tile's token columns it holds
+                // (wm_cols / 2 = 16..128 rows) through the map of that height
+                const int wm_h = kWM ? wm_cols(wk.rows) / 2 : 0;
+                const CUtensorMap* wm_map = &tmBr.m[kWM ? wm_h / 16 - 1 : 0];
+                const uint32_t unit_tx = kWM ? 2 * (kStageA + (uint32_t)wm_h * kBK * 2) : stage_tx;
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, args.status,
@@ -373,16 +405,14 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         break;
                     }
                     const uint32_t fb_local = smem_u32(&full[stage]);
-                    if (leader) mbar_expect_tx(fb_local, stage_tx);
+                    if (leader) mbar_expect_tx(fb_local, unit_tx);
                     const uint32_t sa = smem_u32(stage_a + stage * kStageA);
                     const uint32_t sb = smem_u32(stage_b + stage * kStageB);
                     if constexpr (kWM) {
                         // A: this CTA's 128 weight rows; B: its half of the
-                        // tile's token columns (a 128-row box, of which the
-                        // MMA reads the first wm_cols / 2)
+                        // tile's token columns, exactly the rows the MMA reads
                         const uint32_t fb = map_to_rank(fb_local, 0);
-                        tma_load_2d_pair(sb, &tmB, kb * kBK,
-                                         wk.row0 + (int)rank * (wm_cols(wk.rows) / 2), fb);
+                        tma_load_2d_pair(sb, wm_map, kb * kBK, wk.row0 + (int)rank * wm_h, fb);
                         if constexpr (kMode == kGateUp) {
                             // 64 hidden units per CTA in four groups of 16:
                             // group g's 16 gate rows (TMEM lanes 32g..32g+15)
@@ -441,7 +471,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int w = unit; w < total && !*abort_flag; w += n_units) {
-                const Work wk = get_work<kMode>(w, args);
+                const Work wk = work_at(w);
                 const int kb0 = wk.split * kb_per_split;
                 const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
                 if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1, abort_flag, args.status,
@@ -513,7 +543,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int w = unit; w < total; w += n_units) {
-            const Work wk = get_work<kMode>(w, args);
+            const Work wk = work_at(w);
             const bool got =
                 mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, args.status, limit);
             // tcgen05.ld is warp-collective: the whole warp stops if any lane gave up.
@@ -727,7 +757,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t issued_phase[kAStagesI8];
             for (int s = 0; s < kAStagesI8; ++s) issued[s] = false, issued_phase[s] = 0;
             for (int w = unit; w < total && !*abort_flag && !args.stall_producer; w += n_units) {
-                const Work wk = get_work<kMode>(w, args);
+                const Work wk = work_at(w);
                 const int kb0 = wk.split * kb_per_split;
                 const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
                 bool ok = true;
@@ -763,7 +793,7 @@ grouped_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         int bs = 0;
         uint32_t bphase = 0;
         for (int w = unit; w < total && !*abort_flag; w += n_units) {
-            const Work wk = get_work<kMode>(w, args);
+            const Work wk = work_at(w);
             const int kb0 = wk.split * kb_per_split;
             const int kb1 = min(args.k_blocks, kb0 + kb_per_split);
             // first packed B row of the tile; a multiple of 64 (one block row)
@@ -863,6 +893,12 @@ bool make_tmap_gate_up_wm(CUtensorMap* map, const void* wgu, uint64_t rows, uint
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_token_rows(TokenRowMaps* maps, const void* base, uint64_t rows, uint64_t cols) {
+    for (int i = 0; i < 8; ++i)
+        if (!make_tmap_bf16(&maps->m[i], base, rows, cols, (uint32_t)(16 * (i + 1)))) return false;
+    return true;
+}
+
 size_t tc_gemm_smem_bytes() {
     // ring + barriers (512 B) + 4 epilogue staging tiles + 1024-byte alignment slack
     return (size_t)kBiasOffset + 1024;
@@ -887,9 +923,12 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The B maps of launches that are not weights-as-M (never read).
+const TokenRowMaps kNoTokenRowMaps = {};
+
 template <int kMode, bool kPair, bool kI8 = false, bool kWM = false>
 cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcGemmArgs& args,
-                       int grid, cudaStream_t s) {
+                       int grid, cudaStream_t s, const TokenRowMaps& tmBr = kNoTokenRowMaps) {
     // the router's epilogue warps also keep the logit offset in shared memory
     const size_t smem = tc_gemm_smem_bytes() + (kMode == kRouter ? 4 * kBiasWarpBytes : 0);
     auto k = grouped_gemm_tc<kMode, kPair, kI8, kWM>;
@@ -908,23 +947,23 @@ cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB, const TcG
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k, tmA, tmB, args);
+    return cudaLaunchKernelEx(&cfg, k, tmA, tmB, tmBr, args);
 }
 
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b,
-                           bool weights_m) {
+                           bool weights_m, const TokenRowMaps* wm_b) {
     if (grid <= 0) return cudaSuccess;
     if (weights_m) {
         // CTA pairs, bf16, gate/up over the whole K (the down projection may
         // be split into float32 K slices): tmA the weights (make_tmap_gate_up_wm
-        // for gate/up, 128-row boxes for down), tmB the token rows (128-row boxes)
-        if (!pair || int8_b || mode == kRouter || (mode == kGateUp && args.k_splits != 1) ||
+        // for gate/up, 128-row boxes for down), wm_b the token rows
+        if (!pair || int8_b || !wm_b || mode == kRouter || (mode == kGateUp && args.k_splits != 1) ||
             (args.y_bf16 && args.k_splits != 1))
             return cudaErrorInvalidValue;
-        const cudaError_t e = mode == kGateUp
-                                  ? launch_one<kGateUp, true, false, true>(tmA, tmB, args, grid & ~1, s)
-                                  : launch_one<kDown, true, false, true>(tmA, tmB, args, grid & ~1, s);
+        const cudaError_t e =
+            mode == kGateUp ? launch_one<kGateUp, true, false, true>(tmA, tmB, args, grid & ~1, s, *wm_b)
+                            : launch_one<kDown, true, false, true>(tmA, tmB, args, grid & ~1, s, *wm_b);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
     // bf16 Y: the down projection's rows, not K slices

@@ -56,6 +56,14 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 // The packed bf16 gate/up weights (rows = E * 2 * d_ff, d columns) as the
 // 5-D view the weights-as-M gate/up GEMM loads one CTA's A stage through.
 bool make_tmap_gate_up_wm(CUtensorMap* map, const void* wgu, uint64_t rows, uint64_t d);
+// Token-row tensor maps of Xp or H for the weights-as-M GEMMs: box heights of
+// 16, 32, ..., 128 rows (map i: 16 * (i + 1) rows), 64 columns, the layout of
+// make_tmap_bf16.  A tile whose token columns per CTA are h loads its B stage
+// through map h / 16 - 1, so a narrow tile moves only the rows its MMA reads.
+struct TokenRowMaps {
+    CUtensorMap m[8];
+};
+bool make_tmap_token_rows(TokenRowMaps* maps, const void* base, uint64_t rows, uint64_t cols);
 // pair: run the expert GEMMs on CTA pairs (256-row tiles, B tensor map with
 // 128-row boxes) instead of single CTAs (128-row tiles, 256-row B boxes).
 // int8_b: B is int8 codes (args.q_codes, tile-major, two 128-row tiles per
@@ -67,11 +75,12 @@ bool make_tmap_gate_up_wm(CUtensorMap* map, const void* wgu, uint64_t rows, uint
 // rounded up to 32, so an expert's last tile computes at most 31 padding
 // columns instead of up to 255 padding rows.  tmA: the packed weights (gate/up
 // through make_tmap_gate_up_wm: each CTA's 128 A rows are 4 x (16 gate, 16 up)
-// rows of its 64 hidden units; down with 128-row boxes), tmB: Xp or H
-// (128-row boxes).
+// rows of its 64 hidden units; down with 128-row boxes), wm_b: the token
+// rows (Xp or H) in boxes of the tile's width (make_tmap_token_rows); tmB is
+// not read.
 cudaError_t launch_tc_gemm(int mode, bool pair, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const TcGemmArgs& args, int grid, cudaStream_t s, bool int8_b = false,
-                           bool weights_m = false);
+                           bool weights_m = false, const TokenRowMaps* wm_b = nullptr);
 
 // Decode-sized expert GEMMs with the weights as the MMA's M operand
 // (gemm_dec.cu): tiles of 128 weight rows x 32 tokens of one expert (the tile

@@ -94,6 +94,7 @@ struct colibri_moe {
     bool grouped_ok = false;
     // B operands: 128-row boxes for CTA pairs, 256-row boxes for single CTAs
     CUtensorMap tm_xp, tm_wgu, tm_h, tm_wdT, tm_wr, tm_wgu1, tm_wdT1;
+    TokenRowMaps tm_xp_rows, tm_h_rows;   // B of the weights-as-M GEMMs (bf16 handles)
     CUtensorMap tm_wgu_wm;  // packed gate/up, 5-D view (weights-as-M pair GEMM)
     bool wm_gate_up = false;   // the view encoded
     // decode GEMM (weights as M): token rows in 32-row boxes (bf16 weights:
@@ -592,7 +593,8 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             st = g.done(dec    ? launch_tc_gemm_dec(kGateUp, h->tm_xp32, h->int8 ? h->tm_xp : h->tm_wgu,
                                                     a, grid, s, h->int8)
                         : pair && h->wm_gate_up && d >= kWmGateUpMinK
-                            ? launch_tc_gemm(kGateUp, true, h->tm_wgu_wm, h->tm_xp, a, grid, s, false, true)
+                            ? launch_tc_gemm(kGateUp, true, h->tm_wgu_wm, h->tm_xp, a, grid, s, false, true,
+                                             &h->tm_xp_rows)
                         : pair ? launch_tc_gemm(kGateUp, true, h->tm_xp, h->tm_wgu, a, grid, s)
                                : launch_tc_gemm(kGateUp, false, h->tm_xp, h->tm_wgu1, a, grid, s,
                                                 h->int8),
@@ -630,7 +632,7 @@ colibri_status_t run_layer(colibri_moe_t* h, const void* x, int T, void* y, cons
             st = g.done(dec    ? launch_tc_gemm_dec(kDown, h->tm_h32, h->int8 ? h->tm_h : h->tm_wdT, a,
                                                     grid, s, h->int8)
                         : pair ? launch_tc_gemm(kDown, true, h->tm_wdT, h->tm_h, a, grid, s, false,
-                                                true)
+                                                true, &h->tm_h_rows)
                                : launch_tc_gemm(kDown, false, h->tm_h, h->tm_wdT1, a, grid, s,
                                                 h->int8),
                         1);
@@ -894,7 +896,8 @@ colibri_status_t init_impl(const colibri_moe_config_t* cfg, const void* w_router
                  make_tmap_bf16(&h->tm_wdT, h->wdT, (uint64_t)E * d, f, 128) &&
                  make_tmap_bf16(&h->tm_wgu1, h->wgu, (uint64_t)E * 2 * f, d, 256) &&
                  make_tmap_bf16(&h->tm_wdT1, h->wdT, (uint64_t)E * d, f, 256) &&
-                 true;
+                 make_tmap_token_rows(&h->tm_xp_rows, h->xp, P, d) &&
+                 make_tmap_token_rows(&h->tm_h_rows, h->H, P, f);
         // the 5-D view is optional: without it gate/up stays token-on-M
         if (ok && !int8) h->wm_gate_up = make_tmap_gate_up_wm(&h->tm_wgu_wm, h->wgu, (uint64_t)E * 2 * f, d);
         if (!ok) {
