@@ -21,6 +21,8 @@ from parity import Y_RTOL, Case
 pytestmark = pytest.mark.gpu
 
 SHAPE = synth.LayerShape("routed", 512, 1024, 8, 2, "bf16")
+# d_model 4096: gate/up as well as down run as weights-as-M CTA-pair GEMMs
+WIDE = synth.LayerShape("routed_wide", 4096, 1024, 8, 2, "bf16")
 
 
 def _routing(T, k, E, seed):
@@ -82,5 +84,28 @@ def test_out_of_range_ids_are_reported_and_add_nothing(lib, T):
         torch.cuda.synchronize()
         assert case.layer.check() == 0
         _check(case, x64, y2, idx.numpy(), w.numpy(), np.arange(T))
+    finally:
+        case.close()
+
+
+def test_weights_as_m_token_boxes_of_every_width(lib):
+    """Caller routing that gives each expert's last 256-row tile a different
+    width (17, 49, ..., 241 rows: 32, 64, ..., 256 token columns), so the
+    weights-as-M pair GEMMs load that tile's token rows through each of the
+    eight box heights (16 .. 128 rows per CTA); experts 0, 3 and 6 also get
+    a full tile first.  Every row against the oracle."""
+    counts = [32 * j + 17 + (256 if j % 3 == 0 else 0) for j in range(8)]
+    T = sum(counts)   # 1800 pairs: CTA-pair tiles (at least 128 per expert on average)
+    case = Case(WIDE, seed=41, max_tokens=T)
+    try:
+        x, x64 = case.tokens(T)
+        g = torch.Generator().manual_seed(7)
+        idx = torch.repeat_interleave(torch.arange(8, dtype=torch.int32), torch.tensor(counts))
+        idx = idx[torch.randperm(T, generator=g)].reshape(T, 1)
+        w = torch.rand((T, 1), generator=g, dtype=torch.float32) + 0.05
+        y = case.layer.forward_routed(x, idx.to(case.dev), w.to(case.dev))
+        torch.cuda.synchronize()
+        assert case.layer.check() == 0
+        _check(case, x64, y, idx.numpy(), w.numpy(), np.arange(T))
     finally:
         case.close()
